@@ -1,0 +1,171 @@
+/*
+ * q8act.h -- C ABI of libq8act.so: a GB300 (sm_103a) implementation of the Q8_0 weight x
+ * q8_1 activation block-quantized matmul of an LLM decoder.
+ *
+ * The operation, with the notation used throughout:
+ *   W   Q8_0 weights, n rows ("out_f") of k/32 blocks ("in_f" = k).  A block is 34 bytes:
+ *       a little-endian IEEE binary16 scale d_w at byte 0, then 32 int8 quants wq at bytes
+ *       2..33.  Row r occupies bytes [r*row_bytes, (r+1)*row_bytes), row_bytes = k/32*34.
+ *       (memra-engine 0.124.1 accprobe_bench.rs, synth_w_q8_0; memra-engine 0.113.0
+ *       decode_kernel_census.rs, fn q8: row_bytes = in_f/32*(32+2).)
+ *   x   f32 activations, m tokens x k, row-major.
+ *   q8_1 quantization of x, per token t and block b of 32 values:
+ *       amax = max|x|, d_a = amax/127 (f32, IEEE division), q = clamp(round(x/d_a), -127,
+ *       127) with round half away from zero; a block with d_a == 0 gets q = 0.
+ *       (memra-engine 0.81.0 f16_ffi.rs, try_f16_gemm / f16_act: the per-block formula
+ *       amax/127, (v/d).round().clamp(-127,127), guarded by amax > 0; decode_kernel_census.rs
+ *       fn q8: one i8 per column plus a per-32-block f32 scale.)
+ *   y   f32 output, m x n, row-major:
+ *       y[t][r] = sum_b d_w[r][b] * d_a[t][b] * D[t][r][b],
+ *       D[t][r][b] = sum_{i<32} wq[r][32b+i] * xq[t][32b+i]   (exact int32, |D| <= 516128)
+ *       with the scale fold in f32 (memra-engine 0.70.0 fp8_ffi.rs, try_fp8_gemm doc:
+ *       y[m,out] = x[m,in] @ W^T; accprobe_bench.rs module doc: the MMQ floor folds the
+ *       scales once per 32-wide k block).
+ *
+ * Conventions (as in the pages' extern "C" blocks, fp8_ffi.rs and f16_ffi.rs):
+ *   - every pointer is a DEVICE pointer unless stated otherwise; the caller owns all memory;
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); every call only enqueues
+ *     work on it and returns without synchronizing (q8act_device_status excepted);
+ *   - the return value is 0 on success, a negative Q8ACT_ERR_* code when the arguments are
+ *     refused (nothing is launched), or Q8ACT_ERR_CUDA_BASE + cudaError_t when a CUDA call
+ *     fails;
+ *   - dimensions: k must be a positive multiple of 256 (every row then starts 16-byte
+ *     aligned, which the bulk/TMA copies need); n >= 1; m as stated per call;
+ *   - alignment: every pointer must be 16-byte aligned.
+ *
+ * Kernels time out instead of hanging: a pipeline wait that exceeds about two seconds makes
+ * the kernel record an error in a device-side status word and return early.
+ * q8act_device_status() reads and clears that word.
+ */
+#ifndef Q8ACT_H
+#define Q8ACT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q8ACT_OK 0
+#define Q8ACT_ERR_NULL (-1)       /* a required pointer is NULL                        */
+#define Q8ACT_ERR_DIMS (-2)       /* m, n or k out of range                            */
+#define Q8ACT_ERR_ALIGN (-3)      /* a pointer is not 16-byte aligned                  */
+#define Q8ACT_ERR_WORKSPACE (-4)  /* workspace missing or smaller than required        */
+#define Q8ACT_ERR_DEVICE (-5)     /* current device is not an sm_103 (GB300) GPU       */
+#define Q8ACT_ERR_TIMEOUT (-6)    /* a kernel gave up waiting (see q8act_device_status) */
+#define Q8ACT_ERR_CUDA_BASE 1000  /* 1000 + cudaError_t                                */
+
+/* Largest supported k (values per row). */
+#define Q8ACT_MAX_K 65536
+/* Largest token count of the GEMV (decode m = 1 and speculative verify up to 8). */
+#define Q8ACT_GEMV_MAX_M 8
+
+/* Library version, major*10000 + minor*100 + patch. */
+int q8act_version(void);
+
+/* Human-readable text for a return code (static storage, never NULL). */
+const char *q8act_strerror(int rc);
+
+/*
+ * q8_1 activation quantizer (the decode-side activation form of decode_kernel_census.rs
+ * fn q8: aq = one int8 per column, ad = per-32-block f32 scale).
+ *   x   [m][k] f32 (input)          xq [m][k] int8 (output)      xd [m][k/32] f32 (output)
+ *   m >= 1.  Bit-exact to the formula above (IEEE division, round half away from zero).
+ */
+int q8act_quantize_q8_1(const float *x, int8_t *xq, float *xd, int64_t m, int64_t k,
+                        void *stream);
+
+/*
+ * q8_1 activation quantizer, MMQ (GEMM operand) layout.  Same quants and scales as
+ * q8act_quantize_q8_1, laid out for the tensor-core GEMM, playing the role of the pages'
+ * block_q8_1_mmq activation stream (accprobe_bench.rs, synth_act_q8_1):
+ *   xqh [m][k] uint16: each quant stored as the IEEE binary16 encoding of the same integer
+ *       (exact: |q| <= 127), the operand format of the f16 tensor-core pipe;
+ *   xdt [k/32][ldm] f32: the scales transposed (block-major), ldm = q8act_mmq_ldm(m).
+ */
+int q8act_quantize_q8_1_mmq(const float *x, uint16_t *xqh, float *xdt, int64_t m, int64_t k,
+                            void *stream);
+
+/* Leading dimension (in floats) of the transposed scale array of the MMQ layout: m rounded
+   up to a multiple of 4.  Returns 0 when m < 1. */
+int64_t q8act_mmq_ldm(int64_t m);
+
+/*
+ * Q8_0 weight quantizer (load-time data preparation, the writer of the block format of
+ * accprobe_bench.rs synth_w_q8_0):
+ *   w  [n][k] f32 (input)      wq  n*k/32*34 bytes (output, Q8_0 blocks)
+ *   per block: d = amax/127 (f32), quants q = clamp(round(w/d), -127, 127) computed with
+ *   the f32 d, stored scale = binary16(d) rounded to nearest even; d == 0 gives q = 0.
+ */
+int q8act_quantize_q8_0(const float *w, void *wq, int64_t n, int64_t k, void *stream);
+
+/*
+ * Q8_0 x q8_1 GEMV, the decode ("mmvq") regime: Engine::qmatvec_mmvq_into in
+ * decode_kernel_census.rs fn q8 (weights w, pre-quantized activation aq/ad, m tokens).
+ *   w [n rows of Q8_0 blocks], xq [m][k] int8, xd [m][k/32] f32, y [m][n] f32 (overwritten)
+ *   1 <= m <= Q8ACT_GEMV_MAX_M.  The result for token t does not depend on m (the same
+ *   operations in the same order for every m: the pages' decode == verify law,
+ *   fp8_ffi.rs module doc and f16_ffi.rs module doc).
+ */
+int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m,
+                    int64_t n, int64_t k, void *stream);
+
+/*
+ * Workspace bytes q8act_gemm_q8_0 needs for an m x k activation (the MMQ-layout quants
+ * and scales).  Returns 0 when the dimensions are invalid (as memra_fp8_blk_q8_0_bytes in
+ * fp8_ffi.rs returns 0 on bad dims).
+ */
+size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k);
+
+/*
+ * Q8_0 x q8_1 GEMM, the prefill ("MMQ") regime, activation quantization fused into the call
+ * (fp8_ffi.rs memra_fp8_pp_gemm: one C-ABI call, quantize + GEMM on one stream, caller-owned
+ * workspace):
+ *   w [n rows of Q8_0 blocks], x [m][k] f32, y [m][n] f32 (overwritten),
+ *   ws: device workspace of at least q8act_gemm_workspace_bytes(m, k) bytes.
+ *   m >= 1 (the pages route m >= 16 here; smaller m is accepted).
+ */
+int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k,
+                    void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The GEMM on an activation already quantized by q8act_quantize_q8_1_mmq, so that one
+ * quantization feeds several GEMMs (f16_ffi.rs f16_act / try_f16_gemm_pre: "ONE convert
+ * feeds every ... weight in the group").
+ *   xqh [m][k] binary16 quants, xdt [k/32][q8act_mmq_ldm(m)] f32 scales.
+ */
+int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, float *y,
+                         int64_t m, int64_t n, int64_t k, void *stream);
+
+/*
+ * Q8_0 -> row-major binary16 dequant (f16_ffi.rs memra_q8_0_dequant_f16, which takes out_f
+ * and blocks per row; this call takes k = 32 * blocks per row):
+ *   w [n rows of Q8_0 blocks] -> w16 [n][k] binary16, w16 = fp16_rn(f32(d_w) * q).
+ *   The int8 part is exact in fp16; the only rounding is that of the product (f16_ffi.rs
+ *   module doc, "NUMERIC CONFIG").
+ */
+int q8act_dequant_q8_0_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
+
+/*
+ * Test hooks: export the exact per-block integer dots D[t][r][b] (int32, [m][n][k/32]) as
+ * computed by the block-dot stage of the GEMV (its int8 dot-product path; 1 <= m <= 8) or of
+ * the GEMM (its tensor-core path; m >= 1, activation in the MMQ layout).  The fold is
+ * replaced by a store of D; everything before it is the production code path.
+ */
+int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m,
+                                int64_t n, int64_t k, void *stream);
+int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, int64_t m,
+                                int64_t n, int64_t k, void *stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device-side status word that kernels set
+ * when a pipeline wait times out.  Returns Q8ACT_OK, Q8ACT_ERR_TIMEOUT, or a CUDA error code.
+ */
+int q8act_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8ACT_H */

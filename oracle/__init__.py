@@ -1,0 +1,208 @@
+"""CPU oracle for the Q8_0 x q8_1 block-quantized matmul -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package.  The product library never calls it, and this package never
+imports the product library: the two share no code.
+
+The arithmetic lives in ``q8_oracle.c`` (plain C, single-threaded, compiled with
+``-ffp-contract=off`` so every f32 operation is rounded on its own).  This module builds
+it with gcc and exposes numpy-facing wrappers:
+
+    f32_to_f16, f16_to_f32            O0  IEEE binary16 conversions (round to nearest even)
+    quantize_q8_0(w)                  O1  f32 [n,k] -> Q8_0 bytes [n, k/32*34]
+    quantize_q8_1(x)                  O2  f32 [m,k] -> (int8 [m,k], f32 [m,k/32])
+    block_dots(w, xq, k, rows=None)   O3  exact int32 D[t, r, b]
+    matmul(w, xq, xd, k, rows=None)   O4  (y32, y64, S) with S = sum_b |d_w d_a D|
+    dequant_f16(w, k)                 O5  Q8_0 -> fp16 bits [n, k]
+
+Each C function cites the page passage it follows (memra-engine docs.rs pages:
+accprobe_bench.rs, decode_kernel_census.rs, f16_ffi.rs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libq8oracle.so")
+_LOCK = threading.Lock()
+_LIB = None
+
+QK = 32
+Q8_0_BYTES = 34
+
+
+def build(force: bool = False) -> str:
+    """Compile q8_oracle.c into a shared library (idempotent); returns its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    lib.oracle_f32_to_f16_array.argtypes = [P, P, I64]
+    lib.oracle_f16_to_f32_array.argtypes = [P, P, I64]
+    lib.oracle_quantize_q8_1.argtypes = [P, P, P, I64, I64]
+    lib.oracle_quantize_q8_0.argtypes = [P, P, I64, I64]
+    lib.oracle_block_dots.argtypes = [P, P, P, I64, I64, I64, P, I64]
+    lib.oracle_matmul.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P, P]
+    lib.oracle_dequant_f16.argtypes = [P, P, I64, I64]
+    for name in ("oracle_f32_to_f16_array", "oracle_f16_to_f32_array",
+                 "oracle_quantize_q8_1", "oracle_quantize_q8_0", "oracle_block_dots",
+                 "oracle_matmul", "oracle_dequant_f16"):
+        getattr(lib, name).restype = None
+    return lib
+
+
+def _lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            _LIB = _bind(ctypes.CDLL(build()))
+    return _LIB
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _check_k(k: int) -> None:
+    if k <= 0 or k % QK:
+        raise ValueError(f"k must be a positive multiple of {QK}, got {k}")
+
+
+class Oracle:
+    """The oracle's functions bound to one compiled copy of the C source.
+
+    The module-level functions use the copy built from ``q8_oracle.c``; the test-suite
+    also wraps deliberately broken copies (planted mistakes) to show that its pins catch
+    them.
+    """
+
+    def __init__(self, lib_path: str | None = None):
+        self._path = lib_path
+
+    def lib(self):
+        if self._path is None:
+            return _lib()
+        if not hasattr(self, "_l"):
+            self._l = _bind(ctypes.CDLL(self._path))
+        return self._l
+
+
+def f32_to_f16(x, _o: Oracle | None = None) -> np.ndarray:
+    """Element-wise binary32 -> binary16 bits (uint16), round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    (_o or _DEFAULT).lib().oracle_f32_to_f16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def f16_to_f32(h, _o: Oracle | None = None) -> np.ndarray:
+    """Element-wise binary16 bits (uint16) -> binary32."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    (_o or _DEFAULT).lib().oracle_f16_to_f32_array(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def quantize_q8_0(w: np.ndarray, _o: Oracle | None = None) -> np.ndarray:
+    """O1: f32 weights [n, k] -> Q8_0 bytes uint8 [n, k/32*34]."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    _check_k(k)
+    out = np.empty((n, k // QK * Q8_0_BYTES), dtype=np.uint8)
+    (_o or _DEFAULT).lib().oracle_quantize_q8_0(_ptr(w), _ptr(out), n, k)
+    return out
+
+
+def quantize_q8_1(x: np.ndarray, _o: Oracle | None = None):
+    """O2: f32 activations [m, k] -> (xq int8 [m, k], xd f32 [m, k/32])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    m, k = x.shape
+    _check_k(k)
+    xq = np.empty((m, k), dtype=np.int8)
+    xd = np.empty((m, k // QK), dtype=np.float32)
+    (_o or _DEFAULT).lib().oracle_quantize_q8_1(_ptr(x), _ptr(xq), _ptr(xd), m, k)
+    return xq, xd
+
+
+def _rows_arg(rows, n):
+    if rows is None:
+        return None, n
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    if rows.size and (rows.min() < 0 or rows.max() >= n):
+        raise ValueError("row index out of range")
+    return rows, rows.size
+
+
+def block_dots(w: np.ndarray, xq: np.ndarray, k: int, rows=None, _o: Oracle | None = None) -> np.ndarray:
+    """O3: exact int32 block dots D[t, j, b] for weight rows ``rows`` (default: all)."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    n = w.size // (k // QK * Q8_0_BYTES)
+    m = xq.size // k
+    rows, nr = _rows_arg(rows, n)
+    D = np.empty((m, nr, k // QK), dtype=np.int32)
+    (_o or _DEFAULT).lib().oracle_block_dots(_ptr(w), _ptr(xq), _ptr(D), m, n, k, _ptr(rows), nr)
+    return D
+
+
+def matmul(w: np.ndarray, xq: np.ndarray, xd: np.ndarray, k: int, rows=None, _o: Oracle | None = None):
+    """O4: returns (y32 f32 [m, nr], y64 f64 [m, nr], S f64 [m, nr])."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xd = np.ascontiguousarray(xd, dtype=np.float32)
+    n = w.size // (k // QK * Q8_0_BYTES)
+    m = xq.size // k
+    rows, nr = _rows_arg(rows, n)
+    y32 = np.empty((m, nr), dtype=np.float32)
+    y64 = np.empty((m, nr), dtype=np.float64)
+    S = np.empty((m, nr), dtype=np.float64)
+    (_o or _DEFAULT).lib().oracle_matmul(_ptr(w), _ptr(xq), _ptr(xd), m, n, k, _ptr(rows), nr,
+                         _ptr(y32), _ptr(y64), _ptr(S))
+    return y32, y64, S
+
+
+def dequant_f16(w: np.ndarray, k: int, _o: Oracle | None = None) -> np.ndarray:
+    """O5: Q8_0 bytes -> fp16 bits uint16 [n, k]."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    n = w.size // (k // QK * Q8_0_BYTES)
+    out = np.empty((n, k), dtype=np.uint16)
+    (_o or _DEFAULT).lib().oracle_dequant_f16(_ptr(w), _ptr(out), n, k)
+    return out
+
+
+_DEFAULT = Oracle()
+
+_PUBLIC = ("f32_to_f16", "f16_to_f32", "quantize_q8_0", "quantize_q8_1", "block_dots",
+           "matmul", "dequant_f16")
+
+
+def bound(o: Oracle):
+    """A namespace with the public functions bound to the compiled copy ``o``."""
+    import types
+    import functools
+    g = globals()
+    return types.SimpleNamespace(**{n: functools.partial(g[n], _o=o) for n in _PUBLIC})

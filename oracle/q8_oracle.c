@@ -1,0 +1,263 @@
+/*
+ * q8_oracle.c -- plain, slow, single-threaded CPU oracle for the Q8_0 weight x q8_1
+ * activation block-quantized matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or calls
+ * this file; only the test-suite, the smoke check and the benchmark's CPU-baseline leg
+ * load it (through oracle/__init__.py).  It shares no code, header, table or constant
+ * generator with the CUDA path.
+ *
+ * Sources (docs.rs pages of the memra-engine crate):
+ *   [accprobe]  memra-engine 0.124.1, src/bin/accprobe_bench.rs
+ *               - synth_w_q8_0: a Q8_0 row is in_f/32 blocks of 34 bytes, an fp16 scale
+ *                 at +0 (little endian) followed by 32 int8 quants;
+ *               - f32_to_f16_bits: binary16 with round-to-nearest-even;
+ *               - module doc: the MMQ floor "folds every k32" (one scale fold per block).
+ *   [census]    memra-engine 0.113.0, src/bin/decode_kernel_census.rs, fn q8:
+ *               row_bytes = in_f/32*(32+2); q8_1 activation = one i8 per column plus a
+ *               per-32-block f32 scale; bytes streamed = out_f*row_bytes.
+ *   [f16_ffi]   memra-engine 0.81.0, src/memra_engine/f16_ffi.rs
+ *               - module doc, "NUMERIC CONFIG": the int8 part of the dequant is exact in
+ *                 fp16, rounding enters at the d*q products;
+ *               - try_f16_gemm / f16_act / build_q8_f16 (W8A8 pilot): amax = max |v|;
+ *                 if amax > 0 { d = amax/127; q = (v/d).round().clamp(-127, 127) }.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - the quantizer divides by the f32 scale d = amax/127 with IEEE division and rounds
+ *     half away from zero (Rust f32::round); a block whose d is 0 gets all-zero quants;
+ *   - the Q8_0 weight quantizer divides by the f32 d and stores fp16(d) (round to
+ *     nearest even);
+ *   - the fold is y = sum over blocks, in ascending block order, of
+ *     (f32(d_w) * d_a) * f32(D) with f32 rounding after every operation (y32), and the
+ *     same sum with double products and accumulation (y64, the reference value).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ * -ffp-contract=off keeps every f32 multiply and add separately rounded.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define QK 32           /* values per block                                   */
+#define Q8_0_BYTES 34   /* fp16 scale + 32 int8 quants, [accprobe] synth_w_q8_0 */
+
+/* ------------------------------------------------------------------------------------ */
+/* O0: IEEE-754 binary16 <-> binary32, written from the format definition.               */
+/*   binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.                  */
+/*   normal    value = (1024 + f) * 2^(e - 25), e in 1..30                               */
+/*   subnormal value = f * 2^-24                                                         */
+/* ------------------------------------------------------------------------------------ */
+
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = h >> 15;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)f, -24);
+    else if (e == 31)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexpf((float)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+/* Round-to-nearest, ties-to-even, with gradual underflow and overflow to infinity. */
+uint16_t oracle_f32_to_f16(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, sizeof b);
+    uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
+    uint32_t ebits = (b >> 23) & 0xffu;
+    uint32_t frac = b & 0x7fffffu;
+
+    if (ebits == 0xffu)                         /* inf / NaN */
+        return frac ? (uint16_t)(sign | 0x7e00u) : (uint16_t)(sign | 0x7c00u);
+    if (ebits == 0)                             /* f32 zero or subnormal: < 2^-126 */
+        return sign;                            /* far below half of 2^-24        */
+
+    /* |x| = sig * 2^(e - 23), sig in [2^23, 2^24) */
+    int e = (int)ebits - 127;
+    uint32_t sig = frac | 0x800000u;
+    if (e > 15)
+        return (uint16_t)(sign | 0x7c00u);      /* |x| >= 2^16 > max finite */
+
+    /* Number of low bits of sig to drop: 13 for normal binary16 results; more when the
+       result is subnormal (unit 2^-24). */
+    int shift = (e >= -14) ? 13 : (-1 - e);
+    if (shift > 24)
+        return sign;                            /* |x| < 2^-25: rounds to zero */
+    uint32_t q = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (q & 1u)))
+        q += 1u;
+
+    uint32_t enc;
+    if (e >= -14)
+        enc = ((uint32_t)(e + 14) << 10) + q;   /* q carries the implicit 1024; a carry
+                                                   to 2048 bumps the exponent, and
+                                                   0x7c00 is infinity */
+    else
+        enc = q;                                /* q == 1024 is the smallest normal */
+    if (enc > 0x7c00u)
+        enc = 0x7c00u;
+    return (uint16_t)(sign | enc);
+}
+
+/* Array forms of the two conversions (one call instead of one per element). */
+void oracle_f32_to_f16_array(const float *x, uint16_t *h, int64_t count)
+{
+    for (int64_t i = 0; i < count; i++)
+        h[i] = oracle_f32_to_f16(x[i]);
+}
+
+void oracle_f16_to_f32_array(const uint16_t *h, float *x, int64_t count)
+{
+    for (int64_t i = 0; i < count; i++)
+        x[i] = oracle_f16_to_f32(h[i]);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Per-block scalar quantization, [f16_ffi] W8A8 pilot:                                   */
+/*   amax = max |v|;  d = amax / 127;  q = clamp(round_half_away(v / d), -127, 127).      */
+/* Returns d; writes 32 quants.                                                          */
+/* ------------------------------------------------------------------------------------ */
+static float quantize_block(const float *v, int8_t *q)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < QK; i++) {
+        float a = fabsf(v[i]);
+        if (a > amax)
+            amax = a;
+    }
+    float d = amax / 127.0f;
+    for (int i = 0; i < QK; i++) {
+        if (d == 0.0f) {
+            q[i] = 0;
+            continue;
+        }
+        float r = roundf(v[i] / d);
+        if (r > 127.0f)
+            r = 127.0f;
+        if (r < -127.0f)
+            r = -127.0f;
+        q[i] = (int8_t)r;
+    }
+    return d;
+}
+
+/* O2: q8_1 activation quantization, [census] fn q8 (one i8 per column plus a per-32-block
+   f32 scale).  x is [m][k] row-major; xq is [m][k]; xd is [m][k/32]. */
+void oracle_quantize_q8_1(const float *x, int8_t *xq, float *xd, int64_t m, int64_t k)
+{
+    int64_t nb = k / QK;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t b = 0; b < nb; b++)
+            xd[t * nb + b] = quantize_block(x + t * k + b * QK, xq + t * k + b * QK);
+}
+
+/* O1: Q8_0 weight quantization (data preparation).  w is [n][k] row-major; out holds n
+   rows of k/32 blocks of 34 bytes: fp16(d) little endian, then 32 int8 quants. */
+void oracle_quantize_q8_0(const float *w, uint8_t *out, int64_t n, int64_t k)
+{
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            uint8_t *blk = out + (r * nb + b) * Q8_0_BYTES;
+            int8_t q[QK];
+            float d = quantize_block(w + r * k + b * QK, q);
+            uint16_t h = oracle_f32_to_f16(d);
+            blk[0] = (uint8_t)(h & 0xff);
+            blk[1] = (uint8_t)(h >> 8);
+            memcpy(blk + 2, q, QK);
+        }
+}
+
+static const uint8_t *block_ptr(const uint8_t *w, int64_t r, int64_t b, int64_t nb)
+{
+    return w + (r * nb + b) * Q8_0_BYTES;
+}
+
+static float block_scale(const uint8_t *blk)
+{
+    return oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+}
+
+static int32_t block_dot(const uint8_t *blk, const int8_t *xq)
+{
+    const int8_t *wq = (const int8_t *)(blk + 2);
+    int32_t s = 0;
+    for (int i = 0; i < QK; i++)
+        s += (int32_t)wq[i] * (int32_t)xq[i];
+    return s;
+}
+
+/* O3: exact per-block integer dots D[t][j][b] = sum_i wq[r_j, 32b+i] * xq[t, 32b+i]
+   for the selected weight rows r_j = rows[j] (all rows when rows == NULL). */
+void oracle_block_dots(const uint8_t *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n,
+                       int64_t k, const int64_t *rows, int64_t nrows)
+{
+    int64_t nb = k / QK;
+    int64_t nr = rows ? nrows : n;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t j = 0; j < nr; j++) {
+            int64_t r = rows ? rows[j] : j;
+            for (int64_t b = 0; b < nb; b++)
+                D[(t * nr + j) * nb + b] = block_dot(block_ptr(w, r, b, nb), xq + t * k + b * QK);
+        }
+}
+
+/* O4: the fold.  For each token t and selected weight row r_j:
+     y32[t][j] = sum_b (f32(d_w[r,b]) * d_a[t,b]) * f32(D)   (f32, ascending b)
+     y64[t][j] = sum_b  d_w * d_a * D                          (double)
+     S[t][j]   = sum_b |d_w * d_a * D|                         (double; error scale)
+   Any output pointer may be NULL. */
+void oracle_matmul(const uint8_t *w, const int8_t *xq, const float *xd, int64_t m, int64_t n,
+                   int64_t k, const int64_t *rows, int64_t nrows, float *y32, double *y64,
+                   double *S)
+{
+    int64_t nb = k / QK;
+    int64_t nr = rows ? nrows : n;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t j = 0; j < nr; j++) {
+            int64_t r = rows ? rows[j] : j;
+            float acc32 = 0.0f;
+            double acc64 = 0.0, abs64 = 0.0;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *blk = block_ptr(w, r, b, nb);
+                int32_t dot = block_dot(blk, xq + t * k + b * QK);
+                float dw = block_scale(blk);
+                float da = xd[t * nb + b];
+                float s = dw * da;
+                float term = s * (float)dot;
+                acc32 = acc32 + term;
+                double term64 = (double)dw * (double)da * (double)dot;
+                acc64 += term64;
+                abs64 += fabs(term64);
+            }
+            if (y32)
+                y32[t * nr + j] = acc32;
+            if (y64)
+                y64[t * nr + j] = acc64;
+            if (S)
+                S[t * nr + j] = abs64;
+        }
+}
+
+/* O5: Q8_0 -> fp16 row-major dequant, [f16_ffi] memra_q8_0_dequant_f16:
+   w16[r][32b+i] = fp16_rn(f32(d_w) * q).  The f32 product of an 11-bit significand and
+   a 7-bit integer is exact, so this is the correctly rounded fp16 of the exact product. */
+void oracle_dequant_f16(const uint8_t *w, uint16_t *out, int64_t n, int64_t k)
+{
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = block_ptr(w, r, b, nb);
+            float dw = block_scale(blk);
+            const int8_t *wq = (const int8_t *)(blk + 2);
+            for (int i = 0; i < QK; i++)
+                out[r * k + b * QK + i] = oracle_f32_to_f16(dw * (float)wq[i]);
+        }
+}

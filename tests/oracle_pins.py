@@ -1,0 +1,272 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes a namespace with the oracle's public functions (the real
+oracle, or a copy with a planted mistake) and raises AssertionError when the oracle
+disagrees with what the pages or the mathematics fix:
+
+  * hand-derived worked cases under tests/golden/ (each cites its page);
+  * independent libraries: numpy's binary16 conversion, numpy int64 / float64 matmuls;
+  * closed forms and invariants of the quantizer (range, amax -> +-127, odd symmetry,
+    power-of-two scaling, zero blocks, re-quantization idempotence);
+  * brute force on tiny inputs: the block fold equals the plain float64 dot product of
+    the dequantized operands (sum_b d_w d_a D_b = sum_i (d_w q_w,i)(d_a q_a,i)).
+
+Nothing here calls the CUDA library.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+QK = 32
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def parse_q8_0(wb: np.ndarray, n: int, k: int):
+    """Decode Q8_0 bytes with numpy alone: (d_w float64 [n, k/32], q int64 [n, k/32, 32])."""
+    nb = k // QK
+    blocks = np.ascontiguousarray(wb).reshape(n, nb, 34)
+    d = np.ascontiguousarray(blocks[:, :, 0:2]).view("<f2").reshape(n, nb).astype(np.float64)
+    q = np.ascontiguousarray(blocks[:, :, 2:]).view(np.int8).astype(np.int64)
+    return d, q
+
+
+def _block(entries: dict) -> np.ndarray:
+    v = np.zeros(QK, dtype=np.float32)
+    for i, val in entries.items():
+        v[int(i)] = np.float32(val)
+    return v
+
+
+def _rand_blocks(rng, rows, k, lo=-40, hi=40):
+    """Blocks whose magnitudes span binades 2^lo..2^hi (all f32 scales stay normal)."""
+    x = rng.standard_normal((rows, k)).astype(np.float32)
+    scale = np.exp2(rng.integers(lo, hi, size=(rows, k // QK))).astype(np.float32)
+    x *= np.repeat(scale, QK, axis=1)
+    # a few exact ties and a few zero blocks
+    x[0, :QK] = np.arange(QK, dtype=np.float32) - 15.5
+    if rows > 1:
+        x[1, QK:2 * QK] = 0.0 if k >= 2 * QK else x[1, QK:2 * QK]
+    return x
+
+
+# ---------------------------------------------------------------------------------------
+# O0: binary16 conversions
+# ---------------------------------------------------------------------------------------
+def pin_f16_decode_exhaustive(o):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = o.f16_to_f32(bits)
+    ref = bits.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    # and every finite value survives the round trip
+    back = o.f32_to_f16(got[~nan])
+    assert np.array_equal(back, bits[~nan])
+
+
+def pin_f16_encode_vs_numpy(o, n_random=1 << 20, seed=7):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    raw = rng.integers(0, 1 << 32, size=n_random, dtype=np.uint64).astype(np.uint32)
+    x = raw.view(np.float32)
+    # every midpoint between adjacent finite binary16 values, and its f32 neighbours
+    h = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mid = ((h[:-1] + h[1:]) / 2).astype(np.float32)
+    near = np.concatenate([mid, np.nextafter(mid, np.float32(np.inf)),
+                           np.nextafter(mid, np.float32(0))])
+    x = np.concatenate([x, near, -near]).astype(np.float32)
+    x = x[~np.isnan(x)]
+    got = o.f32_to_f16(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, f"{bad.size} mismatches, first x={x[bad[0]]!r}"
+
+
+def pin_f16_golden(o):
+    g = _golden("f16_conversions.json")
+    xs = np.array([float(c["f32"]) for c in g["cases"]], dtype=np.float32)
+    want = np.array([int(c["f16"], 16) for c in g["cases"]], dtype=np.uint16)
+    got = o.f32_to_f16(xs)
+    for c, gv, wv in zip(g["cases"], got, want):
+        assert gv == wv, f"{c['f32']}: got {gv:#06x}, want {wv:#06x} ({c['why']})"
+
+
+# ---------------------------------------------------------------------------------------
+# O1 / O2: quantizers
+# ---------------------------------------------------------------------------------------
+def pin_q8_1_golden(o):
+    g = _golden("q8_1_worked_cases.json")
+    x = np.stack([_block(c["x"]) for c in g["cases"]]).reshape(1, -1)
+    xq, xd = o.quantize_q8_1(x)
+    for j, c in enumerate(g["cases"]):
+        want_q = np.zeros(QK, dtype=np.int8)
+        for i, v in c["q"].items():
+            want_q[int(i)] = v
+        assert xd[0, j] == np.float32(c["d"]), f"{c['name']}: d={xd[0, j]!r} ({c['why']})"
+        assert np.array_equal(xq[0, j * QK:(j + 1) * QK], want_q), f"{c['name']}: {c['why']}"
+
+
+def pin_q8_0_layout_golden(o):
+    g = _golden("q8_0_block_layout.json")
+    k = g["k"]
+    w = np.zeros((1, k), dtype=np.float32)
+    for i, v in g["row"].items():
+        w[0, int(i)] = v
+    got = o.quantize_q8_0(w)
+    assert got.shape == (1, k // QK * 34)
+    assert got.tobytes().hex() == g["bytes_hex"], g["why"]
+
+
+def _check_quant_block_invariants(x, xq, d):
+    """x [rows, k] f32, xq [rows, k] int, d [rows, k/32] f32 (the f32 scale used)."""
+    rows, k = x.shape
+    nb = k // QK
+    xb = x.reshape(rows, nb, QK)
+    qb = xq.reshape(rows, nb, QK).astype(np.int64)
+    amax = np.abs(xb).max(axis=2)
+    assert np.all(np.abs(qb) <= 127)
+    nz = amax > 0
+    assert np.all(np.abs(qb).max(axis=2)[nz] == 127), "a nonzero block must reach +-127"
+    # the entry holding the block amax maps to +-127 with its own sign
+    idx = np.abs(xb).argmax(axis=2)
+    top_q = np.take_along_axis(qb, idx[..., None], axis=2)[..., 0]
+    top_x = np.take_along_axis(xb, idx[..., None], axis=2)[..., 0]
+    assert np.all(top_q[nz] == np.where(top_x[nz] > 0, 127, -127))
+    assert np.all(qb[~nz] == 0) and np.all(d[~nz] == 0)
+    assert np.all(np.isfinite(d))
+    # d = amax / 127 up to one rounding (both are f32)
+    rel = np.abs(d[nz].astype(np.float64) * 127 - amax[nz]) / amax[nz]
+    assert np.all(rel <= 2.0 ** -23)
+    # each quant is within half a step of x/d, measured in float64
+    ratio = xb.astype(np.float64) / np.where(d > 0, d, 1)[..., None]
+    err = np.abs(ratio - qb)[nz]
+    assert np.all(err <= 0.5 + 1e-5), f"max |x/d - q| = {err.max()}"
+
+
+def pin_quant_invariants(o, seed=3):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for k in (32, 256, 1280):
+        x = _rand_blocks(rng, 17, k)
+        xq, xd = o.quantize_q8_1(x)
+        _check_quant_block_invariants(x, xq, xd)
+        # odd symmetry (fails for floor(x + 0.5) style rounding)
+        nq, nd = o.quantize_q8_1(-x)
+        assert np.array_equal(nq, -xq) and np.array_equal(nd, xd)
+        # power-of-two scaling is exact in binary floating point
+        for s in (-9, 1, 13):
+            sq, sd = o.quantize_q8_1(x * np.float32(2.0 ** s))
+            assert np.array_equal(sq, xq)
+            assert np.array_equal(sd, xd * np.float32(2.0 ** s))
+        # Q8_0 weights: same quants (computed with the f32 d), scale stored as binary16
+        wb = o.quantize_q8_0(x)
+        dh, wq = parse_q8_0(wb, x.shape[0], k)
+        assert np.array_equal(wq.reshape(x.shape[0], k), xq.astype(np.int64))
+        want_h = xd.astype(np.float16).view(np.uint16)
+        got_h = np.ascontiguousarray(wb.reshape(x.shape[0], k // QK, 34)[:, :, 0:2]).view("<u2")
+        assert np.array_equal(got_h.reshape(want_h.shape), want_h)
+
+
+def pin_requant_idempotent(o, seed=4):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k = 512
+    x = _rand_blocks(rng, 9, k)
+    xq, xd = o.quantize_q8_1(x)
+    back = (np.repeat(xd, QK, axis=1) * xq.astype(np.float32)).astype(np.float32)
+    q2, d2 = o.quantize_q8_1(back)
+    assert np.array_equal(q2, xq)
+    ulp = np.spacing(xd)
+    assert np.all(np.abs(d2 - xd) <= ulp)
+    # Q8_0: with the binary16 scale the dequantized block re-quantizes to the same bytes
+    # (scales kept inside the binary16 range so that no scale rounds to 0 or infinity)
+    x = _rand_blocks(rng, 9, k, lo=-6, hi=6)
+    wb = o.quantize_q8_0(x)
+    dh, wq = parse_q8_0(wb, x.shape[0], k)
+    deq = (np.repeat(dh.astype(np.float32), QK, axis=1) * wq.reshape(x.shape[0], k).astype(np.float32))
+    assert np.array_equal(o.quantize_q8_0(deq.astype(np.float32)), wb)
+
+
+# ---------------------------------------------------------------------------------------
+# O3 / O4: block dots and the fold, by brute force
+# ---------------------------------------------------------------------------------------
+def _tiny_problem(rng, m, n, k, o):
+    w = rng.standard_normal((n, k)).astype(np.float32) * np.float32(0.02)
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    x *= np.exp2(rng.integers(-6, 6, size=(m, 1))).astype(np.float32)
+    wb = o.quantize_q8_0(w)
+    xq, xd = o.quantize_q8_1(x)
+    return wb, xq, xd
+
+
+def pin_block_dots_bruteforce(o, seed=5):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for (m, n, k) in ((1, 3, 32), (3, 5, 64), (4, 8, 256), (2, 7, 96)):
+        wb, xq, xd = _tiny_problem(rng, m, n, k, o)
+        _, wq = parse_q8_0(wb, n, k)
+        aq = xq.reshape(m, k // QK, QK).astype(np.int64)
+        ref = np.einsum("rbi,tbi->trb", wq, aq)
+        got = o.block_dots(wb, xq, k)
+        assert got.shape == (m, n, k // QK)
+        assert np.array_equal(got.astype(np.int64), ref)
+        rows = np.array([n - 1, 0, n // 2], dtype=np.int64)
+        assert np.array_equal(o.block_dots(wb, xq, k, rows=rows).astype(np.int64), ref[:, rows])
+
+
+def pin_fold_bruteforce(o, seed=6):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for (m, n, k) in ((1, 3, 32), (3, 5, 64), (4, 8, 256), (2, 6, 4096)):
+        wb, xq, xd = _tiny_problem(rng, m, n, k, o)
+        dw, wq = parse_q8_0(wb, n, k)
+        Wd = (dw[:, :, None] * wq).reshape(n, k)                     # exact in float64
+        Xd = (xd.astype(np.float64)[:, :, None]
+              * xq.reshape(m, k // QK, QK).astype(np.float64)).reshape(m, k)
+        ref = Xd @ Wd.T                                              # [m, n]
+        absref = np.abs((Xd[:, None, :] * Wd[None, :, :]).reshape(m, n, k // QK, QK)
+                        .sum(axis=3)).sum(axis=2)
+        y32, y64, S = o.matmul(wb, xq, xd, k)
+        assert np.allclose(S, absref, rtol=1e-12, atol=0)
+        assert np.all(np.abs(y64 - ref) <= 1e-12 * S + 1e-300)
+        # the f32 fold stays inside the error bound the tolerance is built on
+        nb = k // QK
+        bound = (nb + 2) * 2.0 ** -24 * S
+        assert np.all(np.abs(y32.astype(np.float64) - ref) <= bound + 1e-300)
+        rows = np.array([n - 1, 0], dtype=np.int64)
+        sy32, sy64, sS = o.matmul(wb, xq, xd, k, rows=rows)
+        assert np.array_equal(sy32, y32[:, rows]) and np.array_equal(sy64, y64[:, rows])
+
+
+# ---------------------------------------------------------------------------------------
+# O5: fp16 dequant
+# ---------------------------------------------------------------------------------------
+def pin_dequant_vs_numpy(o, seed=8):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n, k = 13, 512
+    w = _rand_blocks(rng, n, k, lo=-16, hi=6)
+    wb = o.quantize_q8_0(w)
+    dw, wq = parse_q8_0(wb, n, k)
+    prod = (dw.astype(np.float32)[:, :, None] * wq.astype(np.float32)).reshape(n, k)
+    with np.errstate(over="ignore"):
+        ref = prod.astype(np.float16).view(np.uint16)
+    got = o.dequant_f16(wb, k)
+    assert np.array_equal(got, ref)
+
+
+ALL_PINS = [
+    pin_f16_decode_exhaustive,
+    pin_f16_encode_vs_numpy,
+    pin_f16_golden,
+    pin_q8_1_golden,
+    pin_q8_0_layout_golden,
+    pin_quant_invariants,
+    pin_requant_idempotent,
+    pin_block_dots_bruteforce,
+    pin_fold_bruteforce,
+    pin_dequant_vs_numpy,
+]

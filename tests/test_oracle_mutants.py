@@ -1,0 +1,53 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Every mutant is a one-line textual change to a temporary copy of oracle/q8_oracle.c,
+compiled with the same flags; the committed oracle is never modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "q8_oracle.c")
+
+MUTANTS = {
+    "reciprocal_multiply": ("float r = roundf(v[i] / d);", "float r = roundf(v[i] * (1.0f / d));"),
+    "ties_to_even": ("float r = roundf(v[i] / d);", "float r = rintf(v[i] / d);"),
+    "floor_plus_half": ("float r = roundf(v[i] / d);", "float r = floorf(v[i] / d + 0.5f);"),
+    "divisor_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "signed_max": ("float a = fabsf(v[i]);", "float a = v[i];"),
+    "dropped_last_block": ("for (int64_t b = 0; b < nb; b++) {\n                const uint8_t *blk = block_ptr(w, r, b, nb);\n                int32_t dot",
+                           "for (int64_t b = 0; b < nb - 1; b++) {\n                const uint8_t *blk = block_ptr(w, r, b, nb);\n                int32_t dot"),
+    "act_scale_of_block0": ("float da = xd[t * nb + b];", "float da = xd[t * nb];"),
+    "reversed_operand": ("s += (int32_t)wq[i] * (int32_t)xq[i];", "s += (int32_t)wq[i] * (int32_t)xq[QK - 1 - i];"),
+    "negated_dot": ("s += (int32_t)wq[i] * (int32_t)xq[i];", "s -= (int32_t)wq[i] * (int32_t)xq[i];"),
+    "f16_truncate": ("if (rem > half || (rem == half && (q & 1u)))", "if (0)"),
+    "f16_ties_away": ("if (rem > half || (rem == half && (q & 1u)))", "if (rem >= half)"),
+    "f16_decode_bias": ("v = ldexpf((float)(1024 + f), e - 25);", "v = ldexpf((float)(1024 + f), e - 24);"),
+    "dequant_unrounded_scale": ("float dw = block_scale(blk);\n            const int8_t *wq",
+                                "float dw = block_scale(blk) * 1.0001f;\n            const int8_t *wq"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"anchor for {name} not found"
+    mutated = src.replace(old, new)
+    c = tmp_path / "mut.c"
+    so = tmp_path / "libmut.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                    "-shared", "-o", str(so), str(c), "-lm"], check=True)
+    o = oracle.bound(oracle.Oracle(str(so)))
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
