@@ -1,0 +1,109 @@
+"""GB300 (sm_103a) Q8_0 weight x q8_1 activation block-quantized matmul.
+
+The compute lives in libq8act.so (hand-written CUDA kernels behind the C ABI of
+include/q8act.h).  This package is its Python face:
+
+  * the raw ABI under the C names (``q8act_quantize_q8_1``, ``q8act_gemv_q8_0``, ...), which
+    take torch tensors or integer device addresses and return the C return code;
+  * torch conveniences (``quantize_q8_1``, ``gemv_q8_0``, ``gemm_q8_0``, ...) that allocate
+    outputs with torch on the input's device, call the ABI on torch's current stream and
+    raise ``Q8ActError`` on a non-zero return code.
+
+There is no CPU or PyTorch fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401  (re-exported ABI)
+    EXPORTED, LIB_PATH, Q8ACT_ERR_ALIGN, Q8ACT_ERR_CUDA_BASE, Q8ACT_ERR_DEVICE, Q8ACT_ERR_DIMS,
+    Q8ACT_ERR_NULL, Q8ACT_ERR_TIMEOUT, Q8ACT_ERR_WORKSPACE, Q8ACT_GEMV_MAX_M, Q8ACT_MAX_K,
+    Q8ACT_OK, Q8ActError, check, lib, q8act_debug_gemm_block_dots, q8act_debug_gemv_block_dots,
+    q8act_dequant_q8_0_f16, q8act_device_status, q8act_gemm_q8_0, q8act_gemm_q8_0_preq,
+    q8act_gemm_workspace_bytes, q8act_gemv_q8_0, q8act_mmq_ldm, q8act_quantize_q8_0,
+    q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror)
+
+QK = 32
+Q8_0_BYTES = 34
+
+
+def row_bytes(k: int) -> int:
+    """Bytes of one Q8_0 row of k values (k/32 blocks of 34 bytes)."""
+    return k // QK * Q8_0_BYTES
+
+
+def quantize_q8_0(w):
+    """f32 [n, k] CUDA tensor -> Q8_0 bytes, uint8 [n, k/32*34]."""
+    import torch
+    n, k = w.shape
+    out = torch.empty((n, row_bytes(k)), dtype=torch.uint8, device=w.device)
+    check(q8act_quantize_q8_0(w, out, n, k), "q8act_quantize_q8_0")
+    return out
+
+
+def quantize_q8_1(x):
+    """f32 [m, k] -> (xq int8 [m, k], xd f32 [m, k/32])."""
+    import torch
+    m, k = x.shape
+    xq = torch.empty((m, k), dtype=torch.int8, device=x.device)
+    xd = torch.empty((m, k // QK), dtype=torch.float32, device=x.device)
+    check(q8act_quantize_q8_1(x, xq, xd, m, k), "q8act_quantize_q8_1")
+    return xq, xd
+
+
+def quantize_q8_1_mmq(x):
+    """f32 [m, k] -> (xqh uint16 [m, k] binary16 quants, xdt f32 [k/32, ldm] scales)."""
+    import torch
+    m, k = x.shape
+    xqh = torch.empty((m, k), dtype=torch.uint16, device=x.device)
+    xdt = torch.empty((k // QK, q8act_mmq_ldm(m)), dtype=torch.float32, device=x.device)
+    check(q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k), "q8act_quantize_q8_1_mmq")
+    return xqh, xdt
+
+
+def gemv_q8_0(w, xq, xd, n: int, out=None):
+    """Decode GEMV: Q8_0 bytes w (n rows), q8_1 activation (xq, xd) of m <= 8 tokens."""
+    import torch
+    m, k = xq.shape
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    check(q8act_gemv_q8_0(w, xq, xd, y, m, n, k), "q8act_gemv_q8_0")
+    return y
+
+
+def gemm_workspace(m: int, k: int, device):
+    import torch
+    nbytes = q8act_gemm_workspace_bytes(m, k)
+    if nbytes == 0:
+        raise Q8ActError(Q8ACT_ERR_DIMS, "q8act_gemm_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def gemm_q8_0(w, x, n: int, ws=None, out=None):
+    """Prefill GEMM with the q8_1 quantization of x fused into the call."""
+    import torch
+    m, k = x.shape
+    if ws is None:
+        ws = gemm_workspace(m, k, x.device)
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
+    check(q8act_gemm_q8_0(w, x, y, m, n, k, ws, ws.numel()), "q8act_gemm_q8_0")
+    return y
+
+
+def gemm_q8_0_preq(w, xqh, xdt, n: int, out=None):
+    """Prefill GEMM on an activation already in the MMQ layout (quantize_q8_1_mmq)."""
+    import torch
+    m, k = xqh.shape
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xqh.device)
+    check(q8act_gemm_q8_0_preq(w, xqh, xdt, y, m, n, k), "q8act_gemm_q8_0_preq")
+    return y
+
+
+def dequant_q8_0_f16(w, n: int, k: int, out=None):
+    """Q8_0 bytes -> row-major float16 [n, k]."""
+    import torch
+    w16 = out if out is not None else torch.empty((n, k), dtype=torch.float16, device=w.device)
+    check(q8act_dequant_q8_0_f16(w, w16, n, k), "q8act_dequant_q8_0_f16")
+    return w16
+
+
+def device_status(stream=None) -> None:
+    """Synchronize and raise if a kernel recorded a pipeline timeout since the last check."""
+    check(q8act_device_status(stream), "q8act_device_status")

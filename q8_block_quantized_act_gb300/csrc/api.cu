@@ -1,0 +1,247 @@
+// api.cu -- the extern "C" boundary of libq8act (declared in include/q8act.h): argument
+// checks, per-device setup and dispatch to the kernels.  No call allocates memory or
+// synchronizes, except q8act_device_status.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device-side status word: kernels OR bits into it when a pipeline wait times out.
+__device__ int g_status;
+
+struct DeviceSlot {
+    bool ready = false;
+    int rc = Q8ACT_OK;
+    q8::DeviceInfo info{};
+};
+
+DeviceSlot g_slots[kMaxDevices];
+std::mutex g_mutex;
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? Q8ACT_OK : Q8ACT_ERR_CUDA_BASE + (int)e; }
+
+// Current device's info; checks once per device that it is an sm_103 GPU.
+int current_device(const q8::DeviceInfo **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_rc(e);
+    if (dev < 0 || dev >= kMaxDevices) return Q8ACT_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceSlot &s = g_slots[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0, sms = 0, smem = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return cuda_rc(e);
+        if (major != 10 || minor != 3) {
+            s.rc = Q8ACT_ERR_DEVICE;
+        } else {
+            void *status = nullptr;
+            if ((e = cudaGetSymbolAddress(&status, g_status)) != cudaSuccess) return cuda_rc(e);
+            s.info.device = dev;
+            s.info.num_sms = sms;
+            s.info.max_smem_optin = (size_t)smem;
+            s.info.status = static_cast<int *>(status);
+            s.rc = Q8ACT_OK;
+        }
+        s.ready = true;
+    }
+    *out = &s.info;
+    return s.rc;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_k(int64_t k)
+{
+    return (k > 0 && k % q8::K_ALIGN == 0 && k <= Q8ACT_MAX_K) ? Q8ACT_OK : Q8ACT_ERR_DIMS;
+}
+
+// Largest m * k the GEMM accepts (keeps every element index inside 32 bits).
+constexpr int64_t kMaxGemmElems = (int64_t)1 << 30;
+
+int check_gemm_dims(int64_t m, int64_t n, int64_t k)
+{
+    if (check_k(k) != Q8ACT_OK || m < 1 || n < 1) return Q8ACT_ERR_DIMS;
+    if (m * k > kMaxGemmElems || n * k > ((int64_t)1 << 34) || m * n > ((int64_t)1 << 31))
+        return Q8ACT_ERR_DIMS;
+    if (n > INT32_MAX || m > INT32_MAX) return Q8ACT_ERR_DIMS;
+    return Q8ACT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int q8act_version(void) { return 100; }
+
+const char *q8act_strerror(int rc)
+{
+    switch (rc) {
+    case Q8ACT_OK: return "ok";
+    case Q8ACT_ERR_NULL: return "a required pointer is NULL";
+    case Q8ACT_ERR_DIMS: return "dimensions out of range (k must be a positive multiple of 256)";
+    case Q8ACT_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case Q8ACT_ERR_WORKSPACE: return "workspace missing or too small";
+    case Q8ACT_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+    case Q8ACT_ERR_TIMEOUT: return "a kernel timed out waiting in its pipeline";
+    default:
+        if (rc >= Q8ACT_ERR_CUDA_BASE) return cudaGetErrorString((cudaError_t)(rc - Q8ACT_ERR_CUDA_BASE));
+        return "unknown error";
+    }
+}
+
+int64_t q8act_mmq_ldm(int64_t m) { return m < 1 ? 0 : (m + 3) / 4 * 4; }
+
+int q8act_quantize_q8_1(const float *x, int8_t *xq, float *xd, int64_t m, int64_t k, void *stream)
+{
+    if (!x || !xq || !xd) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xd)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_quantize_q8_1(*dev, x, xq, xd, m, k, (cudaStream_t)stream));
+}
+
+int q8act_quantize_q8_1_mmq(const float *x, uint16_t *xqh, float *xdt, int64_t m, int64_t k, void *stream)
+{
+    if (!x || !xqh || !xdt) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m * k > kMaxGemmElems) return Q8ACT_ERR_DIMS;
+    if (!aligned16(x) || !aligned16(xqh) || !aligned16(xdt)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_quantize_q8_1_mmq(*dev, x, xqh, xdt, m, k, q8act_mmq_ldm(m), (cudaStream_t)stream));
+}
+
+int q8act_quantize_q8_0(const float *w, void *wq, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !wq) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || n < 1 || n * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(wq)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_quantize_q8_0(*dev, w, static_cast<uint8_t *>(wq), n, k, (cudaStream_t)stream));
+}
+
+int q8act_dequant_q8_0_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !w16) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || n < 1 || n * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(w16)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_dequant_q8_0_f16(*dev, static_cast<const uint8_t *>(w), static_cast<uint16_t *>(w16), n, k,
+                                               (cudaStream_t)stream));
+}
+
+static int gemv_common(const void *w, const int8_t *xq, const float *xd, float *y, int32_t *dots, int64_t m,
+                       int64_t n, int64_t k, void *stream)
+{
+    if (!w || !xq || !xd || (!y && !dots)) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_MAX_M || n < 1 || n > INT32_MAX / 2 ||
+        n * k > ((int64_t)1 << 36))
+        return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(xq) || !aligned16(xd) || (y && !aligned16(y)) || (dots && !aligned16(dots)))
+        return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if (!q8::gemv_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
+    return cuda_rc(q8::launch_gemv_q8_0(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
+                                        (cudaStream_t)stream));
+}
+
+int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m, int64_t n, int64_t k,
+                    void *stream)
+{
+    if (!y) return Q8ACT_ERR_NULL;
+    return gemv_common(w, xq, xd, y, nullptr, m, n, k, stream);
+}
+
+int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n, int64_t k,
+                                void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    // The dot stage needs valid (unused) scales: pass the quants pointer, which is readable.
+    return gemv_common(w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
+}
+
+size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k)
+{
+    if (check_k(k) != Q8ACT_OK || m < 1 || m * k > kMaxGemmElems) return 0;
+    const size_t quants = (size_t)m * (size_t)k * 2;
+    const size_t scales = (size_t)(k / q8::QK) * (size_t)q8act_mmq_ldm(m) * 4;
+    return ((quants + 255) / 256 * 256) + scales;
+}
+
+static int gemm_core(const void *w, const uint16_t *xqh, const float *xdt, float *y, int32_t *dots, int64_t m,
+                     int64_t n, int64_t k, void *stream)
+{
+    if (!w || !xqh || !xdt || (!y && !dots)) return Q8ACT_ERR_NULL;
+    if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(xqh) || !aligned16(xdt) || (y && !aligned16(y)) || (dots && !aligned16(dots)))
+        return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_gemm_q8_0(*dev, static_cast<const uint8_t *>(w), xqh, xdt, y, dots, m, n, k,
+                                        q8act_mmq_ldm(m), (cudaStream_t)stream));
+}
+
+int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k, void *ws,
+                    size_t ws_bytes, void *stream)
+{
+    if (!w || !x || !y) return Q8ACT_ERR_NULL;
+    if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
+    const size_t need = q8act_gemm_workspace_bytes(m, k);
+    if (!ws || ws_bytes < need) return Q8ACT_ERR_WORKSPACE;
+    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(ws)) return Q8ACT_ERR_ALIGN;
+    uint16_t *xqh = static_cast<uint16_t *>(ws);
+    float *xdt = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k * 2 + 255) / 256 * 256);
+    int rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
+    if (rc) return rc;
+    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, stream);
+}
+
+int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, float *y, int64_t m, int64_t n,
+                         int64_t k, void *stream)
+{
+    if (!y) return Q8ACT_ERR_NULL;
+    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, stream);
+}
+
+int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, int64_t m, int64_t n, int64_t k,
+                                void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    // The dot stage needs a readable (unused) scale array of the right shape: reuse the
+    // quants, which are larger than the scale array.
+    return gemm_core(w, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, stream);
+}
+
+int q8act_device_status(void *stream)
+{
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_rc(e);
+    int host = 0;
+    const int zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&host, g_status, sizeof(int))) != cudaSuccess) return cuda_rc(e);
+    if (host && (e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int))) != cudaSuccess) return cuda_rc(e);
+    return host ? Q8ACT_ERR_TIMEOUT : Q8ACT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// common.cuh -- shared device helpers of libq8act (sm_103a): constants, PTX wrappers for
+// mbarriers, bulk/TMA copies and tcgen05, and bounded pipeline waits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q8act.h"
+
+namespace q8 {
+
+constexpr int QK = 32;            // values per block
+constexpr int Q8_0_BYTES = 34;    // binary16 scale + 32 int8 quants
+constexpr int GROUP_BLOCKS = 8;   // 8 blocks = 272 bytes = 17 x 16 B (lcm of 34 and 16)
+constexpr int GROUP_BYTES = GROUP_BLOCKS * Q8_0_BYTES;
+constexpr int K_ALIGN = 256;      // k must be a multiple of this (row start 16 B aligned)
+
+// Device status word bits (read back by q8act_device_status).
+constexpr int STATUS_TIMEOUT = 1;
+
+// A pipeline wait gives up after this long (the kernel then records STATUS_TIMEOUT and
+// leaves its loop instead of hanging the GPU).
+constexpr unsigned long long WAIT_TIMEOUT_NS = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed.  Returns false (after setting
+// STATUS_TIMEOUT in *status) if that takes longer than WAIT_TIMEOUT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status)
+{
+#pragma unroll 1
+    for (int i = 0; i < 128; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
+    const unsigned long long t0 = globaltimer();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
+            atomicOr(status, STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Bulk (non-tensor) and tensor (TMA) copies global -> shared, completing on an mbarrier.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                         uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const CUtensorMap *map, int32_t x,
+                                            int32_t y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst_smem)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (tensor core reads).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------
+// Small arithmetic helpers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float half_bits_to_float(uint32_t h16)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h16)));
+}
+
+__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c)
+{
+    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+}  // namespace q8

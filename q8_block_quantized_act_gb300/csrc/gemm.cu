@@ -1,0 +1,488 @@
+// gemm.cu -- Q8_0 x q8_1 GEMM for prefill (the "MMQ" regime: m >= 16 in the pages'
+// dispatch, memra-engine 0.70.0 fp8_ffi.rs module doc), on the sm_103a tensor cores.
+//
+//   y[t][r] = sum_b d_w[r][b] * d_a[t][b] * D[t][r][b],  D = exact int32 32-wide block dot.
+//
+// sm_103a has no int8 tcgen05 MMA (ptxas rejects .kind::i8 for this target), so the exact
+// integer dot runs on the f16 pipe: every quant |q| <= 127 is an exact binary16 value, every
+// product |wq * xq| <= 16129 is exact in the f32 accumulator, and so is every partial sum of
+// a 32-wide block (|D| <= 516128 < 2^24).  Each block gets a fresh accumulator in tensor
+// memory (two K=16 MMAs), and fold warps apply the block's scales on the CUDA cores -- the
+// per-32 fold of the pages' MMQ floor (accprobe_bench.rs module doc), scheduled so that the
+// tensor pipe runs ahead into other accumulator buffers while a block is being folded.
+//
+// Tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N, TMEM columns), full k.
+// Warp roles (448 threads):
+//   warps 0-3   converters: raw Q8_0 rows (TMA, 272-byte groups) -> binary16 A tiles in the
+//               128-byte-swizzled K-major layout + f32 weight scales
+//   warps 4-11  fold: tcgen05.ld (16x256b) of a block's D, acc += (d_w * d_a) * D
+//   warp 12     producer: TMA of activation tiles, activation scales and raw weight groups
+//   warp 13     TMEM allocator + single-thread MMA issuer
+#include "common.cuh"
+#include "launch.h"
+
+namespace q8 {
+namespace {
+
+constexpr int BM = 128;            // weight rows per tile
+constexpr int BN = 128;            // tokens per tile
+constexpr int KC = 64;             // k per chunk (one 128-byte swizzle row of binary16)
+constexpr int CHUNKS_PER_GROUP = 4;  // a 256-wide raw weight group feeds 4 chunks
+
+constexpr int ACT_STAGES = 4;
+constexpr int RAW_STAGES = 2;
+constexpr int A_STAGES = 2;
+constexpr int SC_STAGES = 8;
+constexpr int D_BUFS = 4;
+constexpr int TMEM_COLS = 512;
+
+constexpr int ACT_TILE_BYTES = BN * KC * 2;        // 16384
+constexpr int A_TILE_BYTES = BM * KC * 2;          // 16384
+constexpr int RAW_TILE_BYTES = BM * GROUP_BYTES;   // 34816
+constexpr int SC_SLOT_BYTES = 2 * BN * 4 + 2 * BM * 4;  // act scales [2][BN], weight scales [2][BM]
+
+constexpr int OFF_ACT = 0;
+constexpr int OFF_A = OFF_ACT + ACT_STAGES * ACT_TILE_BYTES;
+constexpr int OFF_RAW = OFF_A + A_STAGES * A_TILE_BYTES;
+constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_TILE_BYTES;
+constexpr int OFF_BAR = OFF_SC + SC_STAGES * SC_SLOT_BYTES;
+constexpr int NUM_BARS = 2 * (ACT_STAGES + RAW_STAGES + A_STAGES + SC_STAGES + D_BUFS) + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte base alignment
+
+constexpr int NUM_CONV_WARPS = 4;
+constexpr int NUM_FOLD_WARPS = 8;
+constexpr int PRODUCER_WARP = NUM_CONV_WARPS + NUM_FOLD_WARPS;   // 12
+constexpr int MMA_WARP = PRODUCER_WARP + 1;                      // 13
+constexpr int THREADS = (MMA_WARP + 1) * 32;                     // 448
+
+static_assert(OFF_A % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_SC % 128 == 0, "alignment");
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B binary16 (bits 7-9,
+// 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand stored in 128-byte swizzled rows
+// (8-row atoms of 1024 bytes): start address >> 4 (bits 0-13), leading byte offset
+// (unused for this layout, bits 16-29), stride byte offset = 1024 >> 4 (bits 32-45),
+// descriptor version 1 (bits 46-47), swizzle mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+// 16 lanes x 256 bits, repeated 8 times along the columns: 32 registers per thread.
+// Register 4j+e of thread T holds lane base + T/4 + 8*(e>>1), column base + 8j + 2*(T%4) + (e&1).
+__device__ __forceinline__ void tc_ld_16x256b_x8(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Four signed bytes -> two half2 holding the same integers (exact).
+__device__ __forceinline__ uint2 bytes_to_f16x4(uint32_t q4)
+{
+    const uint32_t u = q4 ^ 0x80808080u;                   // q + 128 in 0..255
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140); // 0x64uu = 1024 + u
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x5342);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&ha),
+                      *reinterpret_cast<const uint32_t *>(&hb));
+}
+
+struct Bars {
+    uint64_t *act_full, *act_empty, *raw_full, *raw_empty, *a_full, *a_empty, *sc_full,
+        *sc_empty, *d_full, *d_empty, *mma_done;
+};
+
+__device__ __forceinline__ Bars carve_bars(uint8_t *base)
+{
+    uint64_t *b = reinterpret_cast<uint64_t *>(base);
+    Bars r;
+    r.act_full = b; b += ACT_STAGES;
+    r.act_empty = b; b += ACT_STAGES;
+    r.raw_full = b; b += RAW_STAGES;
+    r.raw_empty = b; b += RAW_STAGES;
+    r.a_full = b; b += A_STAGES;
+    r.a_empty = b; b += A_STAGES;
+    r.sc_full = b; b += SC_STAGES;
+    r.sc_empty = b; b += SC_STAGES;
+    r.d_full = b; b += D_BUFS;
+    r.d_empty = b; b += D_BUFS;
+    r.mma_done = b;
+    return r;
+}
+
+// A wait that also gives up as soon as another role of this CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *status,
+                                              volatile int *abort_flag)
+{
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
+            atomicOr(status, STATUS_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+template <bool DOTS>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_q8_0_kernel(const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_xd, float *__restrict__ y,
+                     int32_t *__restrict__ dots, int m, int n, int k, int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Bars bars = carve_bars(smem + OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * BM;
+    const int tok0 = blockIdx.y * BN;
+    const int nkc = k / KC;
+    const int nb = k / QK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ACT_STAGES; ++s) { mbar_init(&bars.act_full[s], 1); mbar_init(&bars.act_empty[s], 1); }
+        for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], 32 * NUM_CONV_WARPS); }
+        for (int s = 0; s < A_STAGES; ++s) { mbar_init(&bars.a_full[s], 32 * NUM_CONV_WARPS); mbar_init(&bars.a_empty[s], 1); }
+        for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + 32 * NUM_CONV_WARPS); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
+        for (int s = 0; s < D_BUFS; ++s) { mbar_init(&bars.d_full[s], 1); mbar_init(&bars.d_empty[s], NUM_FOLD_WARPS); }
+        mbar_init(bars.mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == PRODUCER_WARP && lane == 0) {
+        prefetch_tensormap(&tm_w);
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_xd);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == PRODUCER_WARP) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int issued_raw = 0, issued_act = 0, issued_sc = 0;
+            for (int kc = 0; kc < nkc; ++kc) {
+                if ((kc & (CHUNKS_PER_GROUP - 1)) == 0) {
+                    const int g = kc / CHUNKS_PER_GROUP;
+                    const int rs = g % RAW_STAGES;
+                    if (!wait_or_abort(&bars.raw_empty[rs], ((g / RAW_STAGES) & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(&bars.raw_full[rs], RAW_TILE_BYTES);
+                    tma_load_2d(smem + OFF_RAW + rs * RAW_TILE_BYTES, &tm_w, g * (GROUP_BYTES / 2), row0,
+                                &bars.raw_full[rs]);
+                    ++issued_raw;
+                }
+                const int as = kc % ACT_STAGES;
+                if (!wait_or_abort(&bars.act_empty[as], ((kc / ACT_STAGES) & 1) ^ 1, status, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars.act_full[as], ACT_TILE_BYTES);
+                tma_load_2d(smem + OFF_ACT + as * ACT_TILE_BYTES, &tm_x, kc * KC, tok0, &bars.act_full[as]);
+                ++issued_act;
+                const int ss = kc % SC_STAGES;
+                if (!wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars.sc_full[ss], 2 * BN * 4);
+                tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES, &tm_xd, tok0, 2 * kc, &bars.sc_full[ss]);
+                ++issued_sc;
+            }
+            // Drain: never leave with a copy into this CTA's shared memory in flight.
+            for (int i = issued_raw > RAW_STAGES ? issued_raw - RAW_STAGES : 0; i < issued_raw; ++i)
+                mbar_wait(&bars.raw_full[i % RAW_STAGES], (i / RAW_STAGES) & 1, status);
+            for (int i = issued_act > ACT_STAGES ? issued_act - ACT_STAGES : 0; i < issued_act; ++i)
+                mbar_wait(&bars.act_full[i % ACT_STAGES], (i / ACT_STAGES) & 1, status);
+            for (int i = issued_sc > SC_STAGES ? issued_sc - SC_STAGES : 0; i < issued_sc; ++i)
+                mbar_wait(&bars.sc_full[i % SC_STAGES], (i / SC_STAGES) & 1, status);
+        }
+    } else if (warp == MMA_WARP) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            for (int kc = 0; kc < nkc; ++kc) {
+                const int as = kc % ACT_STAGES;
+                const int aslot = kc % A_STAGES;
+                if (!wait_or_abort(&bars.act_full[as], (kc / ACT_STAGES) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&bars.a_full[aslot], (kc / A_STAGES) & 1, status, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + OFF_A + aslot * A_TILE_BYTES);
+                const uint32_t b_addr = smem_u32(smem + OFF_ACT + as * ACT_TILE_BYTES);
+                bool ok = true;
+                for (int h = 0; h < 2; ++h) {
+                    const int b = 2 * kc + h;
+                    const int buf = b % D_BUFS;
+                    if (!wait_or_abort(&bars.d_empty[buf], ((b / D_BUFS) & 1) ^ 1, status, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t off = (uint32_t)(h * 64 + kk * 32);
+                        tc_mma_f16(d_tmem, smem_desc_sw128(a_addr + off), smem_desc_sw128(b_addr + off), kk);
+                    }
+                    tc_commit(&bars.d_full[buf]);
+                }
+                if (!ok) break;
+                tc_commit(&bars.act_empty[as]);
+                tc_commit(&bars.a_empty[aslot]);
+            }
+            // All MMAs issued by this thread have completed once this arrives.
+            tc_commit(bars.mma_done);
+            mbar_wait(bars.mma_done, 0, status);
+        }
+    } else if (warp < NUM_CONV_WARPS) {
+        // ------------------------------ converters ------------------------------
+        const int r = threadIdx.x;  // row within the tile
+        const int ngroups = nkc / CHUNKS_PER_GROUP;
+        for (int g = 0; g < ngroups; ++g) {
+            const int rs = g % RAW_STAGES;
+            if (!wait_or_abort(&bars.raw_full[rs], (g / RAW_STAGES) & 1, status, abort_flag)) break;
+            uint32_t wv[GROUP_BYTES / 4];
+            const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RAW_TILE_BYTES + r * GROUP_BYTES);
+#pragma unroll
+            for (int c = 0; c < GROUP_BYTES / 16; ++c) {
+                const uint4 v = src[c];
+                wv[4 * c + 0] = v.x; wv[4 * c + 1] = v.y; wv[4 * c + 2] = v.z; wv[4 * c + 3] = v.w;
+            }
+            mbar_arrive(&bars.raw_empty[rs]);
+            bool ok = true;
+#pragma unroll
+            for (int part = 0; part < CHUNKS_PER_GROUP; ++part) {
+                const int kc = g * CHUNKS_PER_GROUP + part;
+                const int aslot = kc % A_STAGES;
+                const int ss = kc % SC_STAGES;
+                if (!wait_or_abort(&bars.a_empty[aslot], ((kc / A_STAGES) & 1) ^ 1, status, abort_flag) ||
+                    !wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                // blocks 2*part (even: scale in the low half of word 17*part, quants straddle
+                // words) and 2*part+1 (odd: scale in the high half of word 17*part+8).
+                const int w0 = 17 * part;
+                const int w1 = 17 * part + 8;
+                uint8_t *arow = smem + OFF_A + aslot * A_TILE_BYTES + r * 128;
+                const int sw = r & 7;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t q0 = __byte_perm(wv[w0 + 2 * c], wv[w0 + 2 * c + 1], 0x5432);
+                    const uint32_t q1 = __byte_perm(wv[w0 + 2 * c + 1], wv[w0 + 2 * c + 2], 0x5432);
+                    const uint2 lo = bytes_to_f16x4(q0), hi = bytes_to_f16x4(q1);
+                    *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint2 lo = bytes_to_f16x4(wv[w1 + 1 + 2 * c]);
+                    const uint2 hi = bytes_to_f16x4(wv[w1 + 2 + 2 * c]);
+                    *reinterpret_cast<uint4 *>(arow + (((c + 4) ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                }
+                float *wsc = reinterpret_cast<float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4);
+                wsc[r] = half_bits_to_float(wv[w0] & 0xffffu);
+                wsc[BM + r] = half_bits_to_float(wv[w1] >> 16);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars.a_full[aslot]);
+                mbar_arrive(&bars.sc_full[ss]);
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ------------------------------ fold warps ------------------------------
+        const int fw = warp - NUM_CONV_WARPS;      // 0..7
+        const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+        const int half = fw >> 2;                  // columns 64*half .. +63
+        const int tr = lane >> 2;                  // row within a 16-lane group (and +8)
+        const int tc = 2 * (lane & 3);             // column pair within each 8 columns
+        float acc[2][32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) { acc[0][i] = 0.0f; acc[1][i] = 0.0f; }
+
+        for (int b = 0; b < nb; ++b) {
+            const int kc = b >> 1;
+            const int blk = b & 1;
+            const int ss = kc % SC_STAGES;
+            const int buf = b % D_BUFS;
+            if (!wait_or_abort(&bars.d_full[buf], (b / D_BUFS) & 1, status, abort_flag)) break;
+            if (!wait_or_abort(&bars.sc_full[ss], (kc / SC_STAGES) & 1, status, abort_flag)) break;
+            tc_fence_after();
+            const float *asc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES) + blk * BN + 64 * half + tc;
+            const float *wsc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4) + blk * BM + 32 * quarter + tr;
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+                const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter + 16 * hl) << 16) + (uint32_t)(buf * BN + 64 * half);
+                float dv[32];
+                tc_ld_16x256b_x8(taddr, dv);
+                const float dw0 = wsc[16 * hl];
+                const float dw1 = wsc[16 * hl + 8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float2 da = *reinterpret_cast<const float2 *>(asc + 8 * j);
+                    float *a = &acc[hl][4 * j];
+                    const float *d = &dv[4 * j];
+                    if (DOTS) {
+                        const int rr = row0 + 32 * quarter + 16 * hl + tr;
+                        const int tt = tok0 + 64 * half + 8 * j + tc;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r_e = rr + 8 * (e >> 1), t_e = tt + (e & 1);
+                            if (r_e < n && t_e < m)
+                                dots[((int64_t)t_e * n + r_e) * nb + b] = __float2int_rn(d[e]);
+                        }
+                    } else {
+                        a[0] = __fmaf_rn(__fmul_rn(dw0, da.x), d[0], a[0]);
+                        a[1] = __fmaf_rn(__fmul_rn(dw0, da.y), d[1], a[1]);
+                        a[2] = __fmaf_rn(__fmul_rn(dw1, da.x), d[2], a[2]);
+                        a[3] = __fmaf_rn(__fmul_rn(dw1, da.y), d[3], a[3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.d_empty[buf]);
+            if (blk == 1 || b == nb - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.sc_empty[ss]);
+            }
+        }
+        if (!DOTS && !*abort_flag) {
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
+                        const int t_e = tok0 + 64 * half + 8 * j + tc + (e & 1);
+                        if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = acc[hl][4 * j + e];
+                    }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host: tensor maps through the driver entry point (no libcuda link dependency).
+// ---------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t dim0,
+               uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+               CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride1_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
+                             const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
+                             int64_t k, int64_t ldm, cudaStream_t stream)
+{
+    CUtensorMap tm_w, tm_x, tm_xd;
+    const uint64_t row_bytes = (uint64_t)k / QK * Q8_0_BYTES;
+    // Raw weights viewed as uint16 elements: a 272-byte group is 136 elements (16-byte multiple).
+    if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, row_bytes / 2, (uint64_t)n, row_bytes,
+                   GROUP_BYTES / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xqh, (uint64_t)k, (uint64_t)m,
+                   (uint64_t)k * 2, KC, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tm_xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xdt, (uint64_t)m, (uint64_t)(k / QK),
+                   (uint64_t)ldm * 4, BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((n + BM - 1) / BM), (unsigned)((m + BN - 1) / BN));
+    cudaError_t e;
+    if (dots) {
+        e = cudaFuncSetAttribute(gemm_q8_0_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        gemm_q8_0_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, y, dots, (int)m, (int)n, (int)k, dev.status);
+    } else {
+        e = cudaFuncSetAttribute(gemm_q8_0_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        gemm_q8_0_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, y, dots, (int)m, (int)n, (int)k, dev.status);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace q8

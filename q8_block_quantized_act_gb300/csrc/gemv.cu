@@ -1,0 +1,285 @@
+// gemv.cu -- Q8_0 x q8_1 GEMV for decode and speculative verify (m = 1..8): the "mmvq"
+// regime of memra-engine 0.113.0 decode_kernel_census.rs (fn q8 -> qmatvec_mmvq_into).
+//
+// The weight stream (34 bytes per 32 weights) is read exactly once, so the kernel is bound
+// by HBM bandwidth.  Design (one persistent CTA per SM):
+//   * a producer warp streams "chunks" of R consecutive rows (R * row_bytes <= 34.8 KB,
+//     contiguous in memory) into a ring of shared-memory stages with cp.async.bulk,
+//     completing on mbarriers -- coalesced, 16-byte aligned, no per-thread address math;
+//   * 128 consumer threads split each chunk into "units" of 8 blocks (272 bytes = 17 x 16 B,
+//     the period at which 34-byte blocks realign to 16 bytes); a unit is read with 17
+//     conflict-free 16-byte shared loads, its 8 blocks are dotted with the activation
+//     (4 x dp4a per block per token) and folded as acc += (d_w * d_a) * D;
+//   * the activation (m x k int8 + scales) sits in shared memory for the whole kernel, padded
+//     so that neighbouring units hit different banks;
+//   * the per-row sum over units uses a fixed order, so token t's result is the same
+//     sequence of operations for every m (the pages' decode == verify law).
+#include "common.cuh"
+#include "launch.h"
+
+namespace q8 {
+namespace {
+
+constexpr int CONSUMERS = 128;
+constexpr int THREADS = CONSUMERS + 32;
+constexpr int MAX_STAGES = 6;
+constexpr int XG_WORDS = 68;   // per (token, group): 64 quant words + 4 pad
+constexpr int XDG_WORDS = 12;  // per (token, group): 8 scales + 4 pad
+constexpr int UNIT_WORDS = GROUP_BYTES / 4;  // 68
+
+struct Plan {
+    int G;              // groups of 8 blocks per row (k / 256)
+    int R;              // rows per chunk
+    int U;              // units per chunk (R * G)
+    int stages;
+    uint32_t row_bytes;
+    uint32_t chunk_bytes;
+    int64_t nchunks;
+    size_t off_x, off_xd, off_part, off_bar, smem;
+};
+
+Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap)
+{
+    Plan p{};
+    p.G = (int)(k / 256);
+    p.R = p.G <= CONSUMERS ? CONSUMERS / p.G : 1;
+    if ((int64_t)p.R > n) p.R = (int)n;
+    p.U = p.R * p.G;
+    p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
+    p.chunk_bytes = (uint32_t)p.R * p.row_bytes;
+    p.nchunks = (n + p.R - 1) / p.R;
+    const size_t x_bytes = (size_t)m * p.G * XG_WORDS * 4;
+    const size_t xd_bytes = (size_t)m * p.G * XDG_WORDS * 4;
+    const size_t part_bytes = 2 * (size_t)p.U * m * 4;
+    const size_t fixed = x_bytes + xd_bytes + part_bytes + 2 * MAX_STAGES * 8 + 64;
+    const size_t room = smem_cap > fixed ? smem_cap - fixed : 0;
+    int64_t st = (int64_t)(room / p.chunk_bytes);
+    if (st > MAX_STAGES) st = MAX_STAGES;
+    p.stages = (int)st;
+    p.off_x = (size_t)p.stages * p.chunk_bytes;            // multiple of 16
+    p.off_xd = p.off_x + x_bytes;
+    p.off_part = p.off_xd + xd_bytes;
+    p.off_bar = (p.off_part + part_bytes + 7) & ~(size_t)7;
+    p.smem = p.off_bar + 2 * MAX_STAGES * 8;
+    return p;
+}
+
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+template <int M, bool DOTS>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemv_q8_0_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq,
+                     const float *__restrict__ xd, float *__restrict__ y,
+                     int32_t *__restrict__ dots, int n, int k, Plan p, int *status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem + p.off_x);
+    float *xds = reinterpret_cast<float *>(smem + p.off_xd);
+    float *part = reinterpret_cast<float *>(smem + p.off_part);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + MAX_STAGES;
+
+    const int tid = threadIdx.x;
+    const int G = p.G;
+    const int nb = k / QK;
+
+    // Activation cache: quants [token][group][68 words], scales [token][group][12 words].
+    for (int idx = tid; idx < M * G * 16; idx += THREADS) {
+        const int t = idx / (G * 16), rem = idx - t * G * 16, g = rem >> 4, c = rem & 15;
+        const uint4 v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + g * 256 + c * 16);
+        *reinterpret_cast<uint4 *>(xs + (t * G + g) * XG_WORDS + c * 4) = v;
+    }
+    for (int idx = tid; idx < M * G * 2; idx += THREADS) {
+        const int t = idx / (G * 2), rem = idx - t * G * 2, g = rem >> 1, c = rem & 1;
+        const float4 v = *reinterpret_cast<const float4 *>(xd + (int64_t)t * nb + g * 8 + c * 4);
+        *reinterpret_cast<float4 *>(xds + (t * G + g) * XDG_WORDS + c * 4) = v;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CONSUMERS);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int64_t my_chunks =
+        blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (tid >= CONSUMERS) {
+        // ---------------- producer warp: one lane issues the bulk copies ----------------
+        if (tid == CONSUMERS) {
+            int64_t issued = 0;
+            for (int64_t i = 0; i < my_chunks; ++i) {
+                const int s = (int)(i % p.stages);
+                const uint32_t ph = (uint32_t)((i / p.stages) & 1);
+                if (!mbar_wait(&empty[s], ph ^ 1, status)) break;
+                const int64_t chunk = blockIdx.x + i * gridDim.x;
+                const int64_t row0 = chunk * p.R;
+                const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
+                const uint32_t bytes = (uint32_t)rows * p.row_bytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_g2s(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes,
+                         &full[s]);
+                ++issued;
+            }
+            // Do not leave while copies into this CTA's shared memory may be in flight.
+            for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
+                mbar_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+        }
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    for (int64_t i = 0; i < my_chunks; ++i) {
+        const int s = (int)(i % p.stages);
+        const uint32_t ph = (uint32_t)((i / p.stages) & 1);
+        const bool ok = mbar_wait(&full[s], ph, status);
+        if (bar_red_or(1, CONSUMERS, !ok)) break;
+
+        const int64_t chunk = blockIdx.x + i * gridDim.x;
+        const int64_t row0 = chunk * p.R;
+        const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+        const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
+        float *pbuf = part + (size_t)(i & 1) * p.U * M;
+
+        for (int u = tid; u < p.U; u += CONSUMERS) {
+            const int row = u / G;
+            const int g = u - row * G;
+            if (row >= rows) continue;
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(sbase + (size_t)row * p.row_bytes + g * GROUP_BYTES);
+            uint32_t wv[UNIT_WORDS];
+#pragma unroll
+            for (int c = 0; c < UNIT_WORDS / 4; ++c) {
+                const uint4 v = src[c];
+                wv[4 * c + 0] = v.x;
+                wv[4 * c + 1] = v.y;
+                wv[4 * c + 2] = v.z;
+                wv[4 * c + 3] = v.w;
+            }
+            float acc[M];
+#pragma unroll
+            for (int t = 0; t < M; ++t) acc[t] = 0.0f;
+            const uint32_t *xg = xs + g * XG_WORDS;
+            const float *xdg = xds + g * XDG_WORDS;
+#pragma unroll
+            for (int j = 0; j < GROUP_BLOCKS; ++j) {
+                // Block j of the unit starts at byte 34j: even j at word 17(j/2) (scale in
+                // the low half, quants straddle words), odd j with its scale in the high half
+                // of word 17(j/2)+8 and word-aligned quants after it.
+                uint32_t q[8];
+                uint32_t dbits;
+                if ((j & 1) == 0) {
+                    const int w0 = 17 * (j >> 1);
+                    dbits = wv[w0] & 0xffffu;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[e] = __byte_perm(wv[w0 + e], wv[w0 + e + 1], 0x5432);
+                } else {
+                    const int w1 = 17 * (j >> 1) + 8;
+                    dbits = wv[w1] >> 16;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[e] = wv[w1 + 1 + e];
+                }
+                const float dw = half_bits_to_float(dbits);
+#pragma unroll
+                for (int t = 0; t < M; ++t) {
+                    const uint4 *xv = reinterpret_cast<const uint4 *>(xg + t * G * XG_WORDS + j * 8);
+                    const uint4 a = xv[0], b = xv[1];
+                    int D = dp4a(q[0], a.x, 0);
+                    D = dp4a(q[1], a.y, D);
+                    D = dp4a(q[2], a.z, D);
+                    D = dp4a(q[3], a.w, D);
+                    D = dp4a(q[4], b.x, D);
+                    D = dp4a(q[5], b.y, D);
+                    D = dp4a(q[6], b.z, D);
+                    D = dp4a(q[7], b.w, D);
+                    if (DOTS) {
+                        dots[((int64_t)t * n + row0 + row) * nb + g * GROUP_BLOCKS + j] = D;
+                    } else {
+                        const float da = xdg[t * G * XDG_WORDS + j];
+                        acc[t] = __fmaf_rn(__fmul_rn(dw, da), __int2float_rn(D), acc[t]);
+                    }
+                }
+            }
+            if (!DOTS) {
+#pragma unroll
+                for (int t = 0; t < M; ++t) pbuf[u * M + t] = acc[t];
+            }
+        }
+        mbar_arrive(&empty[s]);  // this stage's bytes are no longer needed
+        if (DOTS) continue;
+        named_bar_sync(1, CONSUMERS);
+        for (int idx = tid; idx < rows * M; idx += CONSUMERS) {
+            const int t = idx / rows, r = idx - t * rows;
+            const float *pr = pbuf + (size_t)r * G * M + t;
+            float sum = pr[0];
+            for (int g = 1; g < G; ++g) sum = __fadd_rn(sum, pr[g * M]);
+            y[(int64_t)t * n + row0 + r] = sum;
+        }
+    }
+}
+
+template <int M, bool DOTS>
+cudaError_t launch_m(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
+                     float *y, int32_t *dots, int64_t n, int64_t k, cudaStream_t stream)
+{
+    const Plan p = make_plan(M, n, k, dev.max_smem_optin);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    auto kern = gemv_q8_0_kernel<M, DOTS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)p.smem);
+    if (e != cudaSuccess) return e;
+    int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
+    kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)n, (int)k, p,
+                                                  dev.status);
+    return cudaGetLastError();
+}
+
+template <bool DOTS>
+cudaError_t dispatch(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
+                     float *y, int32_t *dots, int64_t m, int64_t n, int64_t k,
+                     cudaStream_t stream)
+{
+    switch (m) {
+    case 1: return launch_m<1, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 2: return launch_m<2, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 3: return launch_m<3, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 4: return launch_m<4, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 5: return launch_m<5, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 6: return launch_m<6, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 7: return launch_m<7, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 8: return launch_m<8, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k)
+{
+    if (m < 1 || m > Q8ACT_GEMV_MAX_M) return false;
+    return make_plan(m, 1 << 20, k, dev.max_smem_optin).stages >= 2;
+}
+
+cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
+                             const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream)
+{
+    if (dots) return dispatch<true>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    return dispatch<false>(dev, w, xq, xd, y, dots, m, n, k, stream);
+}
+
+}  // namespace q8

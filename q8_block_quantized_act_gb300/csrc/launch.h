@@ -1,0 +1,39 @@
+// launch.h -- internal launchers of libq8act (host side).  Arguments are validated by the
+// C-ABI layer (api.cu) before any of these is called; each returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q8 {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    size_t max_smem_optin;
+    int *status;  // device address of the status word
+};
+
+cudaError_t launch_quantize_q8_1(const DeviceInfo &dev, const float *x, int8_t *xq, float *xd,
+                                 int64_t m, int64_t k, cudaStream_t stream);
+cudaError_t launch_quantize_q8_1_mmq(const DeviceInfo &dev, const float *x, uint16_t *xqh,
+                                     float *xdt, int64_t m, int64_t k, int64_t ldm,
+                                     cudaStream_t stream);
+cudaError_t launch_quantize_q8_0(const DeviceInfo &dev, const float *w, uint8_t *wq, int64_t n,
+                                 int64_t k, cudaStream_t stream);
+cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
+                                    int64_t n, int64_t k, cudaStream_t stream);
+
+// GEMV: returns cudaErrorInvalidValue when m*k is too large for the shared-memory plan.
+bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);
+cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
+                             const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream);
+
+// GEMM on MMQ-layout activations (xqh binary16 quants [m][k], xdt f32 scales [k/32][ldm]).
+// With dots != nullptr the fold is replaced by a store of the block dots D[m][n][k/32].
+cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
+                             const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
+                             int64_t k, int64_t ldm, cudaStream_t stream);
+
+}  // namespace q8

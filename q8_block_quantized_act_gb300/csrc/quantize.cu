@@ -1,0 +1,148 @@
+// quantize.cu -- the per-32-block quantizers: q8_1 activations (int8 and MMQ layouts) and
+// Q8_0 weights.  All three are HBM-bound elementwise passes: one thread owns 4 consecutive
+// values (one 16-byte load), 8 consecutive lanes own one block and find its amax with three
+// shuffles.
+//
+// The arithmetic is the per-block formula of memra-engine 0.81.0 f16_ffi.rs (try_f16_gemm,
+// W8A8 pilot): amax = max|v|, d = amax / 127, q = clamp(round(v / d), -127, 127), guarded
+// by amax > 0.  The division is IEEE (this file must not be built with fast-math or
+// -prec-div=false) and roundf rounds half away from zero, as Rust's f32::round does.
+#include "common.cuh"
+#include "launch.h"
+
+namespace q8 {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+struct Block4 {
+    int q[4];
+    float d;
+};
+
+// Quantize this thread's 4 values of a block whose 32 values are spread over 8 lanes.
+__device__ __forceinline__ Block4 quantize4(float4 v)
+{
+    // Start from 0 so that a block of NaNs behaves like the scalar loop's "a > amax".
+    float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
+    Block4 r;
+    r.d = __fdiv_rn(a, 127.0f);
+    const float vals[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (r.d == 0.0f) {
+            r.q[i] = 0;
+        } else {
+            float t = roundf(__fdiv_rn(vals[i], r.d));
+            if (t > 127.0f) t = 127.0f;
+            if (t < -127.0f) t = -127.0f;
+            r.q[i] = __float2int_rz(t);  // NaN converts to 0
+        }
+    }
+    return r;
+}
+
+__device__ __forceinline__ float4 load_stream(const float4 *p)
+{
+    return __ldcs(p);
+}
+
+// x [m][k] f32 -> xq [m][k] int8, xd [m][k/32] f32.
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__restrict__ x,
+                                                            uint32_t *__restrict__ xq,
+                                                            float *__restrict__ xd,
+                                                            int64_t nchunks)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
+        Block4 b = quantize4(load_stream(x + i));
+        xq[i] = (uint32_t)(b.q[0] & 0xff) | ((uint32_t)(b.q[1] & 0xff) << 8) |
+                ((uint32_t)(b.q[2] & 0xff) << 16) | ((uint32_t)(b.q[3] & 0xff) << 24);
+        if ((i & 7) == 0) xd[i >> 3] = b.d;
+    }
+}
+
+// x [m][k] f32 -> xqh [m][k] binary16 (exact small integers), xdt [k/32][ldm] f32.
+__global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__restrict__ x,
+                                                                uint2 *__restrict__ xqh,
+                                                                float *__restrict__ xdt,
+                                                                int64_t nchunks,
+                                                                int64_t chunks_per_row,
+                                                                int64_t ldm)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
+        Block4 b = quantize4(load_stream(x + i));
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__int2half_rn(b.q[j]));
+        xqh[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        if ((i & 7) == 0) {
+            const int64_t t = i / chunks_per_row;
+            const int64_t blk = (i - t * chunks_per_row) >> 3;
+            xdt[blk * ldm + t] = b.d;
+        }
+    }
+}
+
+// w [n][k] f32 -> Q8_0 blocks (34 B: binary16 scale of the f32 d, then 32 int8 quants).
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__restrict__ w,
+                                                            uint8_t *__restrict__ out,
+                                                            int64_t nchunks)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
+        Block4 b = quantize4(load_stream(w + i));
+        uint8_t *blk = out + (i >> 3) * Q8_0_BYTES;
+        const int j = (int)(i & 7);
+        // quants of this thread start at byte 2 + 4j: 2-byte aligned
+        uint16_t *q16 = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);
+        q16[0] = (uint16_t)((b.q[0] & 0xff) | ((b.q[1] & 0xff) << 8));
+        q16[1] = (uint16_t)((b.q[2] & 0xff) | ((b.q[3] & 0xff) << 8));
+        if (j == 0)
+            *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__float2half_rn(b.d));
+    }
+}
+
+int grid_for(const DeviceInfo &dev, int64_t nchunks, int threads)
+{
+    int64_t want = (nchunks + threads - 1) / threads;
+    int64_t cap = (int64_t)dev.num_sms * 8;
+    return (int)(want < cap ? want : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8_1(const DeviceInfo &dev, const float *x, int8_t *xq, float *xd,
+                                 int64_t m, int64_t k, cudaStream_t stream)
+{
+    const int64_t nchunks = m * k / 4;
+    quantize_q8_1_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
+        reinterpret_cast<const float4 *>(x), reinterpret_cast<uint32_t *>(xq), xd, nchunks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q8_1_mmq(const DeviceInfo &dev, const float *x, uint16_t *xqh,
+                                     float *xdt, int64_t m, int64_t k, int64_t ldm,
+                                     cudaStream_t stream)
+{
+    const int64_t nchunks = m * k / 4;
+    quantize_q8_1_mmq_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
+        reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xqh), xdt, nchunks, k / 4,
+        ldm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q8_0(const DeviceInfo &dev, const float *w, uint8_t *wq, int64_t n,
+                                 int64_t k, cudaStream_t stream)
+{
+    const int64_t nchunks = n * k / 4;
+    quantize_q8_0_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
+        reinterpret_cast<const float4 *>(w), wq, nchunks);
+    return cudaGetLastError();
+}
+
+}  // namespace q8

@@ -1,0 +1,67 @@
+"""GPU GEMM (prefill MMQ on tcgen05) vs the oracle: exact block dots from the tensor-core
+path, outputs within 1e-5 * S, fused and pre-quantized entry points, ragged tiles."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import q8_block_quantized_act_gb300 as q8
+from gpu_util import (assert_within_tolerance, cuda, device_ok, ensure_built, host, problem,
+                      sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 128, 256), (130, 200, 512), (1, 64, 256),
+                                   (17, 300, 1280), (256, 384, 4096)])
+def test_gemm_block_dots_exact(m, n, k):
+    ensure_built()
+    _, x, wb, xq, _ = problem(m, n, k, "token_scales")
+    xqh, xdt = q8.quantize_q8_1_mmq(cuda(x))
+    D = torch.full((m, n, k // 32), -7, dtype=torch.int32, device="cuda")
+    q8.check(q8.q8act_debug_gemm_block_dots(cuda(wb), xqh, D, m, n, k))
+    device_ok()
+    assert np.array_equal(host(D), oracle.block_dots(wb, xq, k))
+
+
+@pytest.mark.parametrize("m,n,k,kind", [
+    (128, 128, 256, "normal"),
+    (130, 200, 512, "token_scales"),     # ragged in m and n
+    (1, 77, 4096, "normal"),             # m below the prefill threshold
+    (16, 4096, 1280, "normal"),
+    (300, 520, 2048, "outliers"),
+])
+def test_gemm_matches_oracle(m, n, k, kind):
+    ensure_built()
+    _, x, wb, xq, xd = problem(m, n, k, kind)
+    y = host(q8.gemm_q8_0(cuda(wb), cuda(x), n))
+    device_ok()
+    _, y64, S = oracle.matmul(wb, xq, xd, k)
+    assert_within_tolerance(y, y64, S)
+
+
+def test_gemm_preq_equals_fused():
+    ensure_built()
+    m, n, k = 200, 260, 1024
+    _, x, wb, xq, xd = problem(m, n, k, "token_scales")
+    w_d, x_d = cuda(wb), cuda(x)
+    y_fused = host(q8.gemm_q8_0(w_d, x_d, n))
+    xqh, xdt = q8.quantize_q8_1_mmq(x_d)
+    y_pre = host(q8.gemm_q8_0_preq(w_d, xqh, xdt, n))
+    device_ok()
+    assert np.array_equal(y_fused.view(np.uint32), y_pre.view(np.uint32))
+
+
+@pytest.mark.parametrize("m,n", [(512, 4096), (512, 5152), (2048, 20480), (512, 64448)])
+def test_gemm_serving_shapes_sampled(m, n):
+    """The prefill shapes at full size: every token, a seeded sample of weight rows."""
+    ensure_built()
+    k = 4096
+    _, x, wb, xq, xd = problem(m, n, k, "token_scales" if n > 5152 else "normal")
+    y = host(q8.gemm_q8_0(cuda(wb), cuda(x), n))
+    device_ok()
+    rows = sample_rows(n, 256)
+    _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
+    assert_within_tolerance(y[:, rows], y64, S)
+    again = host(q8.gemm_q8_0(cuda(wb), cuda(x), n))
+    assert np.array_equal(again.view(np.uint32), y.view(np.uint32)), "not deterministic"

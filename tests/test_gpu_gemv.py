@@ -1,0 +1,64 @@
+"""GPU GEMV (decode / verify, m = 1..8) vs the oracle: exact block dots, outputs within
+1e-5 * S, bitwise batch invariance (decode == verify) and determinism."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import q8_block_quantized_act_gb300 as q8
+from gpu_util import (assert_within_tolerance, cuda, device_ok, ensure_built, host, problem,
+                      sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gemv(wb, xq, xd, n):
+    return host(q8.gemv_q8_0(cuda(wb), cuda(xq), cuda(xd), n))
+
+
+@pytest.mark.parametrize("m,n,k,kind", [
+    (1, 512, 256, "normal"),          # tiny decode shape
+    (1, 4096, 4096, "outliers"),      # o_proj
+    (1, 5152, 4096, "outliers"),      # fused qkv (ragged chunk tail)
+    (3, 1000, 1280, "normal"),        # short rows, ragged n, odd m
+    (8, 777, 4096, "normal"),
+    (2, 1, 256, "normal"),            # a single row
+    (5, 33, 8192, "token_scales"),
+])
+def test_gemv_matches_oracle(m, n, k, kind):
+    ensure_built()
+    _, _, wb, xq, xd = problem(m, n, k, kind)
+    y = run_gemv(wb, xq, xd, n)
+    device_ok()
+    _, y64, S = oracle.matmul(wb, xq, xd, k)
+    assert y.shape == (m, n)
+    assert_within_tolerance(y, y64, S)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 512, 256), (4, 300, 1280), (8, 130, 4096)])
+def test_gemv_block_dots_exact(m, n, k):
+    ensure_built()
+    _, _, wb, xq, _ = problem(m, n, k)
+    D = torch.zeros((m, n, k // 32), dtype=torch.int32, device="cuda")
+    q8.check(q8.q8act_debug_gemv_block_dots(cuda(wb), cuda(xq), D, m, n, k))
+    device_ok()
+    assert np.array_equal(host(D), oracle.block_dots(wb, xq, k))
+
+
+@pytest.mark.parametrize("n,k", [(4096, 4096), (4096, 1280), (20480, 4096), (64448, 4096)])
+def test_gemv_serving_shapes_batch_invariant(n, k):
+    """decode == verify: token t's output is bitwise the same for m = 1, 2, 4, 8."""
+    ensure_built()
+    _, _, wb, xq, xd = problem(8, n, k)
+    w_d = cuda(wb)
+    ys = {}
+    for m in (8, 4, 2, 1):
+        ys[m] = host(q8.gemv_q8_0(w_d, cuda(xq[:m]), cuda(xd[:m]), n))
+    device_ok()
+    for m in (4, 2, 1):
+        assert np.array_equal(ys[m].view(np.uint32), ys[8][:m].view(np.uint32)), f"m={m}"
+    again = host(q8.gemv_q8_0(w_d, cuda(xq), cuda(xd), n))
+    assert np.array_equal(again.view(np.uint32), ys[8].view(np.uint32)), "not deterministic"
+    rows = sample_rows(n, 1024)
+    _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
+    assert_within_tolerance(ys[8][:, rows], y64, S)
