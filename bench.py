@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q8_0 x q8_1 hot path on GB300.
+
+One step = one pass of the whole hot path on the headline workload:
+  1. q8_1 quantization of one decode token (k = 4096)
+  2. the decode GEMV, m = 1, 4096 -> 64448 (the LM-head half; 280.5 MB of Q8_0 weights)
+  3. the prefill GEMM, m = 512, 4096 -> 4096, q8_1 quantization fused in the call
+  4. the Q8_0 -> fp16 dequant of the same 4096 x 4096 weights
+L2 is flushed before every kernel, outside the timed kernels: a 256 MiB write, then a
+256 MiB read of another buffer (so that the flush's own dirty lines are written back
+before the timed kernel starts, not during it).
+
+`value` is the decode GEMV's weight-stream throughput in GB/s (algorithmic bytes: weights
++ activation + scales + output); the GEMM's TOPS (2*m*n*k / t) and every kernel's roofline
+fraction are reported alongside.  Usage:
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling:
+the path has no exchange step); rank 0 prints the JSON line with max-over-ranks times.
+`--impl reference` times the CPU oracle (the plain C restatement of the method) on the
+same metric, on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "Q8_0 GEMV GB/s (m=1); Q8_0 MMQ GEMM TOPS (m=512); % of roofline"
+GEMV = dict(m=1, n=64448, k=4096)
+GEMM = dict(m=512, n=4096, k=4096)
+DEQ = dict(n=4096, k=4096)
+WORKLOAD = ("decode GEMV m=1 4096->64448 (q8_1 quantize + mmvq) + prefill GEMM m=512 "
+            "4096->4096 (q8_1 quantize fused) + Q8_0->fp16 dequant 4096x4096")
+FLUSH_BYTES = 256 << 20
+
+
+def row_bytes(k):
+    return k // 32 * 34
+
+
+def gemv_bytes(m, n, k):
+    """Algorithmic bytes of one GEMV: Q8_0 weights + int8 quants + f32 scales + f32 output."""
+    return n * row_bytes(k) + m * k + m * (k // 32) * 4 + m * n * 4
+
+
+def gemm_flops(m, n, k):
+    return 2.0 * m * n * k
+
+
+def dequant_bytes(n, k):
+    return n * row_bytes(k) + 2 * n * k
+
+
+def quantize_bytes(m, k):
+    return 4 * m * k + m * k + m * (k // 32) * 4
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------
+# clocks sampled by nvidia-smi while the timed loop runs
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[2:7], float(parts[7])))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:   # a very short timed region: take the samples nearest to it
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for nm, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "in_timed_region": t0 <= inside[0][0] <= t1}
+
+
+# ------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import q8_block_quantized_act_gb300 as q8
+    from q8_block_quantized_act_gb300 import build as q8build
+    from q8_block_quantized_act_gb300 import inputs
+
+    q8build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs: seeded host f32, quantized to Q8_0 on the device by the library ----
+    def weights_q8(n, k):
+        w32 = torch.from_numpy(inputs.weights_f32(n, k)).to(dev)
+        wq = q8.quantize_q8_0(w32)
+        del w32
+        return wq
+
+    w_gemv = weights_q8(GEMV["n"], GEMV["k"])
+    w_gemm = weights_q8(GEMM["n"], GEMM["k"])
+    x_gemv = torch.from_numpy(inputs.activations_f32(GEMV["m"], GEMV["k"])).to(dev)
+    x_gemm = torch.from_numpy(inputs.activations_f32(GEMM["m"], GEMM["k"])).to(dev)
+    xq = torch.empty((GEMV["m"], GEMV["k"]), dtype=torch.int8, device=dev)
+    xd = torch.empty((GEMV["m"], GEMV["k"] // 32), dtype=torch.float32, device=dev)
+    y_gemv = torch.empty((GEMV["m"], GEMV["n"]), dtype=torch.float32, device=dev)
+    ws = q8.gemm_workspace(GEMM["m"], GEMM["k"], dev)
+    y_gemm = torch.empty((GEMM["m"], GEMM["n"]), dtype=torch.float32, device=dev)
+    w16 = torch.empty((DEQ["n"], DEQ["k"]), dtype=torch.float16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.max()
+
+    def k_quant():
+        q8.check(q8.q8act_quantize_q8_1(x_gemv, xq, xd, GEMV["m"], GEMV["k"], stream))
+
+    def k_gemv():
+        q8.check(q8.q8act_gemv_q8_0(w_gemv, xq, xd, y_gemv, GEMV["m"], GEMV["n"], GEMV["k"], stream))
+
+    def k_gemm():
+        q8.check(q8.q8act_gemm_q8_0(w_gemm, x_gemm, y_gemm, GEMM["m"], GEMM["n"], GEMM["k"], ws,
+                                    ws.numel(), stream))
+
+    def k_deq():
+        q8.check(q8.q8act_dequant_q8_0_f16(w_gemm, w16, DEQ["n"], DEQ["k"], stream))
+
+    parts = [("quantize_q8_1", k_quant), ("gemv_q8_0", k_gemv), ("gemm_q8_0", k_gemm),
+             ("dequant_q8_0_f16", k_deq)]
+    launches_per_step = {"quantize_q8_1": 1, "gemv_q8_0": 1, "gemm_q8_0": 2, "dequant_q8_0_f16": 1}
+
+    def step(events=None):
+        for i, (_, fn) in enumerate(parts):
+            flush_l2()                          # evict L2 before every kernel
+            if events is not None:
+                events[i][0].record(stream)
+            fn()
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    q8.device_status(stream)
+
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in parts] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for s in range(args.steps):
+        step(ev[s])
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.stop()
+    q8.device_status(stream)
+
+    per = {name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
+           for i, (name, _) in enumerate(parts)}
+    mean_ms = {name: float(np.mean(v)) for name, v in per.items()}
+    step_ms = float(sum(mean_ms.values()))
+    if world > 1:
+        t = torch.tensor([step_ms] + [mean_ms[nm] for nm, _ in parts], device=dev,
+                         dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t[0])
+        mean_ms = {nm: float(t[i + 1]) for i, (nm, _) in enumerate(parts)}
+
+    # ---- end to end through the public API: host f32 in (pinned), host f32 out ----
+    e2e = run_e2e(args, q8, torch, dev, stream)
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    comps = {}
+    gb = gemv_bytes(**GEMV)
+    comps["gemv_q8_0"] = roof("hbm", gb / (mean_ms["gemv_q8_0"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                              mean_ms["gemv_q8_0"], gb)
+    comps["quantize_q8_1"] = roof("hbm", quantize_bytes(GEMV["m"], GEMV["k"]) / (mean_ms["quantize_q8_1"] * 1e-3) / 1e9,
+                                  peaks["hbm_gbs"], "GB/s", mean_ms["quantize_q8_1"], quantize_bytes(GEMV["m"], GEMV["k"]))
+    fl = gemm_flops(**GEMM)
+    comps["gemm_q8_0"] = roof("tensor", fl / (mean_ms["gemm_q8_0"] * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s",
+                              mean_ms["gemm_q8_0"], fl)
+    db = dequant_bytes(**DEQ)
+    comps["dequant_q8_0_f16"] = roof("hbm", db / (mean_ms["dequant_q8_0_f16"] * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                     "GB/s", mean_ms["dequant_q8_0_f16"], db)
+    dominant = max(mean_ms, key=lambda nm: mean_ms[nm])
+    traffic = load_traffic(dominant)
+    d = comps[dominant]
+    roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} ({'hbm_gbs' if d['bound'] == 'hbm' else 'bf16_tflops burst; f16 pipe, nominal ratio 1'})"}
+
+    value = comps["gemv_q8_0"]["achieved"] * world
+    cpu = cpu_baseline(args) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    clocks = sampler.summary(t0, t1) if sampler else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded numpy PCG64: weights N(0,0.02) seed 0, activations N(0,1) seed 1)",
+        "config": {"workload": WORKLOAD, "gemv": GEMV, "gemm": GEMM, "dequant": DEQ,
+                   "l2": "flushed before every timed kernel (256 MiB write, then a 256 MiB read)",
+                   "parallelism": f"replicas x{world}"},
+        "gemm_tops": round(comps["gemm_q8_0"]["achieved"], 2),
+        "components": comps,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": sum(launches_per_step.values()) * args.steps,
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    return line
+
+
+def roof(bound, achieved, peak, unit, ms, work):
+    return {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "us": round(ms * 1e3, 3), "work_per_launch": work}
+
+
+KERNEL_SOURCES = {"gemv_q8_0": "gemv.cu", "gemm_q8_0": "gemm.cu", "dequant_q8_0_f16": "dequant.cu",
+                  "quantize_q8_1": "quantize.cu"}
+
+
+def source_sha(kernel):
+    import hashlib
+    p = os.path.join(ROOT, "q8_block_quantized_act_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel):
+    """Per-launch DRAM bytes (read + write) of `kernel` from the committed ncu summary, or
+    None when there is none or the kernel's source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    v = d.get(kernel)
+    if not isinstance(v, dict) or v.get("source_sha") != source_sha(kernel):
+        return None
+    return v.get("bytes_per_launch")
+
+
+def run_e2e(args, q8, torch, dev, stream):
+    """The decode GEMV through the public API with host buffers: pinned host weights and
+    activation are copied in, the activation is quantized, the GEMV runs, y is copied out."""
+    from q8_block_quantized_act_gb300 import inputs
+    m, n, k = GEMV["m"], GEMV["n"], GEMV["k"]
+    w_host = torch.empty((n, row_bytes(k)), dtype=torch.uint8).pin_memory()
+    w_dev_tmp = q8.quantize_q8_0(torch.from_numpy(inputs.weights_f32(n, k)).to(dev))
+    w_host.copy_(w_dev_tmp.cpu())
+    del w_dev_tmp
+    x_host = torch.from_numpy(inputs.activations_f32(m, k)).pin_memory()
+    y_host = torch.empty((m, n), dtype=torch.float32).pin_memory()
+    w_dev = torch.empty_like(w_host, device=dev)
+    x_dev = torch.empty_like(x_host, device=dev)
+    xq = torch.empty((m, k), dtype=torch.int8, device=dev)
+    xd = torch.empty((m, k // 32), dtype=torch.float32, device=dev)
+    y_dev = torch.empty((m, n), dtype=torch.float32, device=dev)
+
+    def one():
+        w_dev.copy_(w_host, non_blocking=True)
+        x_dev.copy_(x_host, non_blocking=True)
+        q8.check(q8.q8act_quantize_q8_1(x_dev, xq, xd, m, k, stream))
+        q8.check(q8.q8act_gemv_q8_0(w_dev, xq, xd, y_dev, m, n, k, stream))
+        y_host.copy_(y_dev, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return {"value": round(gemv_bytes(m, n, k) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(w_host.numel() + x_host.numel() * 4),
+            "d2h_bytes_per_step": int(y_host.numel() * 4), "ms_per_step": round(ms, 4)}
+
+
+# ------------------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline)
+# ------------------------------------------------------------------------------------
+def oracle_gemv_sample(min_seconds=10.0, max_seconds=30.0, rows_per_rep=16384):
+    """Time the oracle on the decode GEMV workload: quantize the token, then the fold over a
+    seeded block of weight rows; repeated (different row blocks) until >= min_seconds."""
+    import oracle
+    from q8_block_quantized_act_gb300 import inputs
+    m, n, k = GEMV["m"], GEMV["n"], GEMV["k"]
+    oracle.build()
+    w = inputs.weights_f32(rows_per_rep, k)
+    wb = oracle.quantize_q8_0(w)
+    x = inputs.activations_f32(m, k)
+    done_bytes, t_total, reps = 0, 0.0, 0
+    while reps == 0 or (t_total < min_seconds and t_total < max_seconds):
+        t = time.perf_counter()
+        xq, xd = oracle.quantize_q8_1(x)
+        oracle.matmul(wb, xq, xd, k)
+        t_total += time.perf_counter() - t
+        done_bytes += gemv_bytes(m, rows_per_rep, k)
+        reps += 1
+    return done_bytes / t_total / 1e9, reps, rows_per_rep, t_total
+
+
+def cpu_baseline(args):
+    gbs, reps, rows, secs = oracle_gemv_sample(min_seconds=args.cpu_seconds)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"decode GEMV m=1, k=4096: {reps} x {rows} weight rows "
+                      f"({reps * rows / GEMV['n']:.2f} x the 64448-row workload), {secs:.1f} s, "
+                      "single-threaded C oracle"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_gemv_sample(min_seconds=0.0, rows_per_rep=1024)
+    t_all = 0.0
+    bytes_all = 0
+    for _ in range(args.steps):
+        gbs, reps, rows, secs = oracle_gemv_sample(min_seconds=0.0, rows_per_rep=4096)
+        per_step.append(secs)
+        t_all += secs
+        bytes_all += gemv_bytes(GEMV["m"], rows, GEMV["k"])
+    value = bytes_all / t_all / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t_all / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "gemv": GEMV},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: the decode GEMV (m=1, k=4096) over 4096 of the "
+                                   "64448 weight rows, single-threaded C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
