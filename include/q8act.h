@@ -139,6 +139,24 @@ int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, f
                          int64_t m, int64_t n, int64_t k, void *stream);
 
 /*
+ * The fused GEMM above for callers that cannot allocate device memory (an allocator's own
+ * hooks, a serving loop that forbids allocation after start-up, a runtime that passes only
+ * the buffers it owns).  No counterpart in the pages: it is an addition of this library.
+ *   w, x, y, m, n, k, stream: as for q8act_gemm_q8_0; no workspace argument.
+ * The activation quants and scales go into one fixed device array of Q8ACT_NOALLOC_WS_BYTES
+ * that the library reserves on every GPU that loads it, until the process exits.  Returns
+ * Q8ACT_ERR_WORKSPACE (nothing launched) when q8act_gemm_workspace_bytes(m, k) exceeds that
+ * size (for k = 4096: m up to 2891).  The call never allocates or frees memory.  Its first
+ * call on a device looks up the array's address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  All calls on a device share
+ * the array and it keeps the previous call's contents; nothing in it needs to start at zero.
+ * Calls that can overlap on the GPU (unordered streams) race on the array.
+ */
+#define Q8ACT_NOALLOC_WS_BYTES (24u << 20)
+int q8act_gemm_q8_0_noalloc(const void *w, const float *x, float *y, int64_t m, int64_t n,
+                            int64_t k, void *stream);
+
+/*
  * Q8_0 -> row-major binary16 dequant (f16_ffi.rs memra_q8_0_dequant_f16, which takes out_f
  * and blocks per row; this call takes k = 32 * blocks per row):
  *   w [n rows of Q8_0 blocks] -> w16 [n][k] binary16, w16 = fp16_rn(f32(d_w) * q).

@@ -34,7 +34,9 @@ EXPORTED = (
     "q8act_mmq_ldm", "q8act_quantize_q8_0", "q8act_gemv_q8_0", "q8act_gemm_workspace_bytes",
     "q8act_gemm_q8_0", "q8act_gemm_q8_0_preq", "q8act_dequant_q8_0_f16",
     "q8act_debug_gemv_block_dots", "q8act_debug_gemm_block_dots", "q8act_device_status",
+    "q8act_gemm_q8_0_noalloc",
 )
+Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 
 
 class Q8ActError(RuntimeError):
@@ -74,6 +76,7 @@ def lib() -> ctypes.CDLL:
                 "q8act_debug_gemv_block_dots": ([P, P, P, I64, I64, I64, P], I32),
                 "q8act_debug_gemm_block_dots": ([P, P, P, I64, I64, I64, P], I32),
                 "q8act_device_status": ([P], I32),
+                "q8act_gemm_q8_0_noalloc": ([P, P, P, I64, I64, I64, P], I32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -164,3 +167,9 @@ def q8act_debug_gemm_block_dots(w, xqh, D, m, n, k, stream=None) -> int:
 
 def q8act_device_status(stream=None) -> int:
     return lib().q8act_device_status(_s(stream))
+
+
+def q8act_gemm_q8_0_noalloc(w, x, y, m, n, k, stream=None) -> int:
+    """The fused GEMM using the library's fixed device scratch instead of a caller workspace
+    (for callers that cannot allocate device memory)."""
+    return lib().q8act_gemm_q8_0_noalloc(_p(w), _p(x), _p(y), m, n, k, _s(stream))

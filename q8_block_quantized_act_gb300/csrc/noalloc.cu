@@ -1,0 +1,68 @@
+// noalloc.cu -- q8act_gemm_q8_0_noalloc: the fused-quantize GEMM for callers that must not
+// allocate device memory.
+//
+// Who needs it: code that runs where cudaMalloc (or any allocator) is off limits -- for
+// example a custom allocator's own hooks, a real-time serving loop that forbids allocation
+// after start-up, or a runtime that hands kernels only the input and output buffers it
+// already owns.  q8act_gemm_q8_0 asks such callers for a workspace they cannot provide.
+//
+// What it does instead: the quantized activation (binary16 quants + transposed scales, the
+// same bytes q8act_gemm_q8_0 writes into its caller's workspace) goes into one fixed device
+// array declared in this file.  Every GPU that loads the library reserves the whole array
+// (Q8ACT_NOALLOC_WS_BYTES) for the life of the process.  The first call on a device looks up
+// the array's device address with cudaGetSymbolAddress while that device is current; later
+// calls reuse the cached address.  The call itself allocates nothing and frees nothing.
+//
+// Sharing rules: every call on a device uses the same array, and the array keeps whatever
+// the previous call left in it.  Nothing in it has to start at zero: each call rewrites all
+// the quants and scales it reads (the scale columns past m are never read).  Two calls whose
+// work can overlap on the GPU -- on different streams without ordering between them -- race
+// on the array and may corrupt each other's results; order them on one stream or with events.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_ws[Q8ACT_NOALLOC_WS_BYTES];
+
+struct NoallocSlot {
+    bool ready = false;
+    void *ptr = nullptr;
+};
+
+NoallocSlot g_noalloc_slots[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+}  // namespace
+
+extern "C" int q8act_gemm_q8_0_noalloc(const void *w, const float *x, float *y, int64_t m,
+                                       int64_t n, int64_t k, void *stream)
+{
+    if (!w || !x || !y) return Q8ACT_ERR_NULL;
+    const size_t need = q8act_gemm_workspace_bytes(m, k);
+    if (need == 0 || n < 1) return Q8ACT_ERR_DIMS;
+    if (need > (size_t)Q8ACT_NOALLOC_WS_BYTES) return Q8ACT_ERR_WORKSPACE;
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return Q8ACT_ERR_CUDA_BASE + (int)e;
+    if (dev < 0 || dev >= kMaxDevices) return Q8ACT_ERR_DEVICE;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        NoallocSlot &s = g_noalloc_slots[dev];
+        if (!s.ready) {
+            // Device `dev` is current here, so this is the array's address on that device.
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_ws);
+            if (e != cudaSuccess) return Q8ACT_ERR_CUDA_BASE + (int)e;
+            s.ptr = p;
+            s.ready = true;
+        }
+        ws = s.ptr;
+    }
+    return q8act_gemm_q8_0(w, x, y, m, n, k, ws, (size_t)Q8ACT_NOALLOC_WS_BYTES, stream);
+}
