@@ -131,8 +131,8 @@ int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t 
 
 /*
  * The GEMM on an activation already quantized by q8act_quantize_q8_1_mmq, so that one
- * quantization feeds several GEMMs (f16_ffi.rs f16_act / try_f16_gemm_pre: "ONE convert
- * feeds every ... weight in the group").
+ * quantization feeds several GEMMs (the grouped dispatch of f16_ffi.rs f16_act /
+ * try_f16_gemm_pre, where a single activation conversion serves every GEMM of a group).
  *   xqh [m][k] binary16 quants, xdt [k/32][q8act_mmq_ldm(m)] f32 scales.
  */
 int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, float *y,
@@ -161,7 +161,7 @@ int q8act_gemm_q8_0_noalloc(const void *w, const float *x, float *y, int64_t m, 
  * and blocks per row; this call takes k = 32 * blocks per row):
  *   w [n rows of Q8_0 blocks] -> w16 [n][k] binary16, w16 = fp16_rn(f32(d_w) * q).
  *   The int8 part is exact in fp16; the only rounding is that of the product (f16_ffi.rs
- *   module doc, "NUMERIC CONFIG").
+ *   module doc, numeric-config paragraph).
  */
 int q8act_dequant_q8_0_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
 

@@ -12,13 +12,13 @@
  *               - synth_w_q8_0: a Q8_0 row is in_f/32 blocks of 34 bytes, an fp16 scale
  *                 at +0 (little endian) followed by 32 int8 quants;
  *               - f32_to_f16_bits: binary16 with round-to-nearest-even;
- *               - module doc: the MMQ floor "folds every k32" (one scale fold per block).
+ *               - module doc: the MMQ floor applies the scales once per 32-wide k block.
  *   [census]    memra-engine 0.113.0, src/bin/decode_kernel_census.rs, fn q8:
  *               row_bytes = in_f/32*(32+2); q8_1 activation = one i8 per column plus a
  *               per-32-block f32 scale; bytes streamed = out_f*row_bytes.
  *   [f16_ffi]   memra-engine 0.81.0, src/memra_engine/f16_ffi.rs
- *               - module doc, "NUMERIC CONFIG": the int8 part of the dequant is exact in
- *                 fp16, rounding enters at the d*q products;
+ *               - module doc, numeric-config paragraph: int8 values are exact in fp16,
+ *                 so the dequant rounds only the d*q products;
  *               - try_f16_gemm / f16_act / build_q8_f16 (W8A8 pilot): amax = max |v|;
  *                 if amax > 0 { d = amax/127; q = (v/d).round().clamp(-127, 127) }.
  *

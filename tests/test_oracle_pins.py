@@ -12,7 +12,7 @@ def test_oracle_pin(pin):
 
 def test_q8_0_bytes_per_weight():
     """34 bytes per 32 weights = 1.0625 B/w, the ratio fp8_ffi.rs (st_e4m3_enabled doc)
-    reports as measured ("exactly 1.06250")."""
+    reports as its measured resident byte ratio."""
     import numpy as np
     for k in (256, 1280, 4096):
         wb = oracle.quantize_q8_0(np.zeros((3, k), dtype=np.float32))
