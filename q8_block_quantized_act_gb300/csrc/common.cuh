@@ -74,19 +74,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the waiting thread is parked by the hardware until the
+// phase completes or about `hint_ns` nanoseconds pass, instead of spinning on the issue slots
+// that the working warps of the same SM sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t WAIT_HINT_NS = 200000;
+
 // Wait until the phase with the given parity has completed.  Returns false (after setting
 // STATUS_TIMEOUT in *status) if that takes longer than WAIT_TIMEOUT_NS.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status)
 {
-#pragma unroll 1
-    for (int i = 0; i < 128; ++i)
-        if (mbar_try_wait(bar, parity))
-            return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity))
-            return true;
+        if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return true;
         if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
             atomicOr(status, STATUS_TIMEOUT);
             return false;

@@ -1,16 +1,58 @@
 // dequant.cu -- Q8_0 -> row-major binary16 (memra-engine 0.81.0 f16_ffi.rs,
 // memra_q8_0_dequant_f16: w16[r][32b+i] = fp16(d_w * q)).
 //
-// HBM-bound: 34 bytes in and 64 bytes out per block.  One lane produces one 16-byte output
-// chunk (8 values), so a warp writes 512 contiguous bytes per step and reads the 272
-// contiguous bytes of 8 blocks.  The int8 quants become binary16 exactly (|q| <= 127), and
-// the product d_w * q is formed by the binary16 multiplier, which rounds the exact product
-// once to nearest even -- the same value as rounding the (exact) f32 product.
+// HBM-bound: 34 bytes in and 64 bytes out per block.  Persistent CTAs stream chunks of
+// whole rows (contiguous, 16-byte aligned) into a shared-memory ring with cp.async.bulk.
+// A warp converts one 272-byte unit (8 blocks = 256 values) at a time: lane j builds the
+// 16-byte output piece j (8 values of block j/4) from shared memory and the warp stores the
+// unit's 512 output bytes with one fully coalesced 16-byte-per-lane store.
+//
+// Arithmetic: the int8 quants become binary16 exactly (|q| <= 127), and the binary16
+// multiplier rounds the exact product d_w * q once, to nearest even -- the same value as
+// rounding the (exact) f32 product, which is how the format's dequant is defined.
 #include "common.cuh"
 #include "launch.h"
 
 namespace q8 {
 namespace {
+
+constexpr int CONV_WARPS = 8;
+constexpr int THREADS = (CONV_WARPS + 1) * 32;   // + one bulk-copy producer warp
+constexpr int MAX_STAGES = 6;
+constexpr int TARGET_CHUNK = 34816;               // bytes of raw rows per stage (<= 128 units)
+
+struct Plan {
+    int G;               // units (272-byte groups) per row
+    int R;               // rows per chunk
+    int stages;
+    uint32_t row_bytes;
+    uint32_t chunk_bytes;
+    int64_t nchunks;
+    size_t off_bar, smem;
+};
+
+Plan make_plan(int64_t n, int64_t k, size_t smem_cap)
+{
+    Plan p{};
+    p.G = (int)(k / 256);
+    p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
+    p.R = (int)(TARGET_CHUNK / p.row_bytes);
+    if (p.R < 1) p.R = 1;
+    if ((int64_t)p.R > n) p.R = (int)n;
+    p.chunk_bytes = (uint32_t)p.R * p.row_bytes;
+    p.nchunks = (n + p.R - 1) / p.R;
+    const size_t room = smem_cap > 2 * MAX_STAGES * 8 + 64 ? smem_cap - 2 * MAX_STAGES * 8 - 64 : 0;
+    int64_t st = (int64_t)(room / p.chunk_bytes);
+    p.stages = (int)(st > MAX_STAGES ? MAX_STAGES : st);
+    p.off_bar = (size_t)p.stages * p.chunk_bytes;
+    p.smem = p.off_bar + 2 * MAX_STAGES * 8;
+    return p;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(const uint8_t *p)
+{
+    return *reinterpret_cast<const uint16_t *>(p);
+}
 
 // Four signed bytes (packed in a 32-bit word) -> two half2 with the same integer values.
 // (b ^ 0x80) is q + 128 in 0..255; the binary16 pattern 0x6400 | u is 1024 + u, so
@@ -25,31 +67,92 @@ __device__ __forceinline__ void bytes_to_half2x2(uint32_t q4, __half2 &lo, __hal
     hi = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
 }
 
-__global__ void __launch_bounds__(256) dequant_q8_0_f16_kernel(const uint8_t *__restrict__ w,
-                                                               uint4 *__restrict__ out,
-                                                               int64_t nchunks)
+__global__ void __launch_bounds__(THREADS, 1)
+    dequant_q8_0_f16_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out, int n, int k,
+                            Plan p, int *status)
 {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
-        const uint8_t *blk = w + (c >> 2) * Q8_0_BYTES;
-        const int sub = (int)(c & 3);
-        const uint16_t *p = reinterpret_cast<const uint16_t *>(blk);  // 2-byte aligned
-        const uint32_t dbits = __ldg(p);
-        const uint16_t *qp = reinterpret_cast<const uint16_t *>(blk + 2 + 8 * sub);
-        const uint32_t q01 = (uint32_t)__ldg(qp + 0) | ((uint32_t)__ldg(qp + 1) << 16);
-        const uint32_t q23 = (uint32_t)__ldg(qp + 2) | ((uint32_t)__ldg(qp + 3) << 16);
-        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
-        __half2 h[4];
-        bytes_to_half2x2(q01, h[0], h[1]);
-        bytes_to_half2x2(q23, h[2], h[3]);
-        uint4 o;
-        uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half2 prod = __hmul2_rn(h[j], d2);
-            ow[j] = *reinterpret_cast<const uint32_t *>(&prod);
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + MAX_STAGES;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CONV_WARPS);
         }
-        __stcs(out + c, o);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int64_t my_chunks =
+        blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (warp == CONV_WARPS) {
+        if (lane == 0) {
+            int64_t issued = 0;
+            for (int64_t i = 0; i < my_chunks; ++i) {
+                const int s = (int)(i % p.stages);
+                if (!mbar_wait(&empty[s], (uint32_t)(((i / p.stages) & 1) ^ 1), status)) break;
+                const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+                const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
+                const uint32_t bytes = (uint32_t)rows * p.row_bytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_g2s(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes, &full[s]);
+                ++issued;
+            }
+            for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
+                mbar_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+        }
+        return;
+    }
+
+    const int jb = lane >> 2;           // block within the unit
+    const int sub = lane & 3;           // 8-value piece within the block
+    for (int64_t i = 0; i < my_chunks; ++i) {
+        const int s = (int)(i % p.stages);
+        const bool ok = mbar_wait(&full[s], (uint32_t)((i / p.stages) & 1), status);
+        if (__any_sync(0xffffffffu, !ok)) break;
+        const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+        const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+        const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
+        const int units = rows * p.G;
+        // Four units per warp step: their shared-memory reads are issued together.
+        constexpr int UNR = 4;
+        for (int u0 = warp; u0 < units; u0 += UNR * CONV_WARPS) {
+            uint32_t dbits[UNR], q01[UNR], q23[UNR];
+#pragma unroll
+            for (int e = 0; e < UNR; ++e) {
+                const int u = u0 + e * CONV_WARPS;
+                const int uu = u < units ? u : u0;   // an in-range unit; its result is not stored
+                const uint8_t *blk = sbase + (size_t)uu * GROUP_BYTES + jb * Q8_0_BYTES;
+                const uint8_t *qp = blk + 2 + 8 * sub;
+                dbits[e] = lds_u16(blk);
+                q01[e] = lds_u16(qp) | (lds_u16(qp + 2) << 16);
+                q23[e] = lds_u16(qp + 4) | (lds_u16(qp + 6) << 16);
+            }
+#pragma unroll
+            for (int e = 0; e < UNR; ++e) {
+                const int u = u0 + e * CONV_WARPS;
+                if (u >= units) break;
+                const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits[e]));
+                __half2 h[4];
+                bytes_to_half2x2(q01[e], h[0], h[1]);
+                bytes_to_half2x2(q23[e], h[2], h[3]);
+                uint4 o;
+                uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2 prod = __hmul2_rn(h[j], d2);
+                    ow[j] = *reinterpret_cast<const uint32_t *>(&prod);
+                }
+                const int row = u / p.G, g = u - row * p.G;
+                // 256 outputs of the unit = 32 pieces of 16 bytes: piece `lane`.
+                __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)g * 256) / 8 + lane, o);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
@@ -58,12 +161,14 @@ __global__ void __launch_bounds__(256) dequant_q8_0_f16_kernel(const uint8_t *__
 cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
                                     int64_t n, int64_t k, cudaStream_t stream)
 {
-    const int64_t nchunks = n * k / 8;
-    int64_t grid = (nchunks + 255) / 256;
-    const int64_t cap = (int64_t)dev.num_sms * 8;
-    if (grid > cap) grid = cap;
-    dequant_q8_0_f16_kernel<<<(int)grid, 256, 0, stream>>>(w, reinterpret_cast<uint4 *>(w16),
-                                                           nchunks);
+    const Plan p = make_plan(n, k, dev.max_smem_optin);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(dequant_q8_0_f16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
+    dequant_q8_0_f16_kernel<<<(int)grid, THREADS, p.smem, stream>>>(
+        w, reinterpret_cast<uint4 *>(w16), (int)n, (int)k, p, dev.status);
     return cudaGetLastError();
 }
 

@@ -12,12 +12,13 @@
 // tensor pipe runs ahead into other accumulator buffers while a block is being folded.
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N, TMEM columns), full k.
-// Warp roles (448 threads):
-//   warps 0-3   converters: raw Q8_0 rows (TMA, 272-byte groups) -> binary16 A tiles in the
-//               128-byte-swizzled K-major layout + f32 weight scales
-//   warps 4-11  fold: tcgen05.ld (16x256b) of a block's D, acc += (d_w * d_a) * D
-//   warp 12     producer: TMA of activation tiles, activation scales and raw weight groups
-//   warp 13     TMEM allocator + single-thread MMA issuer
+// Warp roles (640 threads, 20 warps: a multiple of 4, so registers are not rounded away):
+//   warps 0-1   converters: raw Q8_0 rows (TMA, 272-byte groups) -> binary16 A tiles in the
+//               128-byte-swizzled K-major layout + f32 weight scales (two rows per thread)
+//   warps 2-17  fold: each owns 32 TMEM lanes (its warp index mod 4) x 32 columns;
+//               tcgen05.ld (16x256b) of a block's D, acc += (d_w * d_a) * D in packed f32x2
+//   warp 18     producer: TMA of activation tiles, activation scales and raw weight groups
+//   warp 19     TMEM allocator + single-thread MMA issuer
 #include "common.cuh"
 #include "launch.h"
 
@@ -31,7 +32,7 @@ constexpr int CHUNKS_PER_GROUP = 4;  // a 256-wide raw weight group feeds 4 chun
 
 constexpr int ACT_STAGES = 4;
 constexpr int RAW_STAGES = 2;
-constexpr int A_STAGES = 2;
+constexpr int A_STAGES = 4;
 constexpr int SC_STAGES = 8;
 constexpr int D_BUFS = 4;
 constexpr int TMEM_COLS = 512;
@@ -50,11 +51,12 @@ constexpr int NUM_BARS = 2 * (ACT_STAGES + RAW_STAGES + A_STAGES + SC_STAGES + D
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte base alignment
 
-constexpr int NUM_CONV_WARPS = 4;
-constexpr int NUM_FOLD_WARPS = 8;
-constexpr int PRODUCER_WARP = NUM_CONV_WARPS + NUM_FOLD_WARPS;   // 12
-constexpr int MMA_WARP = PRODUCER_WARP + 1;                      // 13
-constexpr int THREADS = (MMA_WARP + 1) * 32;                     // 448
+constexpr int NUM_CONV_WARPS = 2;
+constexpr int NUM_FOLD_WARPS = 16;
+constexpr int PRODUCER_WARP = NUM_CONV_WARPS + NUM_FOLD_WARPS;   // 18
+constexpr int MMA_WARP = PRODUCER_WARP + 1;                      // 19
+constexpr int THREADS = (MMA_WARP + 1) * 32;                     // 640 (20 warps)
+constexpr int FOLD_COLS = 32;                                    // columns per fold warp
 
 static_assert(OFF_A % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_SC % 128 == 0, "alignment");
 
@@ -115,6 +117,70 @@ __device__ __forceinline__ void tc_ld_16x256b_x8(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 lanes x 256 bits, repeated 4 times along the columns (16 registers), asynchronous:
+// the registers are valid only after tc_wait_ld_bind16.
+__device__ __forceinline__ void tc_ld_16x256b_x4_async(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+template <bool WAIT>
+__device__ __forceinline__ void tc_wait_ld_bind16(uint32_t (&r)[16])
+{
+    if (WAIT) asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+// Asynchronous x8 form: issue the load; the registers are valid only after tc_wait_ld_bind.
+__device__ __forceinline__ void tc_ld_16x256b_x8_async(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Ties 32 registers of an issued tcgen05.ld to a point after tcgen05.wait::ld (the first
+// call waits; later calls only order the registers after it).
+template <bool WAIT>
+__device__ __forceinline__ void tc_wait_ld_bind(uint32_t (&r)[32])
+{
+    if (WAIT) asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
+                   "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+                   "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Packed f32x2 arithmetic (two f32 lanes per instruction, each rounded to nearest even
+// exactly like the scalar mul.rn / fma.rn), through the compiler's builtins so that the
+// operand pairs are allocated as register pairs.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
 // Four signed bytes -> two half2 holding the same integers (exact).
 __device__ __forceinline__ uint2 bytes_to_f16x4(uint32_t q4)
 {
@@ -155,13 +221,11 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *status,
                                               volatile int *abort_flag)
 {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
             atomicOr(status, STATUS_TIMEOUT);
@@ -216,6 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+
 
     if (warp == PRODUCER_WARP) {
         // ------------------------------ TMA producer ------------------------------
@@ -285,19 +350,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp < NUM_CONV_WARPS) {
         // ------------------------------ converters ------------------------------
-        const int r = threadIdx.x;  // row within the tile
+        // Thread t converts rows t and t + 64 of the tile.  For chunk `part` of a raw group,
+        // the 68 bytes of its two blocks start at byte 68*part; the five 16-byte words from
+        // byte 64*part cover them, the data starting at word `part` of that window.
         const int ngroups = nkc / CHUNKS_PER_GROUP;
         for (int g = 0; g < ngroups; ++g) {
             const int rs = g % RAW_STAGES;
             if (!wait_or_abort(&bars.raw_full[rs], (g / RAW_STAGES) & 1, status, abort_flag)) break;
-            uint32_t wv[GROUP_BYTES / 4];
-            const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RAW_TILE_BYTES + r * GROUP_BYTES);
-#pragma unroll
-            for (int c = 0; c < GROUP_BYTES / 16; ++c) {
-                const uint4 v = src[c];
-                wv[4 * c + 0] = v.x; wv[4 * c + 1] = v.y; wv[4 * c + 2] = v.z; wv[4 * c + 3] = v.w;
-            }
-            mbar_arrive(&bars.raw_empty[rs]);
             bool ok = true;
 #pragma unroll
             for (int part = 0; part < CHUNKS_PER_GROUP; ++part) {
@@ -309,44 +368,61 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                // blocks 2*part (even: scale in the low half of word 17*part, quants straddle
-                // words) and 2*part+1 (odd: scale in the high half of word 17*part+8).
-                const int w0 = 17 * part;
-                const int w1 = 17 * part + 8;
-                uint8_t *arow = smem + OFF_A + aslot * A_TILE_BYTES + r * 128;
-                const int sw = r & 7;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t q0 = __byte_perm(wv[w0 + 2 * c], wv[w0 + 2 * c + 1], 0x5432);
-                    const uint32_t q1 = __byte_perm(wv[w0 + 2 * c + 1], wv[w0 + 2 * c + 2], 0x5432);
-                    const uint2 lo = bytes_to_f16x4(q0), hi = bytes_to_f16x4(q1);
-                    *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint2 lo = bytes_to_f16x4(wv[w1 + 1 + 2 * c]);
-                    const uint2 hi = bytes_to_f16x4(wv[w1 + 2 + 2 * c]);
-                    *reinterpret_cast<uint4 *>(arow + (((c + 4) ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-                }
                 float *wsc = reinterpret_cast<float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4);
-                wsc[r] = half_bits_to_float(wv[w0] & 0xffffu);
-                wsc[BM + r] = half_bits_to_float(wv[w1] >> 16);
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = threadIdx.x + 64 * rr;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        smem + OFF_RAW + rs * RAW_TILE_BYTES + r * GROUP_BYTES + 64 * part);
+                    uint32_t wv[20];
+#pragma unroll
+                    for (int c = 0; c < 5; ++c) {
+                        const uint4 v = src[c];
+                        wv[4 * c + 0] = v.x; wv[4 * c + 1] = v.y; wv[4 * c + 2] = v.z; wv[4 * c + 3] = v.w;
+                    }
+                    // block 2*part: scale in the low half of data word 0, quants straddle words;
+                    // block 2*part+1: scale in the high half of data word 8, quants in words 9..16.
+                    const int w0 = part;
+                    const int w1 = part + 8;
+                    uint8_t *arow = smem + OFF_A + aslot * A_TILE_BYTES + r * 128;
+                    const int sw = r & 7;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t q0 = __byte_perm(wv[w0 + 2 * c], wv[w0 + 2 * c + 1], 0x5432);
+                        const uint32_t q1 = __byte_perm(wv[w0 + 2 * c + 1], wv[w0 + 2 * c + 2], 0x5432);
+                        const uint2 lo = bytes_to_f16x4(q0), hi = bytes_to_f16x4(q1);
+                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint2 lo = bytes_to_f16x4(wv[w1 + 1 + 2 * c]);
+                        const uint2 hi = bytes_to_f16x4(wv[w1 + 2 + 2 * c]);
+                        *reinterpret_cast<uint4 *>(arow + (((c + 4) ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    }
+                    wsc[r] = half_bits_to_float(wv[w0] & 0xffffu);
+                    wsc[BM + r] = half_bits_to_float(wv[w1] >> 16);
+                }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars.a_full[aslot]);
                 mbar_arrive(&bars.sc_full[ss]);
+                if (part == CHUNKS_PER_GROUP - 1) mbar_arrive(&bars.raw_empty[rs]);
             }
             if (!ok) break;
         }
     } else {
         // ------------------------------ fold warps ------------------------------
-        const int fw = warp - NUM_CONV_WARPS;      // 0..7
+        const int fw = warp - NUM_CONV_WARPS;      // 0..15
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
-        const int half = fw >> 2;                  // columns 64*half .. +63
+        const int cq = fw >> 2;                    // columns FOLD_COLS*cq .. +FOLD_COLS-1
         const int tr = lane >> 2;                  // row within a 16-lane group (and +8)
         const int tc = 2 * (lane & 3);             // column pair within each 8 columns
-        float acc[2][32];
+        constexpr int NJ = FOLD_COLS / 8;
+        // acc[hl][j][e]: rows tr + 8e of the 16-lane half hl, columns (8j+tc, 8j+tc+1).
+        float2 acc[2][NJ][2];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) { acc[0][i] = 0.0f; acc[1][i] = 0.0f; }
+        for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) { acc[hl][j][0] = make_float2(0.f, 0.f); acc[hl][j][1] = make_float2(0.f, 0.f); }
 
         for (int b = 0; b < nb; ++b) {
             const int kc = b >> 1;
@@ -356,41 +432,51 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_or_abort(&bars.d_full[buf], (b / D_BUFS) & 1, status, abort_flag)) break;
             if (!wait_or_abort(&bars.sc_full[ss], (kc / SC_STAGES) & 1, status, abort_flag)) break;
             tc_fence_after();
-            const float *asc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES) + blk * BN + 64 * half + tc;
-            const float *wsc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4) + blk * BM + 32 * quarter + tr;
-#pragma unroll
-            for (int hl = 0; hl < 2; ++hl) {
-                const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter + 16 * hl) << 16) + (uint32_t)(buf * BN + 64 * half);
-                float dv[32];
-                tc_ld_16x256b_x8(taddr, dv);
-                const float dw0 = wsc[16 * hl];
-                const float dw1 = wsc[16 * hl + 8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float2 da = *reinterpret_cast<const float2 *>(asc + 8 * j);
-                    float *a = &acc[hl][4 * j];
-                    const float *d = &dv[4 * j];
-                    if (DOTS) {
-                        const int rr = row0 + 32 * quarter + 16 * hl + tr;
-                        const int tt = tok0 + 64 * half + 8 * j + tc;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int r_e = rr + 8 * (e >> 1), t_e = tt + (e & 1);
-                            if (r_e < n && t_e < m)
-                                dots[((int64_t)t_e * n + r_e) * nb + b] = __float2int_rn(d[e]);
-                        }
-                    } else {
-                        a[0] = __fmaf_rn(__fmul_rn(dw0, da.x), d[0], a[0]);
-                        a[1] = __fmaf_rn(__fmul_rn(dw0, da.y), d[1], a[1]);
-                        a[2] = __fmaf_rn(__fmul_rn(dw1, da.x), d[2], a[2]);
-                        a[3] = __fmaf_rn(__fmul_rn(dw1, da.y), d[3], a[3]);
-                    }
-                }
-            }
+            // Both 16-lane halves of this warp's 32 x 32 slice of the block's accumulator.
+            uint32_t d0[16], d1[16];
+            const uint32_t tcol = (uint32_t)(buf * BN + FOLD_COLS * cq);
+            tc_ld_16x256b_x4_async(tmem_base + ((uint32_t)(32 * quarter) << 16) + tcol, d0);
+            tc_ld_16x256b_x4_async(tmem_base + ((uint32_t)(32 * quarter + 16) << 16) + tcol, d1);
+            tc_wait_ld_bind16<true>(d0);
+            tc_wait_ld_bind16<false>(d1);
+            // The accumulator buffer is free for the next MMA as soon as it sits in registers.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.d_empty[buf]);
-            if (blk == 1 || b == nb - 1) {
+
+            const float *asc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES) + blk * BN + FOLD_COLS * cq + tc;
+            const float *wsc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4) + blk * BM + 32 * quarter + tr;
+            if (DOTS) {
+#pragma unroll
+                for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
+                            const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
+                            const uint32_t v = hl ? d1[4 * j + e] : d0[4 * j + e];
+                            if (r_e < n && t_e < m)
+                                dots[((int64_t)t_e * n + r_e) * nb + b] = __float2int_rn(__uint_as_float(v));
+                        }
+            } else {
+                const float dw00 = wsc[0], dw01 = wsc[8], dw10 = wsc[16], dw11 = wsc[24];
+                const float2 w00 = make_float2(dw00, dw00), w01 = make_float2(dw01, dw01);
+                const float2 w10 = make_float2(dw10, dw10), w11 = make_float2(dw11, dw11);
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const float2 da = *reinterpret_cast<const float2 *>(asc + 8 * j);
+                    const float2 a0 = make_float2(__uint_as_float(d0[4 * j + 0]), __uint_as_float(d0[4 * j + 1]));
+                    const float2 a1 = make_float2(__uint_as_float(d0[4 * j + 2]), __uint_as_float(d0[4 * j + 3]));
+                    const float2 b0 = make_float2(__uint_as_float(d1[4 * j + 0]), __uint_as_float(d1[4 * j + 1]));
+                    const float2 b1 = make_float2(__uint_as_float(d1[4 * j + 2]), __uint_as_float(d1[4 * j + 3]));
+                    acc[0][j][0] = fma2_rn(mul2_rn(w00, da), a0, acc[0][j][0]);
+                    acc[0][j][1] = fma2_rn(mul2_rn(w01, da), a1, acc[0][j][1]);
+                    acc[1][j][0] = fma2_rn(mul2_rn(w10, da), b0, acc[1][j][0]);
+                    acc[1][j][1] = fma2_rn(mul2_rn(w11, da), b1, acc[1][j][1]);
+                }
+            }
+            if (blk == 1) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.sc_empty[ss]);
             }
@@ -399,12 +485,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < NJ; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
-                        const int t_e = tok0 + 64 * half + 8 * j + tc + (e & 1);
-                        if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = acc[hl][4 * j + e];
+                        const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
+                        const float2 v = acc[hl][j][e >> 1];
+                        if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = (e & 1) ? v.y : v.x;
                     }
         }
     }

@@ -12,8 +12,10 @@
 //     (4 x dp4a per block per token) and folded as acc += (d_w * d_a) * D;
 //   * the activation (m x k int8 + scales) sits in shared memory for the whole kernel, padded
 //     so that neighbouring units hit different banks;
-//   * the per-row sum over units uses a fixed order, so token t's result is the same
-//     sequence of operations for every m (the pages' decode == verify law).
+//   * the per-row sum over units uses a fixed order -- a butterfly of warp shuffles when a
+//     row's units are consecutive lanes of one warp, else a shared-memory pass -- so token
+//     t's result is the same sequence of operations for every m (the pages' decode == verify
+//     law, fp8_ffi.rs and f16_ffi.rs module docs).
 #include "common.cuh"
 #include "launch.h"
 
@@ -32,6 +34,8 @@ struct Plan {
     int R;              // rows per chunk
     int U;              // units per chunk (R * G)
     int stages;
+    int ctas_per_sm;    // resident CTAs per SM the shared-memory plan allows
+    int warp_reduce;    // 1: a row's units are consecutive lanes of one warp (G divides 32)
     uint32_t row_bytes;
     uint32_t chunk_bytes;
     int64_t nchunks;
@@ -61,7 +65,21 @@ Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap)
     p.off_part = p.off_xd + xd_bytes;
     p.off_bar = (p.off_part + part_bytes + 7) & ~(size_t)7;
     p.smem = p.off_bar + 2 * MAX_STAGES * 8;
+    p.ctas_per_sm = 1;
+    p.warp_reduce = (p.G <= 32 && 32 % p.G == 0) ? 1 : 0;
     return p;
+}
+
+// Two CTAs per SM when two rings of at least 3 stages fit, else one CTA with up to 6 stages.
+Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
+{
+    const size_t half = 113 * 1024;
+    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin);
+    if (p.stages >= 3) {
+        p.ctas_per_sm = 2;
+        return p;
+    }
+    return make_plan(m, n, k, smem_optin);
 }
 
 __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
@@ -79,7 +97,7 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
 }
 
 template <int M, bool DOTS>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     gemv_q8_0_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq,
                      const float *__restrict__ xd, float *__restrict__ y,
                      int32_t *__restrict__ dots, int n, int k, Plan p, int *status)
@@ -147,7 +165,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = (int)(i % p.stages);
         const uint32_t ph = (uint32_t)((i / p.stages) & 1);
         const bool ok = mbar_wait(&full[s], ph, status);
-        if (bar_red_or(1, CONSUMERS, !ok)) break;
+        // Leave together: the whole CTA when rows are reduced through shared memory, the
+        // whole warp when they are reduced with shuffles.
+        if (p.warp_reduce ? __any_sync(0xffffffffu, !ok) : bar_red_or(1, CONSUMERS, !ok)) break;
 
         const int64_t chunk = blockIdx.x + i * gridDim.x;
         const int64_t row0 = chunk * p.R;
@@ -155,72 +175,90 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
         float *pbuf = part + (size_t)(i & 1) * p.U * M;
 
-        for (int u = tid; u < p.U; u += CONSUMERS) {
+        // In shuffle mode every lane of a warp takes part (lanes past the last unit act as
+        // empty units of rows beyond `rows`).
+        const int ulimit = p.warp_reduce ? (p.U + 31) / 32 * 32 : p.U;
+        for (int u = tid; u < ulimit; u += CONSUMERS) {
             const int row = u / G;
             const int g = u - row * G;
-            if (row >= rows) continue;
-            const uint4 *src =
-                reinterpret_cast<const uint4 *>(sbase + (size_t)row * p.row_bytes + g * GROUP_BYTES);
-            uint32_t wv[UNIT_WORDS];
-#pragma unroll
-            for (int c = 0; c < UNIT_WORDS / 4; ++c) {
-                const uint4 v = src[c];
-                wv[4 * c + 0] = v.x;
-                wv[4 * c + 1] = v.y;
-                wv[4 * c + 2] = v.z;
-                wv[4 * c + 3] = v.w;
-            }
             float acc[M];
 #pragma unroll
             for (int t = 0; t < M; ++t) acc[t] = 0.0f;
-            const uint32_t *xg = xs + g * XG_WORDS;
-            const float *xdg = xds + g * XDG_WORDS;
+            if (row < rows) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(sbase + (size_t)row * p.row_bytes +
+                                                                   g * GROUP_BYTES);
+                uint32_t wv[UNIT_WORDS];
 #pragma unroll
-            for (int j = 0; j < GROUP_BLOCKS; ++j) {
-                // Block j of the unit starts at byte 34j: even j at word 17(j/2) (scale in
-                // the low half, quants straddle words), odd j with its scale in the high half
-                // of word 17(j/2)+8 and word-aligned quants after it.
-                uint32_t q[8];
-                uint32_t dbits;
-                if ((j & 1) == 0) {
-                    const int w0 = 17 * (j >> 1);
-                    dbits = wv[w0] & 0xffffu;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) q[e] = __byte_perm(wv[w0 + e], wv[w0 + e + 1], 0x5432);
-                } else {
-                    const int w1 = 17 * (j >> 1) + 8;
-                    dbits = wv[w1] >> 16;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) q[e] = wv[w1 + 1 + e];
+                for (int c = 0; c < UNIT_WORDS / 4; ++c) {
+                    const uint4 v = src[c];
+                    wv[4 * c + 0] = v.x;
+                    wv[4 * c + 1] = v.y;
+                    wv[4 * c + 2] = v.z;
+                    wv[4 * c + 3] = v.w;
                 }
-                const float dw = half_bits_to_float(dbits);
+                const uint32_t *xg = xs + g * XG_WORDS;
+                const float *xdg = xds + g * XDG_WORDS;
 #pragma unroll
-                for (int t = 0; t < M; ++t) {
-                    const uint4 *xv = reinterpret_cast<const uint4 *>(xg + t * G * XG_WORDS + j * 8);
-                    const uint4 a = xv[0], b = xv[1];
-                    int D = dp4a(q[0], a.x, 0);
-                    D = dp4a(q[1], a.y, D);
-                    D = dp4a(q[2], a.z, D);
-                    D = dp4a(q[3], a.w, D);
-                    D = dp4a(q[4], b.x, D);
-                    D = dp4a(q[5], b.y, D);
-                    D = dp4a(q[6], b.z, D);
-                    D = dp4a(q[7], b.w, D);
-                    if (DOTS) {
-                        dots[((int64_t)t * n + row0 + row) * nb + g * GROUP_BLOCKS + j] = D;
+                for (int j = 0; j < GROUP_BLOCKS; ++j) {
+                    // Block j of the unit starts at byte 34j: even j at word 17(j/2) (scale in
+                    // the low half, quants straddle words), odd j with its scale in the high
+                    // half of word 17(j/2)+8 and word-aligned quants after it.
+                    uint32_t q[8];
+                    uint32_t dbits;
+                    if ((j & 1) == 0) {
+                        const int w0 = 17 * (j >> 1);
+                        dbits = wv[w0] & 0xffffu;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) q[e] = __byte_perm(wv[w0 + e], wv[w0 + e + 1], 0x5432);
                     } else {
-                        const float da = xdg[t * G * XDG_WORDS + j];
-                        acc[t] = __fmaf_rn(__fmul_rn(dw, da), __int2float_rn(D), acc[t]);
+                        const int w1 = 17 * (j >> 1) + 8;
+                        dbits = wv[w1] >> 16;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) q[e] = wv[w1 + 1 + e];
+                    }
+                    const float dw = half_bits_to_float(dbits);
+#pragma unroll
+                    for (int t = 0; t < M; ++t) {
+                        const uint4 *xv = reinterpret_cast<const uint4 *>(xg + t * G * XG_WORDS + j * 8);
+                        const uint4 a = xv[0], b = xv[1];
+                        int D = dp4a(q[0], a.x, 0);
+                        D = dp4a(q[1], a.y, D);
+                        D = dp4a(q[2], a.z, D);
+                        D = dp4a(q[3], a.w, D);
+                        D = dp4a(q[4], b.x, D);
+                        D = dp4a(q[5], b.y, D);
+                        D = dp4a(q[6], b.z, D);
+                        D = dp4a(q[7], b.w, D);
+                        if (DOTS) {
+                            dots[((int64_t)t * n + row0 + row) * nb + g * GROUP_BLOCKS + j] = D;
+                        } else {
+                            const float da = xdg[t * G * XDG_WORDS + j];
+                            acc[t] = __fmaf_rn(__fmul_rn(dw, da), __int2float_rn(D), acc[t]);
+                        }
                     }
                 }
             }
-            if (!DOTS) {
+            if (DOTS) continue;
+            if (p.warp_reduce) {
+                // The row's G units sit in G consecutive lanes (G divides 32): butterfly sum,
+                // the same fixed sequence of additions for every m.
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    if (o >= G) break;
+#pragma unroll
+                    for (int t = 0; t < M; ++t) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xffffffffu, acc[t], o));
+                }
+                if (g == 0 && row < rows) {
+#pragma unroll
+                    for (int t = 0; t < M; ++t) y[(int64_t)t * n + row0 + row] = acc[t];
+                }
+            } else {
 #pragma unroll
                 for (int t = 0; t < M; ++t) pbuf[u * M + t] = acc[t];
             }
         }
         mbar_arrive(&empty[s]);  // this stage's bytes are no longer needed
-        if (DOTS) continue;
+        if (DOTS || p.warp_reduce) continue;
         named_bar_sync(1, CONSUMERS);
         for (int idx = tid; idx < rows * M; idx += CONSUMERS) {
             const int t = idx / rows, r = idx - t * rows;
@@ -236,13 +274,14 @@ template <int M, bool DOTS>
 cudaError_t launch_m(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
                      float *y, int32_t *dots, int64_t n, int64_t k, cudaStream_t stream)
 {
-    const Plan p = make_plan(M, n, k, dev.max_smem_optin);
+    const Plan p = choose_plan(M, n, k, dev.max_smem_optin);
     if (p.stages < 2) return cudaErrorInvalidValue;
     auto kern = gemv_q8_0_kernel<M, DOTS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)p.smem);
     if (e != cudaSuccess) return e;
-    int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
+    const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
+    int64_t grid = p.nchunks < slots ? p.nchunks : slots;
     kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)n, (int)k, p,
                                                   dev.status);
     return cudaGetLastError();
@@ -271,7 +310,7 @@ cudaError_t dispatch(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, 
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 {
     if (m < 1 || m > Q8ACT_GEMV_MAX_M) return false;
-    return make_plan(m, 1 << 20, k, dev.max_smem_optin).stages >= 2;
+    return choose_plan(m, 1 << 20, k, dev.max_smem_optin).stages >= 2;
 }
 
 cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
