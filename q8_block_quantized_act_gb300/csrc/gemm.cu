@@ -30,11 +30,10 @@ constexpr int BN = 128;            // tokens per tile
 constexpr int KC = 64;             // k per chunk (one 128-byte swizzle row of binary16)
 constexpr int CHUNKS_PER_GROUP = 4;  // a 256-wide raw weight group feeds 4 chunks
 
-constexpr int ACT_STAGES = 4;
+constexpr int STAGES = 4;          // k chunks in flight: activation tile + converted weight tile
 constexpr int RAW_STAGES = 2;
-constexpr int A_STAGES = 4;
 constexpr int SC_STAGES = 8;
-constexpr int D_BUFS = 4;
+constexpr int D_PAIRS = 2;         // TMEM accumulator buffers, handed over in pairs (one chunk)
 constexpr int TMEM_COLS = 512;
 
 constexpr int ACT_TILE_BYTES = BN * KC * 2;        // 16384
@@ -43,11 +42,11 @@ constexpr int RAW_TILE_BYTES = BM * GROUP_BYTES;   // 34816
 constexpr int SC_SLOT_BYTES = 2 * BN * 4 + 2 * BM * 4;  // act scales [2][BN], weight scales [2][BM]
 
 constexpr int OFF_ACT = 0;
-constexpr int OFF_A = OFF_ACT + ACT_STAGES * ACT_TILE_BYTES;
-constexpr int OFF_RAW = OFF_A + A_STAGES * A_TILE_BYTES;
+constexpr int OFF_A = OFF_ACT + STAGES * ACT_TILE_BYTES;
+constexpr int OFF_RAW = OFF_A + STAGES * A_TILE_BYTES;
 constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_TILE_BYTES;
 constexpr int OFF_BAR = OFF_SC + SC_STAGES * SC_SLOT_BYTES;
-constexpr int NUM_BARS = 2 * (ACT_STAGES + RAW_STAGES + A_STAGES + SC_STAGES + D_BUFS) + 1;
+constexpr int NUM_BARS = 2 * (STAGES + RAW_STAGES + SC_STAGES + D_PAIRS) + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte base alignment
 
@@ -194,25 +193,27 @@ __device__ __forceinline__ uint2 bytes_to_f16x4(uint32_t q4)
                       *reinterpret_cast<const uint32_t *>(&hb));
 }
 
+// Barriers.  stage_full[s] completes when chunk s's activation tile has landed (TMA bytes)
+// and the converters have written its weight tile; stage_empty[s] when the MMAs reading
+// both have completed.  pair_full[p] / pair_empty[p] hand the two accumulator buffers of
+// one chunk between the MMA issuer and the fold warps.
 struct Bars {
-    uint64_t *act_full, *act_empty, *raw_full, *raw_empty, *a_full, *a_empty, *sc_full,
-        *sc_empty, *d_full, *d_empty, *mma_done;
+    uint64_t *stage_full, *stage_empty, *raw_full, *raw_empty, *sc_full, *sc_empty,
+        *pair_full, *pair_empty, *mma_done;
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t *base)
 {
     uint64_t *b = reinterpret_cast<uint64_t *>(base);
     Bars r;
-    r.act_full = b; b += ACT_STAGES;
-    r.act_empty = b; b += ACT_STAGES;
+    r.stage_full = b; b += STAGES;
+    r.stage_empty = b; b += STAGES;
     r.raw_full = b; b += RAW_STAGES;
     r.raw_empty = b; b += RAW_STAGES;
-    r.a_full = b; b += A_STAGES;
-    r.a_empty = b; b += A_STAGES;
     r.sc_full = b; b += SC_STAGES;
     r.sc_empty = b; b += SC_STAGES;
-    r.d_full = b; b += D_BUFS;
-    r.d_empty = b; b += D_BUFS;
+    r.pair_full = b; b += D_PAIRS;
+    r.pair_empty = b; b += D_PAIRS;
     r.mma_done = b;
     return r;
 }
@@ -257,11 +258,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nb = k / QK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ACT_STAGES; ++s) { mbar_init(&bars.act_full[s], 1); mbar_init(&bars.act_empty[s], 1); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&bars.stage_full[s], 1 + 32 * NUM_CONV_WARPS); mbar_init(&bars.stage_empty[s], 1); }
         for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], 32 * NUM_CONV_WARPS); }
-        for (int s = 0; s < A_STAGES; ++s) { mbar_init(&bars.a_full[s], 32 * NUM_CONV_WARPS); mbar_init(&bars.a_empty[s], 1); }
         for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + 32 * NUM_CONV_WARPS); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
-        for (int s = 0; s < D_BUFS; ++s) { mbar_init(&bars.d_full[s], 1); mbar_init(&bars.d_empty[s], NUM_FOLD_WARPS); }
+        for (int s = 0; s < D_PAIRS; ++s) { mbar_init(&bars.pair_full[s], 1); mbar_init(&bars.pair_empty[s], NUM_FOLD_WARPS); }
         mbar_init(bars.mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -296,10 +296,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 &bars.raw_full[rs]);
                     ++issued_raw;
                 }
-                const int as = kc % ACT_STAGES;
-                if (!wait_or_abort(&bars.act_empty[as], ((kc / ACT_STAGES) & 1) ^ 1, status, abort_flag)) break;
-                mbar_arrive_expect_tx(&bars.act_full[as], ACT_TILE_BYTES);
-                tma_load_2d(smem + OFF_ACT + as * ACT_TILE_BYTES, &tm_x, kc * KC, tok0, &bars.act_full[as]);
+                const int st = kc % STAGES;
+                if (!wait_or_abort(&bars.stage_empty[st], ((kc / STAGES) & 1) ^ 1, status, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES);
+                tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, kc * KC, tok0, &bars.stage_full[st]);
                 ++issued_act;
                 const int ss = kc % SC_STAGES;
                 if (!wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) break;
@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // Drain: never leave with a copy into this CTA's shared memory in flight.
             for (int i = issued_raw > RAW_STAGES ? issued_raw - RAW_STAGES : 0; i < issued_raw; ++i)
                 mbar_wait(&bars.raw_full[i % RAW_STAGES], (i / RAW_STAGES) & 1, status);
-            for (int i = issued_act > ACT_STAGES ? issued_act - ACT_STAGES : 0; i < issued_act; ++i)
-                mbar_wait(&bars.act_full[i % ACT_STAGES], (i / ACT_STAGES) & 1, status);
+            for (int i = issued_act > STAGES ? issued_act - STAGES : 0; i < issued_act; ++i)
+                mbar_wait(&bars.stage_full[i % STAGES], (i / STAGES) & 1, status);
             for (int i = issued_sc > SC_STAGES ? issued_sc - SC_STAGES : 0; i < issued_sc; ++i)
                 mbar_wait(&bars.sc_full[i % SC_STAGES], (i / SC_STAGES) & 1, status);
         }
@@ -319,30 +319,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             for (int kc = 0; kc < nkc; ++kc) {
-                const int as = kc % ACT_STAGES;
-                const int aslot = kc % A_STAGES;
-                if (!wait_or_abort(&bars.act_full[as], (kc / ACT_STAGES) & 1, status, abort_flag)) break;
-                if (!wait_or_abort(&bars.a_full[aslot], (kc / A_STAGES) & 1, status, abort_flag)) break;
+                const int st = kc % STAGES;
+                const int pr = kc & 1;
+                if (!wait_or_abort(&bars.stage_full[st], (kc / STAGES) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&bars.pair_empty[pr], ((kc >> 1) & 1) ^ 1, status, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + OFF_A + aslot * A_TILE_BYTES);
-                const uint32_t b_addr = smem_u32(smem + OFF_ACT + as * ACT_TILE_BYTES);
-                bool ok = true;
+                const uint32_t a_addr = smem_u32(smem + OFF_A + st * A_TILE_BYTES);
+                const uint32_t b_addr = smem_u32(smem + OFF_ACT + st * ACT_TILE_BYTES);
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int b = 2 * kc + h;
-                    const int buf = b % D_BUFS;
-                    if (!wait_or_abort(&bars.d_empty[buf], ((b / D_BUFS) & 1) ^ 1, status, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                    // block 2kc+h -> accumulator buffer 2*pr+h
+                    const uint32_t d_tmem = tmem_base + (uint32_t)((2 * pr + h) * BN);
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const uint32_t off = (uint32_t)(h * 64 + kk * 32);
                         tc_mma_f16(d_tmem, smem_desc_sw128(a_addr + off), smem_desc_sw128(b_addr + off), kk);
                     }
-                    tc_commit(&bars.d_full[buf]);
                 }
-                if (!ok) break;
-                tc_commit(&bars.act_empty[as]);
-                tc_commit(&bars.a_empty[aslot]);
+                tc_commit(&bars.pair_full[pr]);
+                tc_commit(&bars.stage_empty[st]);
             }
             // All MMAs issued by this thread have completed once this arrives.
             tc_commit(bars.mma_done);
@@ -361,9 +356,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int part = 0; part < CHUNKS_PER_GROUP; ++part) {
                 const int kc = g * CHUNKS_PER_GROUP + part;
-                const int aslot = kc % A_STAGES;
+                const int aslot = kc % STAGES;
                 const int ss = kc % SC_STAGES;
-                if (!wait_or_abort(&bars.a_empty[aslot], ((kc / A_STAGES) & 1) ^ 1, status, abort_flag) ||
+                if (!wait_or_abort(&bars.stage_empty[aslot], ((kc / STAGES) & 1) ^ 1, status, abort_flag) ||
                     !wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) {
                     ok = false;
                     break;
@@ -403,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     wsc[BM + r] = half_bits_to_float(wv[w1] >> 16);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars.a_full[aslot]);
+                mbar_arrive(&bars.stage_full[aslot]);
                 mbar_arrive(&bars.sc_full[ss]);
                 if (part == CHUNKS_PER_GROUP - 1) mbar_arrive(&bars.raw_empty[rs]);
             }
@@ -424,62 +419,64 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < NJ; ++j) { acc[hl][j][0] = make_float2(0.f, 0.f); acc[hl][j][1] = make_float2(0.f, 0.f); }
 
-        for (int b = 0; b < nb; ++b) {
-            const int kc = b >> 1;
-            const int blk = b & 1;
+        for (int kc = 0; kc < nkc; ++kc) {
             const int ss = kc % SC_STAGES;
-            const int buf = b % D_BUFS;
-            if (!wait_or_abort(&bars.d_full[buf], (b / D_BUFS) & 1, status, abort_flag)) break;
+            const int pr = kc & 1;
+            if (!wait_or_abort(&bars.pair_full[pr], (kc >> 1) & 1, status, abort_flag)) break;
             if (!wait_or_abort(&bars.sc_full[ss], (kc / SC_STAGES) & 1, status, abort_flag)) break;
             tc_fence_after();
-            // Both 16-lane halves of this warp's 32 x 32 slice of the block's accumulator.
-            uint32_t d0[16], d1[16];
-            const uint32_t tcol = (uint32_t)(buf * BN + FOLD_COLS * cq);
-            tc_ld_16x256b_x4_async(tmem_base + ((uint32_t)(32 * quarter) << 16) + tcol, d0);
-            tc_ld_16x256b_x4_async(tmem_base + ((uint32_t)(32 * quarter + 16) << 16) + tcol, d1);
-            tc_wait_ld_bind16<true>(d0);
-            tc_wait_ld_bind16<false>(d1);
-            // The accumulator buffer is free for the next MMA as soon as it sits in registers.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.d_empty[buf]);
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                const int b = 2 * kc + blk;
+                // Both 16-lane halves of this warp's 32 x 32 slice of the block's accumulator.
+                uint32_t d0[16], d1[16];
+                const uint32_t tcol = (uint32_t)((2 * pr + blk) * BN + FOLD_COLS * cq);
+                tc_ld_16x256b_x4_async(tmem_base + ((uint32_t)(32 * quarter) << 16) + tcol, d0);
+                tc_ld_16x256b_x4_async(tmem_base + ((uint32_t)(32 * quarter + 16) << 16) + tcol, d1);
+                tc_wait_ld_bind16<true>(d0);
+                tc_wait_ld_bind16<false>(d1);
+                if (blk == 1) {
+                    // Both buffers of the pair sit in registers (or are folded): hand them back.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.pair_empty[pr]);
+                }
 
-            const float *asc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES) + blk * BN + FOLD_COLS * cq + tc;
-            const float *wsc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4) + blk * BM + 32 * quarter + tr;
-            if (DOTS) {
+                const float *asc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES) + blk * BN + FOLD_COLS * cq + tc;
+                const float *wsc = reinterpret_cast<const float *>(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4) + blk * BM + 32 * quarter + tr;
+                if (DOTS) {
 #pragma unroll
-                for (int hl = 0; hl < 2; ++hl)
+                    for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                    for (int j = 0; j < NJ; ++j)
+                        for (int j = 0; j < NJ; ++j)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
-                            const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
-                            const uint32_t v = hl ? d1[4 * j + e] : d0[4 * j + e];
-                            if (r_e < n && t_e < m)
-                                dots[((int64_t)t_e * n + r_e) * nb + b] = __float2int_rn(__uint_as_float(v));
-                        }
-            } else {
-                const float dw00 = wsc[0], dw01 = wsc[8], dw10 = wsc[16], dw11 = wsc[24];
-                const float2 w00 = make_float2(dw00, dw00), w01 = make_float2(dw01, dw01);
-                const float2 w10 = make_float2(dw10, dw10), w11 = make_float2(dw11, dw11);
+                            for (int e = 0; e < 4; ++e) {
+                                const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
+                                const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
+                                const uint32_t v = hl ? d1[4 * j + e] : d0[4 * j + e];
+                                if (r_e < n && t_e < m)
+                                    dots[((int64_t)t_e * n + r_e) * nb + b] = __float2int_rn(__uint_as_float(v));
+                            }
+                } else {
+                    const float dw00 = wsc[0], dw01 = wsc[8], dw10 = wsc[16], dw11 = wsc[24];
+                    const float2 w00 = make_float2(dw00, dw00), w01 = make_float2(dw01, dw01);
+                    const float2 w10 = make_float2(dw10, dw10), w11 = make_float2(dw11, dw11);
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const float2 da = *reinterpret_cast<const float2 *>(asc + 8 * j);
-                    const float2 a0 = make_float2(__uint_as_float(d0[4 * j + 0]), __uint_as_float(d0[4 * j + 1]));
-                    const float2 a1 = make_float2(__uint_as_float(d0[4 * j + 2]), __uint_as_float(d0[4 * j + 3]));
-                    const float2 b0 = make_float2(__uint_as_float(d1[4 * j + 0]), __uint_as_float(d1[4 * j + 1]));
-                    const float2 b1 = make_float2(__uint_as_float(d1[4 * j + 2]), __uint_as_float(d1[4 * j + 3]));
-                    acc[0][j][0] = fma2_rn(mul2_rn(w00, da), a0, acc[0][j][0]);
-                    acc[0][j][1] = fma2_rn(mul2_rn(w01, da), a1, acc[0][j][1]);
-                    acc[1][j][0] = fma2_rn(mul2_rn(w10, da), b0, acc[1][j][0]);
-                    acc[1][j][1] = fma2_rn(mul2_rn(w11, da), b1, acc[1][j][1]);
+                    for (int j = 0; j < NJ; ++j) {
+                        const float2 da = *reinterpret_cast<const float2 *>(asc + 8 * j);
+                        const float2 a0 = make_float2(__uint_as_float(d0[4 * j + 0]), __uint_as_float(d0[4 * j + 1]));
+                        const float2 a1 = make_float2(__uint_as_float(d0[4 * j + 2]), __uint_as_float(d0[4 * j + 3]));
+                        const float2 b0 = make_float2(__uint_as_float(d1[4 * j + 0]), __uint_as_float(d1[4 * j + 1]));
+                        const float2 b1 = make_float2(__uint_as_float(d1[4 * j + 2]), __uint_as_float(d1[4 * j + 3]));
+                        acc[0][j][0] = fma2_rn(mul2_rn(w00, da), a0, acc[0][j][0]);
+                        acc[0][j][1] = fma2_rn(mul2_rn(w01, da), a1, acc[0][j][1]);
+                        acc[1][j][0] = fma2_rn(mul2_rn(w10, da), b0, acc[1][j][0]);
+                        acc[1][j][1] = fma2_rn(mul2_rn(w11, da), b1, acc[1][j][1]);
+                    }
                 }
             }
-            if (blk == 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.sc_empty[ss]);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.sc_empty[ss]);
         }
         if (!DOTS && !*abort_flag) {
 #pragma unroll
