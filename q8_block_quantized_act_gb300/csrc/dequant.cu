@@ -16,9 +16,10 @@
 namespace q8 {
 namespace {
 
-constexpr int CONV_WARPS = 8;
+constexpr int CONV_WARPS = 16;
 constexpr int THREADS = (CONV_WARPS + 1) * 32;   // + one bulk-copy producer warp
 constexpr int MAX_STAGES = 6;
+constexpr size_t TWO_PER_SM_SMEM = 113 * 1024;   // two CTAs per SM when 3 stages fit in this
 constexpr int TARGET_CHUNK = 34816;               // bytes of raw rows per stage (<= 128 units)
 
 struct Plan {
@@ -67,7 +68,7 @@ __device__ __forceinline__ void bytes_to_half2x2(uint32_t q4, __half2 &lo, __hal
     hi = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     dequant_q8_0_f16_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out, int n, int k,
                             Plan p, int *status)
 {
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == CONV_WARPS) {
         if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();   // the weights are read once
             int64_t issued = 0;
             for (int64_t i = 0; i < my_chunks; ++i) {
                 const int s = (int)(i % p.stages);
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
                 const uint32_t bytes = (uint32_t)rows * p.row_bytes;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_g2s(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes, &full[s]);
+                bulk_g2s_hint(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes, &full[s],
+                              policy);
                 ++issued;
             }
             for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
@@ -161,12 +164,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
                                     int64_t n, int64_t k, cudaStream_t stream)
 {
-    const Plan p = make_plan(n, k, dev.max_smem_optin);
+    Plan p = make_plan(n, k, TWO_PER_SM_SMEM < dev.max_smem_optin ? TWO_PER_SM_SMEM : dev.max_smem_optin);
+    int per_sm = 2;
+    if (p.stages < 3) {
+        p = make_plan(n, k, dev.max_smem_optin);
+        per_sm = 1;
+    }
     if (p.stages < 2) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(dequant_q8_0_f16_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
+    cudaFuncSetAttribute(dequant_q8_0_f16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    const int64_t slots = (int64_t)dev.num_sms * per_sm;
+    const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
     dequant_q8_0_f16_kernel<<<(int)grid, THREADS, p.smem, stream>>>(
         w, reinterpret_cast<uint4 *>(w16), (int)n, (int)k, p, dev.status);
     return cudaGetLastError();

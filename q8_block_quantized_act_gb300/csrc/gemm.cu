@@ -95,27 +95,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
         : "memory");
 }
 
-// 16 lanes x 256 bits, repeated 8 times along the columns: 32 registers per thread.
-// Register 4j+e of thread T holds lane base + T/4 + 8*(e>>1), column base + 8j + 2*(T%4) + (e&1).
-__device__ __forceinline__ void tc_ld_16x256b_x8(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // 16 lanes x 256 bits, repeated 4 times along the columns (16 registers), asynchronous:
 // the registers are valid only after tc_wait_ld_bind16.
 __device__ __forceinline__ void tc_ld_16x256b_x4_async(uint32_t taddr, uint32_t (&r)[16])
@@ -137,39 +116,6 @@ __device__ __forceinline__ void tc_wait_ld_bind16(uint32_t (&r)[16])
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                    "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-
-// Asynchronous x8 form: issue the load; the registers are valid only after tc_wait_ld_bind.
-__device__ __forceinline__ void tc_ld_16x256b_x8_async(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-
-// Ties 32 registers of an issued tcgen05.ld to a point after tcgen05.wait::ld (the first
-// call waits; later calls only order the registers after it).
-template <bool WAIT>
-__device__ __forceinline__ void tc_wait_ld_bind(uint32_t (&r)[32])
-{
-    if (WAIT) asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
-                   "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
-                   "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                  :
                  : "memory");
 }
@@ -560,10 +506,14 @@ cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint
     if (dots) {
         e = cudaFuncSetAttribute(gemm_q8_0_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        cudaFuncSetAttribute(gemm_q8_0_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
         gemm_q8_0_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, y, dots, (int)m, (int)n, (int)k, dev.status);
     } else {
         e = cudaFuncSetAttribute(gemm_q8_0_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        cudaFuncSetAttribute(gemm_q8_0_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
         gemm_q8_0_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, y, dots, (int)m, (int)n, (int)k, dev.status);
     }
     return cudaGetLastError();

@@ -113,17 +113,6 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int G = p.G;
     const int nb = k / QK;
 
-    // Activation cache: quants [token][group][68 words], scales [token][group][12 words].
-    for (int idx = tid; idx < M * G * 16; idx += THREADS) {
-        const int t = idx / (G * 16), rem = idx - t * G * 16, g = rem >> 4, c = rem & 15;
-        const uint4 v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + g * 256 + c * 16);
-        *reinterpret_cast<uint4 *>(xs + (t * G + g) * XG_WORDS + c * 4) = v;
-    }
-    for (int idx = tid; idx < M * G * 2; idx += THREADS) {
-        const int t = idx / (G * 2), rem = idx - t * G * 2, g = rem >> 1, c = rem & 1;
-        const float4 v = *reinterpret_cast<const float4 *>(xd + (int64_t)t * nb + g * 8 + c * 4);
-        *reinterpret_cast<float4 *>(xds + (t * G + g) * XDG_WORDS + c * 4) = v;
-    }
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
@@ -132,6 +121,22 @@ __global__ void __launch_bounds__(THREADS, 2)
         fence_mbar_init();
     }
     __syncthreads();
+    // The producer starts streaming weights right away; the consumers meanwhile load the
+    // activation cache -- quants [token][group][68 words], scales [token][group][12 words] --
+    // and meet at a named barrier before their first chunk.
+    if (tid < CONSUMERS) {
+        for (int idx = tid; idx < M * G * 16; idx += CONSUMERS) {
+            const int t = idx / (G * 16), rem = idx - t * G * 16, g = rem >> 4, c = rem & 15;
+            const uint4 v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + g * 256 + c * 16);
+            *reinterpret_cast<uint4 *>(xs + (t * G + g) * XG_WORDS + c * 4) = v;
+        }
+        for (int idx = tid; idx < M * G * 2; idx += CONSUMERS) {
+            const int t = idx / (G * 2), rem = idx - t * G * 2, g = rem >> 1, c = rem & 1;
+            const float4 v = *reinterpret_cast<const float4 *>(xd + (int64_t)t * nb + g * 8 + c * 4);
+            *reinterpret_cast<float4 *>(xds + (t * G + g) * XDG_WORDS + c * 4) = v;
+        }
+        named_bar_sync(2, CONSUMERS);
+    }
 
     const int64_t my_chunks =
         blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -139,6 +144,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (tid >= CONSUMERS) {
         // ---------------- producer warp: one lane issues the bulk copies ----------------
         if (tid == CONSUMERS) {
+            const uint64_t policy = l2_policy_evict_first();   // the weights are read once
             int64_t issued = 0;
             for (int64_t i = 0; i < my_chunks; ++i) {
                 const int s = (int)(i % p.stages);
@@ -149,8 +155,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                 const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
                 const uint32_t bytes = (uint32_t)rows * p.row_bytes;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_g2s(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes,
-                         &full[s]);
+                bulk_g2s_hint(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes, &full[s],
+                              policy);
                 ++issued;
             }
             // Do not leave while copies into this CTA's shared memory may be in flight.
@@ -280,6 +286,7 @@ cudaError_t launch_m(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)p.smem);
     if (e != cudaSuccess) return e;
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
     kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)n, (int)k, p,

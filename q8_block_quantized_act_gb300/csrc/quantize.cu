@@ -30,13 +30,21 @@ __device__ __forceinline__ Block4 quantize4(float4 v)
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
     Block4 r;
     r.d = __fdiv_rn(a, 127.0f);
+    // round(fl(v / d)) without a division per value: q' = v * rcp_rn(d) differs from
+    // fl(v / d) by at most ~2.3e-5 (|v / d| <= 127, each of rcp, the product and the quotient
+    // is within 2^-24 relative), so unless q' lies within 1e-3 of a half-integer -- or is not
+    // finite -- it rounds to the same integer.  Those rare cases take the IEEE division.
+    const float rc = __frcp_rn(r.d);
     const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         if (r.d == 0.0f) {
             r.q[i] = 0;
         } else {
-            float t = roundf(__fdiv_rn(vals[i], r.d));
+            const float qa = __fmul_rn(vals[i], rc);
+            const float aq = fabsf(qa);
+            const float fr = aq - floorf(aq);
+            float t = (fabsf(fr - 0.5f) > 1e-3f) ? roundf(qa) : roundf(__fdiv_rn(vals[i], r.d));
             if (t > 127.0f) t = 127.0f;
             if (t < -127.0f) t = -127.0f;
             r.q[i] = __float2int_rz(t);  // NaN converts to 0
@@ -56,12 +64,22 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__rest
                                                             float *__restrict__ xd,
                                                             int64_t nchunks)
 {
+    // Two independent chunks per step (more loads in flight).  nchunks is a multiple of 64
+    // and the stride of 32, so both halves are warp-uniform, as the shuffles need.
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
-        Block4 b = quantize4(load_stream(x + i));
-        xq[i] = (uint32_t)(b.q[0] & 0xff) | ((uint32_t)(b.q[1] & 0xff) << 8) |
-                ((uint32_t)(b.q[2] & 0xff) << 16) | ((uint32_t)(b.q[3] & 0xff) << 24);
-        if ((i & 7) == 0) xd[i >> 3] = b.d;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += 2 * stride) {
+        const bool two = i + stride < nchunks;
+        const float4 v0 = load_stream(x + i);
+        const float4 v1 = two ? load_stream(x + i + stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !two) break;
+            const int64_t c = i + h * stride;
+            Block4 b = quantize4(h ? v1 : v0);
+            xq[c] = (uint32_t)(b.q[0] & 0xff) | ((uint32_t)(b.q[1] & 0xff) << 8) |
+                    ((uint32_t)(b.q[2] & 0xff) << 16) | ((uint32_t)(b.q[3] & 0xff) << 24);
+            if ((c & 7) == 0) xd[c >> 3] = b.d;
+        }
     }
 }
 
@@ -74,16 +92,24 @@ __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__
                                                                 int64_t ldm)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
-        Block4 b = quantize4(load_stream(x + i));
-        uint32_t h[4];
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += 2 * stride) {
+        const bool two = i + stride < nchunks;
+        const float4 v0 = load_stream(x + i);
+        const float4 v1 = two ? load_stream(x + i + stride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__int2half_rn(b.q[j]));
-        xqh[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-        if ((i & 7) == 0) {
-            const int64_t t = i / chunks_per_row;
-            const int64_t blk = (i - t * chunks_per_row) >> 3;
-            xdt[blk * ldm + t] = b.d;
+        for (int hh = 0; hh < 2; ++hh) {
+            if (hh == 1 && !two) break;
+            const int64_t c = i + hh * stride;
+            Block4 b = quantize4(hh ? v1 : v0);
+            uint32_t h[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__int2half_rn(b.q[j]));
+            xqh[c] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+            if ((c & 7) == 0) {
+                const int64_t t = c / chunks_per_row;
+                const int64_t blk = (c - t * chunks_per_row) >> 3;
+                xdt[blk * ldm + t] = b.d;
+            }
         }
     }
 }
@@ -107,6 +133,20 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__rest
     }
 }
 
+// Every kernel of the library asks for the largest shared-memory carveout, so that moving
+// between these smem-free passes and the shared-memory-heavy GEMV/GEMM/dequant never forces
+// the SM to re-partition its L1/shared memory between launches.
+template <typename K>
+void set_max_carveout(K kern)
+{
+    static bool done = false;
+    if (!done) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        done = true;
+    }
+}
+
 int grid_for(const DeviceInfo &dev, int64_t nchunks, int threads)
 {
     int64_t want = (nchunks + threads - 1) / threads;
@@ -120,6 +160,7 @@ cudaError_t launch_quantize_q8_1(const DeviceInfo &dev, const float *x, int8_t *
                                  int64_t m, int64_t k, cudaStream_t stream)
 {
     const int64_t nchunks = m * k / 4;
+    set_max_carveout(quantize_q8_1_kernel);
     quantize_q8_1_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
         reinterpret_cast<const float4 *>(x), reinterpret_cast<uint32_t *>(xq), xd, nchunks);
     return cudaGetLastError();
@@ -130,6 +171,7 @@ cudaError_t launch_quantize_q8_1_mmq(const DeviceInfo &dev, const float *x, uint
                                      cudaStream_t stream)
 {
     const int64_t nchunks = m * k / 4;
+    set_max_carveout(quantize_q8_1_mmq_kernel);
     quantize_q8_1_mmq_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
         reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xqh), xdt, nchunks, k / 4,
         ldm);
@@ -140,6 +182,7 @@ cudaError_t launch_quantize_q8_0(const DeviceInfo &dev, const float *w, uint8_t 
                                  int64_t k, cudaStream_t stream)
 {
     const int64_t nchunks = n * k / 4;
+    set_max_carveout(quantize_q8_0_kernel);
     quantize_q8_0_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
         reinterpret_cast<const float4 *>(w), wq, nchunks);
     return cudaGetLastError();
