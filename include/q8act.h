@@ -58,8 +58,10 @@ extern "C" {
 
 /* Largest supported k (values per row). */
 #define Q8ACT_MAX_K 65536
-/* Largest token count of the GEMV (decode m = 1 and speculative verify up to 8). */
-#define Q8ACT_GEMV_MAX_M 8
+/* Largest token count of the GEMV: decode m = 1 and the m = K + 1 speculative-verify tier,
+   i.e. the whole m < 16 range that the pages keep on the dp4a/MMVQ chain (fp8_ffi.rs and
+   f16_ffi.rs module docs; m >= 16 is prefill). */
+#define Q8ACT_GEMV_MAX_M 15
 
 /* Library version, major*10000 + minor*100 + patch. */
 int q8act_version(void);
@@ -104,7 +106,10 @@ int q8act_quantize_q8_0(const float *w, void *wq, int64_t n, int64_t k, void *st
  * Q8_0 x q8_1 GEMV, the decode ("mmvq") regime: Engine::qmatvec_mmvq_into in
  * decode_kernel_census.rs fn q8 (weights w, pre-quantized activation aq/ad, m tokens).
  *   w [n rows of Q8_0 blocks], xq [m][k] int8, xd [m][k/32] f32, y [m][n] f32 (overwritten)
- *   1 <= m <= Q8ACT_GEMV_MAX_M.  The result for token t does not depend on m (the same
+ *   1 <= m <= Q8ACT_GEMV_MAX_M.  The m-token activation (1.25 * m * k bytes) is cached in
+ *   shared memory beside at least two weight stages, which bounds k: 65536 at m = 1,
+ *   18688 at m = 8, 10752 at m = 15; beyond that the call returns Q8ACT_ERR_DIMS.  The result for token t
+ *   does not depend on m (the same
  *   operations in the same order for every m: the pages' decode == verify law,
  *   fp8_ffi.rs module doc and f16_ffi.rs module doc).
  */

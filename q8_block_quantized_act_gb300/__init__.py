@@ -60,7 +60,7 @@ def quantize_q8_1_mmq(x):
 
 
 def gemv_q8_0(w, xq, xd, n: int, out=None):
-    """Decode GEMV: Q8_0 bytes w (n rows), q8_1 activation (xq, xd) of m <= 8 tokens."""
+    """Decode GEMV: Q8_0 bytes w (n rows), q8_1 activation (xq, xd) of m <= Q8ACT_GEMV_MAX_M (15) tokens."""
     import torch
     m, k = xq.shape
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)

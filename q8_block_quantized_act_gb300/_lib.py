@@ -27,7 +27,7 @@ Q8ACT_ERR_DEVICE = -5
 Q8ACT_ERR_TIMEOUT = -6
 Q8ACT_ERR_CUDA_BASE = 1000
 Q8ACT_MAX_K = 65536
-Q8ACT_GEMV_MAX_M = 8
+Q8ACT_GEMV_MAX_M = 15
 
 EXPORTED = (
     "q8act_version", "q8act_strerror", "q8act_quantize_q8_1", "q8act_quantize_q8_1_mmq",

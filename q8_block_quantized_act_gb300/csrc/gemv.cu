@@ -1,4 +1,4 @@
-// gemv.cu -- Q8_0 x q8_1 GEMV for decode and speculative verify (m = 1..8): the "mmvq"
+// gemv.cu -- Q8_0 x q8_1 GEMV for decode and speculative verify (m = 1..15): the "mmvq"
 // regime of memra-engine 0.113.0 decode_kernel_census.rs (fn q8 -> qmatvec_mmvq_into).
 //
 // The weight stream (34 bytes per 32 weights) is read exactly once, so the kernel is bound
@@ -42,11 +42,12 @@ struct Plan {
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap)
+Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap)
 {
     Plan p{};
     p.G = (int)(k / 256);
     p.R = p.G <= CONSUMERS ? CONSUMERS / p.G : 1;
+    if (p.R > r_cap) p.R = r_cap;
     if ((int64_t)p.R > n) p.R = (int)n;
     p.U = p.R * p.G;
     p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
@@ -71,15 +72,20 @@ Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap)
 }
 
 // Two CTAs per SM when two rings of at least 3 stages fit, else one CTA with up to 6 stages.
+// When a large activation leaves room for fewer than 2 full-size stages, the chunk shrinks
+// (fewer rows per chunk) until two fit.
 Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
 {
     const size_t half = 113 * 1024;
-    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin);
+    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin, CONSUMERS);
     if (p.stages >= 3) {
         p.ctas_per_sm = 2;
         return p;
     }
-    return make_plan(m, n, k, smem_optin);
+    p = make_plan(m, n, k, smem_optin, CONSUMERS);
+    for (int r_cap = p.R / 2; p.stages < 2 && r_cap >= 1; r_cap /= 2)
+        p = make_plan(m, n, k, smem_optin, r_cap);
+    return p;
 }
 
 __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
@@ -308,6 +314,13 @@ cudaError_t dispatch(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, 
     case 6: return launch_m<6, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
     case 7: return launch_m<7, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
     case 8: return launch_m<8, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 9: return launch_m<9, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 10: return launch_m<10, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 11: return launch_m<11, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 12: return launch_m<12, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 13: return launch_m<13, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 14: return launch_m<14, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 15: return launch_m<15, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
     default: return cudaErrorInvalidValue;
     }
 }

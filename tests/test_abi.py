@@ -60,7 +60,7 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_quantize_q8_1_mmq(A, None, A, 1, 256, S0), q8.Q8ACT_ERR_NULL),
     (lambda: q8.q8act_quantize_q8_0(A, A, 4, 288, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemv_q8_0(A, A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
-    (lambda: q8.q8act_gemv_q8_0(A, A, A, A, 9, 8, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0(A, A, A, A, q8.Q8ACT_GEMV_MAX_M + 1, 8, 256, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemv_q8_0(A, A, A, A, 0, 8, 256, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemv_q8_0(A, A, A, A, 1, 0, 256, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemv_q8_0(A, A, A, A, 1, 8, 1280 + 32, S0), q8.Q8ACT_ERR_DIMS),

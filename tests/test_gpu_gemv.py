@@ -1,4 +1,4 @@
-"""GPU GEMV (decode / verify, m = 1..8) vs the oracle: exact block dots, outputs within
+"""GPU GEMV (decode / verify, m = 1..15) vs the oracle: exact block dots, outputs within
 1e-5 * S, bitwise batch invariance (decode == verify) and determinism."""
 import numpy as np
 import pytest
@@ -24,6 +24,11 @@ def run_gemv(wb, xq, xd, n):
     (8, 777, 4096, "normal"),
     (2, 1, 256, "normal"),            # a single row
     (5, 33, 8192, "token_scales"),
+    (9, 640, 4096, "outliers"),       # verify tier, K = 8 drafted tokens
+    (12, 300, 2048, "token_scales"),
+    (15, 1000, 4096, "normal"),       # largest m below the prefill threshold
+    (15, 40, 10752, "normal"),        # largest k at m = 15 (shrunken chunks)
+    (8, 24, 18688, "outliers"),       # largest k at m = 8
 ])
 def test_gemv_matches_oracle(m, n, k, kind):
     ensure_built()
@@ -35,7 +40,7 @@ def test_gemv_matches_oracle(m, n, k, kind):
     assert_within_tolerance(y, y64, S)
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 512, 256), (4, 300, 1280), (8, 130, 4096)])
+@pytest.mark.parametrize("m,n,k", [(1, 512, 256), (4, 300, 1280), (8, 130, 4096), (15, 70, 4096)])
 def test_gemv_block_dots_exact(m, n, k):
     ensure_built()
     _, _, wb, xq, _ = problem(m, n, k)
@@ -47,18 +52,38 @@ def test_gemv_block_dots_exact(m, n, k):
 
 @pytest.mark.parametrize("n,k", [(4096, 4096), (4096, 1280), (20480, 4096), (64448, 4096)])
 def test_gemv_serving_shapes_batch_invariant(n, k):
-    """decode == verify: token t's output is bitwise the same for m = 1, 2, 4, 8."""
+    """decode == verify: token t's output is bitwise the same for every m of the GEMV."""
     ensure_built()
-    _, _, wb, xq, xd = problem(8, n, k)
+    mmax = q8.Q8ACT_GEMV_MAX_M
+    _, _, wb, xq, xd = problem(mmax, n, k)
     w_d = cuda(wb)
     ys = {}
-    for m in (8, 4, 2, 1):
+    for m in (mmax, 12, 9, 8, 4, 2, 1):
         ys[m] = host(q8.gemv_q8_0(w_d, cuda(xq[:m]), cuda(xd[:m]), n))
     device_ok()
-    for m in (4, 2, 1):
-        assert np.array_equal(ys[m].view(np.uint32), ys[8][:m].view(np.uint32)), f"m={m}"
+    for m in (12, 9, 8, 4, 2, 1):
+        assert np.array_equal(ys[m].view(np.uint32), ys[mmax][:m].view(np.uint32)), f"m={m}"
     again = host(q8.gemv_q8_0(w_d, cuda(xq), cuda(xd), n))
-    assert np.array_equal(again.view(np.uint32), ys[8].view(np.uint32)), "not deterministic"
+    assert np.array_equal(again.view(np.uint32), ys[mmax].view(np.uint32)), "not deterministic"
     rows = sample_rows(n, 1024)
     _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
-    assert_within_tolerance(ys[8][:, rows], y64, S)
+    assert_within_tolerance(ys[mmax][:, rows], y64, S)
+
+
+@pytest.mark.parametrize("m,kmax", [(1, 65536), (8, 18688), (15, 10752)])
+def test_gemv_k_limit(m, kmax):
+    """The documented largest k per m is accepted and the next multiple of 256 is refused
+    before any launch (the activation cache no longer fits beside two weight stages)."""
+    ensure_built()
+    _, _, wb, xq, xd = problem(m, 8, kmax)
+    y = run_gemv(wb, xq, xd, 8)
+    device_ok()
+    _, y64, S = oracle.matmul(wb, xq, xd, kmax)
+    assert_within_tolerance(y, y64, S)
+    k = kmax + 256
+    w = torch.zeros(8 * k // 32 * 34, dtype=torch.uint8, device="cuda")
+    aq = torch.zeros((m, k), dtype=torch.int8, device="cuda")
+    ad = torch.zeros((m, k // 32), dtype=torch.float32, device="cuda")
+    out = torch.zeros((m, 8), dtype=torch.float32, device="cuda")
+    rc = q8.q8act_gemv_q8_0(w, aq, ad, out, m, 8, k)
+    assert rc == q8.Q8ACT_ERR_DIMS
