@@ -250,11 +250,7 @@ def run_ours(args, rank, world, local_rank):
     mean_ms = {name: float(np.mean(v)) for name, v in per.items()}
     step_ms = float(sum(mean_ms.values()))
     if world > 1:
-        t = torch.tensor([step_ms] + [mean_ms[nm] for nm, _ in parts], device=dev,
-                         dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t[0])
-        mean_ms = {nm: float(t[i + 1]) for i, (nm, _) in enumerate(parts)}
+        step_ms, mean_ms = max_over_ranks(step_ms, mean_ms, [nm for nm, _ in parts], dev)
 
     # ---- end to end through the public API: host f32 in (pinned), host f32 out ----
     e2e = run_e2e(args, q8, torch, dev, stream)
@@ -281,7 +277,7 @@ def run_ours(args, rank, world, local_rank):
                 "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} ({'hbm_gbs' if d['bound'] == 'hbm' else 'bf16_tflops burst; f16 pipe, nominal ratio 1'})"}
 
-    value = comps["gemv_q8_0"]["achieved"] * world
+    value = whole_job_value(comps["gemv_q8_0"]["achieved"], world)
     cpu = cpu_baseline(args) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     clocks = sampler.summary(t0, t1) if sampler else None
     line = {
@@ -302,6 +298,20 @@ def run_ours(args, rank, world, local_rank):
         "impl": "ours",
     }
     return line
+
+
+def max_over_ranks(step_ms, mean_ms, names, device):
+    """The slowest rank's step time and per-kernel times (every rank gets the same result)."""
+    import torch
+    t = torch.tensor([step_ms] + [mean_ms[nm] for nm in names], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t[0]), {nm: float(t[i + 1]) for i, nm in enumerate(names)}
+
+
+def whole_job_value(per_rank_gbs_at_max_time, world):
+    """Weak scaling: every rank streams the same bytes, so the job moves world x those bytes in
+    the slowest rank's time."""
+    return per_rank_gbs_at_max_time * world
 
 
 def roof(bound, achieved, peak, unit, ms, work):
