@@ -20,7 +20,7 @@ constexpr int CONV_WARPS = 16;
 constexpr int THREADS = (CONV_WARPS + 1) * 32;   // + one bulk-copy producer warp
 constexpr int MAX_STAGES = 6;
 constexpr size_t TWO_PER_SM_SMEM = 113 * 1024;   // two CTAs per SM when 3 stages fit in this
-constexpr int TARGET_CHUNK = 34816;               // bytes of raw rows per stage (<= 128 units)
+constexpr int TARGET_CHUNK = 17408;               // bytes of raw rows per stage (<= 64 units)
 
 struct Plan {
     int G;               // units (272-byte groups) per row

@@ -84,33 +84,25 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__rest
 }
 
 // x [m][k] f32 -> xqh [m][k] binary16 (exact small integers), xdt [k/32][ldm] f32.
+// Grid: (ceil(k/4 / 256), min(m, 65535)); thread (token t = blockIdx.y + i * gridDim.y,
+// chunk c of its row).  k/4 is a multiple of 64, so every warp is either fully inside the
+// row or fully past its end.
 __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__restrict__ x,
                                                                 uint2 *__restrict__ xqh,
                                                                 float *__restrict__ xdt,
-                                                                int64_t nchunks,
-                                                                int64_t chunks_per_row,
+                                                                int64_t m, int chunks_per_row,
                                                                 int64_t ldm)
 {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += 2 * stride) {
-        const bool two = i + stride < nchunks;
-        const float4 v0 = load_stream(x + i);
-        const float4 v1 = two ? load_stream(x + i + stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= chunks_per_row) return;
+    for (int64_t t = blockIdx.y; t < m; t += gridDim.y) {
+        const int64_t g = t * chunks_per_row + c;
+        Block4 b = quantize4(load_stream(x + g));
+        uint32_t h[4];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            if (hh == 1 && !two) break;
-            const int64_t c = i + hh * stride;
-            Block4 b = quantize4(hh ? v1 : v0);
-            uint32_t h[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__int2half_rn(b.q[j]));
-            xqh[c] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-            if ((c & 7) == 0) {
-                const int64_t t = c / chunks_per_row;
-                const int64_t blk = (c - t * chunks_per_row) >> 3;
-                xdt[blk * ldm + t] = b.d;
-            }
-        }
+        for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__int2half_rn(b.q[j]));
+        xqh[g] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        if ((c & 7) == 0) xdt[(int64_t)(c >> 3) * ldm + t] = b.d;
     }
 }
 
@@ -170,11 +162,11 @@ cudaError_t launch_quantize_q8_1_mmq(const DeviceInfo &dev, const float *x, uint
                                      float *xdt, int64_t m, int64_t k, int64_t ldm,
                                      cudaStream_t stream)
 {
-    const int64_t nchunks = m * k / 4;
+    const int cpr = (int)(k / 4);
     set_max_carveout(quantize_q8_1_mmq_kernel);
-    quantize_q8_1_mmq_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
-        reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xqh), xdt, nchunks, k / 4,
-        ldm);
+    const dim3 grid((unsigned)((cpr + 255) / 256), (unsigned)(m < 65535 ? m : 65535));
+    quantize_q8_1_mmq_kernel<<<grid, 256, 0, stream>>>(
+        reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xqh), xdt, m, cpr, ldm);
     return cudaGetLastError();
 }
 
