@@ -62,9 +62,10 @@ def _bind(lib):
     lib.oracle_block_dots.argtypes = [P, P, P, I64, I64, I64, P, I64]
     lib.oracle_matmul.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P, P]
     lib.oracle_dequant_f16.argtypes = [P, P, I64, I64]
+    lib.oracle_repack_q8_0.argtypes = [P, P, P, I64, I64, I64]
     for name in ("oracle_f32_to_f16_array", "oracle_f16_to_f32_array",
                  "oracle_quantize_q8_1", "oracle_quantize_q8_0", "oracle_block_dots",
-                 "oracle_matmul", "oracle_dequant_f16"):
+                 "oracle_matmul", "oracle_dequant_f16", "oracle_repack_q8_0"):
         getattr(lib, name).restype = None
     return lib
 
@@ -194,10 +195,23 @@ def dequant_f16(w: np.ndarray, k: int, _o: Oracle | None = None) -> np.ndarray:
     return out
 
 
+def repack_q8_0(w: np.ndarray, k: int, ldn: int | None = None, _o: Oracle | None = None):
+    """O6: Q8_0 bytes -> (wq16 binary16 bits uint16 [n, k], wdt f32 [k/32, ldn]); the
+    columns n..ldn-1 of wdt are zero."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    n = w.size // (k // QK * Q8_0_BYTES)
+    ldn = n if ldn is None else ldn
+    wq16 = np.empty((n, k), dtype=np.uint16)
+    wdt = np.zeros((k // QK, ldn), dtype=np.float32)
+    (_o or _DEFAULT).lib().oracle_repack_q8_0(_ptr(w), _ptr(wq16), _ptr(wdt), n, k, ldn)
+    return wq16, wdt
+
+
 _DEFAULT = Oracle()
 
 _PUBLIC = ("f32_to_f16", "f16_to_f32", "quantize_q8_0", "quantize_q8_1", "block_dots",
-           "matmul", "dequant_f16")
+           "matmul", "dequant_f16", "repack_q8_0")
 
 
 def bound(o: Oracle):

@@ -261,3 +261,21 @@ void oracle_dequant_f16(const uint8_t *w, uint16_t *out, int64_t n, int64_t k)
                 out[r * k + b * QK + i] = oracle_f32_to_f16(dw * (float)wq[i]);
         }
 }
+
+/* O6: load-time repack of Q8_0 for the tensor-core GEMM (a layout change, no arithmetic
+   beyond exact conversions): wq16[r][32b+i] = binary16(q) -- exact, |q| <= 127 -- and the
+   scale plane wdt[b][r] = f32(d_w[r][b]), block-major with leading dimension ldn >= n
+   (columns n..ldn-1 are left untouched). */
+void oracle_repack_q8_0(const uint8_t *w, uint16_t *wq16, float *wdt, int64_t n, int64_t k,
+                        int64_t ldn)
+{
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = block_ptr(w, r, b, nb);
+            const int8_t *wq = (const int8_t *)(blk + 2);
+            for (int i = 0; i < QK; i++)
+                wq16[r * k + b * QK + i] = oracle_f32_to_f16((float)wq[i]);
+            wdt[b * ldn + r] = block_scale(blk);
+        }
+}

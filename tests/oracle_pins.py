@@ -258,6 +258,25 @@ def pin_dequant_vs_numpy(o, seed=8):
     assert np.array_equal(got, ref)
 
 
+def pin_repack(o, seed=9):
+    """The repacked planes hold exactly the Q8_0 quants and scales: numpy's own binary16
+    decode of wq16 gives back the int8 quants, wdt is numpy's binary16 -> f32 of the stored
+    scale bits (transposed), and re-rounding wdt * wq16 to fp16 reproduces the dequant."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n, k, ldn = 11, 768, 16
+    w = _rand_blocks(rng, n, k, lo=-16, hi=6)
+    wb = o.quantize_q8_0(w)
+    dw, wq = parse_q8_0(wb, n, k)
+    wq16, wdt = o.repack_q8_0(wb, k, ldn)
+    assert np.array_equal(wq16.view(np.float16).astype(np.float64),
+                          wq.reshape(n, k).astype(np.float64))
+    assert np.array_equal(wdt[:, :n], dw.astype(np.float32).T)
+    assert not wdt[:, n:].any()
+    prod = wdt[:, :n].T.repeat(32, axis=1) * wq16.view(np.float16).astype(np.float32)
+    with np.errstate(over="ignore"):
+        assert np.array_equal(prod.astype(np.float16).view(np.uint16), o.dequant_f16(wb, k))
+
+
 ALL_PINS = [
     pin_f16_decode_exhaustive,
     pin_f16_encode_vs_numpy,
@@ -269,4 +288,5 @@ ALL_PINS = [
     pin_block_dots_bruteforce,
     pin_fold_bruteforce,
     pin_dequant_vs_numpy,
+    pin_repack,
 ]

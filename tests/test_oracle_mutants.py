@@ -1,6 +1,6 @@
 """Planted mistakes in a copy of the oracle must each fail at least one pin.
 
-Every mutant is a one-line textual change to a temporary copy of oracle/q8_oracle.c,
+Every mutant is a small textual change to a temporary copy of oracle/q8_oracle.c,
 compiled with the same flags; the committed oracle is never modified.
 """
 import os
@@ -29,6 +29,9 @@ MUTANTS = {
     "f16_decode_bias": ("v = ldexpf((float)(1024 + f), e - 25);", "v = ldexpf((float)(1024 + f), e - 24);"),
     "dequant_unrounded_scale": ("float dw = block_scale(blk);\n            const int8_t *wq",
                                 "float dw = block_scale(blk) * 1.0001f;\n            const int8_t *wq"),
+    "repack_scales_row_major": ("wdt[b * ldn + r] = block_scale(blk);", "wdt[r * nb + b] = block_scale(blk);"),
+    "repack_offset_binary": ("wq16[r * k + b * QK + i] = oracle_f32_to_f16((float)wq[i]);",
+                             "wq16[r * k + b * QK + i] = oracle_f32_to_f16((float)(wq[i] + 128));"),
 }
 
 
