@@ -171,6 +171,34 @@ int q8act_gemm_q8_0_noalloc(const void *w, const float *x, float *y, int64_t m, 
 int q8act_dequant_q8_0_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
 
 /*
+ * Load-time repack of Q8_0 weights for the tensor-core GEMM (the pages name such a repack,
+ * build_q8_rp4 in the hybrid loader, without defining it; this one keeps the method exact):
+ *   w [n rows of Q8_0 blocks] -> wq16 [n][k] binary16, wq16[r][32b+i] = q (exact, |q| <= 127),
+ *                                wdt [k/32][ldn] f32, wdt[b][r] = f32(d_w[r][b]),
+ *   ldn = q8act_repack_ldn(n); columns n..ldn-1 of wdt are not written.
+ *   Output: 2 n k + 4 ldn k/32 bytes (2.125 bytes per weight, twice the Q8_0 bytes, like the
+ *   pages' resident fp16 mirror, which however rounds d_w * q).  Caller-owned buffers,
+ *   16-byte aligned.
+ */
+int q8act_repack_q8_0(const void *w, uint16_t *wq16, float *wdt, int64_t n, int64_t k,
+                      void *stream);
+
+/* Leading dimension (in floats) of the repacked scale plane: n rounded up to a multiple of 4
+   (16-byte rows for the tensor-memory copies).  Returns 0 when n < 1. */
+int64_t q8act_repack_ldn(int64_t n);
+
+/*
+ * The fused GEMM of q8act_gemm_q8_0 on repacked weights (q8act_repack_q8_0): the same
+ * quantization, exact int32 block dots and f32 fold, with the weight tiles loaded by the
+ * tensor-memory copy engine instead of being converted from 34-byte blocks in every call.
+ *   wq16, wdt: the repack of an n-row weight; x, y, m, n, k, ws, ws_bytes, stream: as for
+ *   q8act_gemm_q8_0.
+ */
+int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float *x, float *y,
+                             int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes,
+                             void *stream);
+
+/*
  * Test hooks: export the exact per-block integer dots D[t][r][b] (int32, [m][n][k/32]) as
  * computed by the block-dot stage of the GEMV (its int8 dot-product path; 1 <= m <= 8) or of
  * the GEMM (its tensor-core path; m >= 1, activation in the MMQ layout).  The fold is
@@ -180,6 +208,11 @@ int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int
                                 int64_t n, int64_t k, void *stream);
 int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, int64_t m,
                                 int64_t n, int64_t k, void *stream);
+
+/* The repacked GEMM's block dots (same contract as q8act_debug_gemm_block_dots). */
+int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt,
+                                         const uint16_t *xqh, int32_t *D, int64_t m, int64_t n,
+                                         int64_t k, void *stream);
 
 /*
  * Synchronizes `stream`, then reads and clears the device-side status word that kernels set

@@ -19,7 +19,8 @@ from ._lib import (  # noqa: F401  (re-exported ABI)
     Q8ACT_NOALLOC_WS_BYTES, Q8ACT_OK, Q8ActError, check, lib, q8act_debug_gemm_block_dots, q8act_debug_gemv_block_dots,
     q8act_dequant_q8_0_f16, q8act_device_status, q8act_gemm_q8_0, q8act_gemm_q8_0_preq,
     q8act_gemm_q8_0_noalloc, q8act_gemm_workspace_bytes, q8act_gemv_q8_0, q8act_mmq_ldm, q8act_quantize_q8_0,
-    q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror)
+    q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror,
+    q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots)
 
 QK = 32
 Q8_0_BYTES = 34
@@ -93,6 +94,28 @@ def gemm_q8_0_preq(w, xqh, xdt, n: int, out=None):
     m, k = xqh.shape
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xqh.device)
     check(q8act_gemm_q8_0_preq(w, xqh, xdt, y, m, n, k), "q8act_gemm_q8_0_preq")
+    return y
+
+
+def repack_q8_0(w, n: int, k: int):
+    """Load-time repack of Q8_0 bytes for the tensor-core GEMM: (wq16 float16 [n, k] holding
+    the exact quants, wdt float32 [k/32, q8act_repack_ldn(n)] holding the block scales)."""
+    import torch
+    wq16 = torch.empty((n, k), dtype=torch.float16, device=w.device)
+    wdt = torch.zeros((k // QK, q8act_repack_ldn(n)), dtype=torch.float32, device=w.device)
+    check(q8act_repack_q8_0(w, wq16, wdt, n, k), "q8act_repack_q8_0")
+    return wq16, wdt
+
+
+def gemm_q8_0_repacked(wq16, wdt, x, ws=None, out=None):
+    """Prefill GEMM (q8_1 quantization fused) on repacked weights (repack_q8_0)."""
+    import torch
+    m, k = x.shape
+    n = wq16.shape[0]
+    if ws is None:
+        ws = gemm_workspace(m, k, x.device)
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
+    check(q8act_gemm_q8_0_repacked(wq16, wdt, x, y, m, n, k, ws, ws.numel()), "q8act_gemm_q8_0_repacked")
     return y
 
 

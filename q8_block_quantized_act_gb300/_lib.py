@@ -34,7 +34,8 @@ EXPORTED = (
     "q8act_mmq_ldm", "q8act_quantize_q8_0", "q8act_gemv_q8_0", "q8act_gemm_workspace_bytes",
     "q8act_gemm_q8_0", "q8act_gemm_q8_0_preq", "q8act_dequant_q8_0_f16",
     "q8act_debug_gemv_block_dots", "q8act_debug_gemm_block_dots", "q8act_device_status",
-    "q8act_gemm_q8_0_noalloc",
+    "q8act_gemm_q8_0_noalloc", "q8act_repack_q8_0", "q8act_repack_ldn",
+    "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
                 "q8act_debug_gemm_block_dots": ([P, P, P, I64, I64, I64, P], I32),
                 "q8act_device_status": ([P], I32),
                 "q8act_gemm_q8_0_noalloc": ([P, P, P, I64, I64, I64, P], I32),
+                "q8act_repack_q8_0": ([P, P, P, I64, I64, P], I32),
+                "q8act_repack_ldn": ([I64], I64),
+                "q8act_gemm_q8_0_repacked": ([P, P, P, P, I64, I64, I64, P, SZ, P], I32),
+                "q8act_debug_gemm_repacked_block_dots": ([P, P, P, P, I64, I64, I64, P], I32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -173,3 +178,21 @@ def q8act_gemm_q8_0_noalloc(w, x, y, m, n, k, stream=None) -> int:
     """The fused GEMM using the library's fixed device scratch instead of a caller workspace
     (for callers that cannot allocate device memory)."""
     return lib().q8act_gemm_q8_0_noalloc(_p(w), _p(x), _p(y), m, n, k, _s(stream))
+
+
+def q8act_repack_q8_0(w, wq16, wdt, n, k, stream=None) -> int:
+    return lib().q8act_repack_q8_0(_p(w), _p(wq16), _p(wdt), n, k, _s(stream))
+
+
+def q8act_repack_ldn(n) -> int:
+    return lib().q8act_repack_ldn(n)
+
+
+def q8act_gemm_q8_0_repacked(wq16, wdt, x, y, m, n, k, ws, ws_bytes, stream=None) -> int:
+    return lib().q8act_gemm_q8_0_repacked(_p(wq16), _p(wdt), _p(x), _p(y), m, n, k, _p(ws), ws_bytes,
+                                          _s(stream))
+
+
+def q8act_debug_gemm_repacked_block_dots(wq16, wdt, xqh, D, m, n, k, stream=None) -> int:
+    return lib().q8act_debug_gemm_repacked_block_dots(_p(wq16), _p(wdt), _p(xqh), _p(D), m, n, k,
+                                                      _s(stream))

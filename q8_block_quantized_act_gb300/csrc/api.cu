@@ -145,6 +145,20 @@ int q8act_dequant_q8_0_f16(const void *w, void *w16, int64_t n, int64_t k, void 
                                                (cudaStream_t)stream));
 }
 
+int64_t q8act_repack_ldn(int64_t n) { return n < 1 ? 0 : (n + 3) / 4 * 4; }
+
+int q8act_repack_q8_0(const void *w, uint16_t *wq16, float *wdt, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !wq16 || !wdt) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || n < 1 || n * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(wq16) || !aligned16(wdt)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_repack_q8_0(*dev, static_cast<const uint8_t *>(w), wq16, wdt, q8act_repack_ldn(n),
+                                          n, k, (cudaStream_t)stream));
+}
+
 static int gemv_common(const void *w, const int8_t *xq, const float *xd, float *y, int32_t *dots, int64_t m,
                        int64_t n, int64_t k, void *stream)
 {
@@ -219,6 +233,45 @@ int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, f
 {
     if (!y) return Q8ACT_ERR_NULL;
     return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, stream);
+}
+
+static int gemm_repacked_core(const uint16_t *wq16, const float *wdt, const uint16_t *xqh, const float *xdt,
+                              float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, void *stream)
+{
+    if (!wq16 || !wdt || !xqh || !xdt || (!y && !dots)) return Q8ACT_ERR_NULL;
+    if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
+    if (!aligned16(wq16) || !aligned16(wdt) || !aligned16(xqh) || !aligned16(xdt) || (y && !aligned16(y)) ||
+        (dots && !aligned16(dots)))
+        return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_gemm_q8_0_repacked(*dev, wq16, wdt, q8act_repack_ldn(n), xqh, xdt, y, dots, m, n, k,
+                                                 q8act_mmq_ldm(m), (cudaStream_t)stream));
+}
+
+int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float *x, float *y, int64_t m,
+                             int64_t n, int64_t k, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!wq16 || !wdt || !x || !y) return Q8ACT_ERR_NULL;
+    if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
+    const size_t need = q8act_gemm_workspace_bytes(m, k);
+    if (!ws || ws_bytes < need) return Q8ACT_ERR_WORKSPACE;
+    if (!aligned16(wq16) || !aligned16(wdt) || !aligned16(x) || !aligned16(y) || !aligned16(ws))
+        return Q8ACT_ERR_ALIGN;
+    uint16_t *xqh = static_cast<uint16_t *>(ws);
+    float *xdt = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k * 2 + 255) / 256 * 256);
+    int rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
+    if (rc) return rc;
+    return gemm_repacked_core(wq16, wdt, xqh, xdt, y, nullptr, m, n, k, stream);
+}
+
+int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt, const uint16_t *xqh, int32_t *D,
+                                         int64_t m, int64_t n, int64_t k, void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    // The dot stage needs a readable (unused) activation-scale array: reuse the quants.
+    return gemm_repacked_core(wq16, wdt, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, stream);
 }
 
 int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, int64_t m, int64_t n, int64_t k,

@@ -1,5 +1,7 @@
 // dequant.cu -- Q8_0 -> row-major binary16 (memra-engine 0.81.0 f16_ffi.rs,
-// memra_q8_0_dequant_f16: w16[r][32b+i] = fp16(d_w * q)).
+// memra_q8_0_dequant_f16: w16[r][32b+i] = fp16(d_w * q)), and the load-time repack for the
+// tensor-core GEMM (the same stream; it stores the exact binary16 quants wq16[r][32b+i] = q
+// and the scale plane wdt[b][r] = f32(d_w) instead of their rounded product).
 //
 // HBM-bound: 34 bytes in and 64 bytes out per block.  Persistent CTAs stream chunks of
 // whole rows (contiguous, 16-byte aligned) into a shared-memory ring with cp.async.bulk.
@@ -68,9 +70,10 @@ __device__ __forceinline__ void bytes_to_half2x2(uint32_t q4, __half2 &lo, __hal
     hi = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
 }
 
+template <bool REPACK>
 __global__ void __launch_bounds__(THREADS, 2)
-    dequant_q8_0_f16_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out, int n, int k,
-                            Plan p, int *status)
+    dequant_q8_0_f16_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out,
+                            float *__restrict__ wdt, int64_t ldn, int n, int k, Plan p, int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
@@ -146,10 +149,12 @@ __global__ void __launch_bounds__(THREADS, 2)
                 uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const __half2 prod = __hmul2_rn(h[j], d2);
+                    const __half2 prod = REPACK ? h[j] : __hmul2_rn(h[j], d2);
                     ow[j] = *reinterpret_cast<const uint32_t *>(&prod);
                 }
                 const int row = u / p.G, g = u - row * p.G;
+                if (REPACK && sub == 0)
+                    wdt[(int64_t)(g * GROUP_BLOCKS + jb) * ldn + row0 + row] = half_bits_to_float(dbits[e]);
                 // 256 outputs of the unit = 32 pieces of 16 bytes: piece `lane`.
                 __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)g * 256) / 8 + lane, o);
             }
@@ -159,10 +164,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
 }
 
-}  // namespace
-
-cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
-                                    int64_t n, int64_t k, cudaStream_t stream)
+template <bool REPACK>
+cudaError_t launch_stream(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16, float *wdt,
+                          int64_t ldn, int64_t n, int64_t k, cudaStream_t stream)
 {
     Plan p = make_plan(n, k, TWO_PER_SM_SMEM < dev.max_smem_optin ? TWO_PER_SM_SMEM : dev.max_smem_optin);
     int per_sm = 2;
@@ -171,16 +175,29 @@ cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uin
         per_sm = 1;
     }
     if (p.stages < 2) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(dequant_q8_0_f16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    auto kern = dequant_q8_0_f16_kernel<REPACK>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return e;
-    cudaFuncSetAttribute(dequant_q8_0_f16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    dequant_q8_0_f16_kernel<<<(int)grid, THREADS, p.smem, stream>>>(
-        w, reinterpret_cast<uint4 *>(w16), (int)n, (int)k, p, dev.status);
+    kern<<<(int)grid, THREADS, p.smem, stream>>>(w, reinterpret_cast<uint4 *>(w16), wdt, ldn, (int)n,
+                                                 (int)k, p, dev.status);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
+                                    int64_t n, int64_t k, cudaStream_t stream)
+{
+    return launch_stream<false>(dev, w, w16, nullptr, 0, n, k, stream);
+}
+
+cudaError_t launch_repack_q8_0(const DeviceInfo &dev, const uint8_t *w, uint16_t *wq16, float *wdt,
+                               int64_t ldn, int64_t n, int64_t k, cudaStream_t stream)
+{
+    return launch_stream<true>(dev, w, wq16, wdt, ldn, n, k, stream);
 }
 
 }  // namespace q8

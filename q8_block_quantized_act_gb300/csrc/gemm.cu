@@ -182,11 +182,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
     }
 }
 
-template <bool DOTS>
+// REPACKED: the weights come as the load-time repacked planes (binary16 quants [n][k] and
+// f32 scales [k/32][ldn]) and are loaded by TMA exactly like the activation; the converter
+// warps have nothing to do.
+template <bool DOTS, bool REPACKED>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_q8_0_kernel(const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_x,
-                     const __grid_constant__ CUtensorMap tm_xd, float *__restrict__ y,
+                     const __grid_constant__ CUtensorMap tm_xd,
+                     const __grid_constant__ CUtensorMap tm_wd, float *__restrict__ y,
                      int32_t *__restrict__ dots, int m, int n, int k, int *status)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -204,9 +208,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nb = k / QK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&bars.stage_full[s], 1 + 32 * NUM_CONV_WARPS); mbar_init(&bars.stage_empty[s], 1); }
+        constexpr uint32_t conv_arrivals = REPACKED ? 0 : 32 * NUM_CONV_WARPS;
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&bars.stage_full[s], 1 + conv_arrivals); mbar_init(&bars.stage_empty[s], 1); }
         for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], 32 * NUM_CONV_WARPS); }
-        for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + 32 * NUM_CONV_WARPS); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
+        for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + conv_arrivals); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
         for (int s = 0; s < D_PAIRS; ++s) { mbar_init(&bars.pair_full[s], 1); mbar_init(&bars.pair_empty[s], NUM_FOLD_WARPS); }
         mbar_init(bars.mma_done, 1);
         *abort_flag = 0;
@@ -221,6 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tensormap(&tm_w);
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_xd);
+        if (REPACKED) prefetch_tensormap(&tm_wd);
     }
     tc_fence_before();
     __syncthreads();
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int issued_raw = 0, issued_act = 0, issued_sc = 0;
             for (int kc = 0; kc < nkc; ++kc) {
-                if ((kc & (CHUNKS_PER_GROUP - 1)) == 0) {
+                if (!REPACKED && (kc & (CHUNKS_PER_GROUP - 1)) == 0) {
                     const int g = kc / CHUNKS_PER_GROUP;
                     const int rs = g % RAW_STAGES;
                     if (!wait_or_abort(&bars.raw_empty[rs], ((g / RAW_STAGES) & 1) ^ 1, status, abort_flag)) break;
@@ -244,13 +250,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const int st = kc % STAGES;
                 if (!wait_or_abort(&bars.stage_empty[st], ((kc / STAGES) & 1) ^ 1, status, abort_flag)) break;
-                mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES);
+                mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES + (REPACKED ? A_TILE_BYTES : 0));
                 tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, kc * KC, tok0, &bars.stage_full[st]);
+                if (REPACKED)
+                    tma_load_2d(smem + OFF_A + st * A_TILE_BYTES, &tm_w, kc * KC, row0, &bars.stage_full[st]);
                 ++issued_act;
                 const int ss = kc % SC_STAGES;
                 if (!wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) break;
-                mbar_arrive_expect_tx(&bars.sc_full[ss], 2 * BN * 4);
+                mbar_arrive_expect_tx(&bars.sc_full[ss], 2 * BN * 4 + (REPACKED ? 2 * BM * 4 : 0));
                 tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES, &tm_xd, tok0, 2 * kc, &bars.sc_full[ss]);
+                if (REPACKED)
+                    tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4, &tm_wd, row0, 2 * kc, &bars.sc_full[ss]);
                 ++issued_sc;
             }
             // Drain: never leave with a copy into this CTA's shared memory in flight.
@@ -290,6 +300,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(bars.mma_done, 0, status);
         }
     } else if (warp < NUM_CONV_WARPS) {
+        if (REPACKED) {
+            // nothing to convert: the producer loads the binary16 weight tiles directly
+        } else {
         // ------------------------------ converters ------------------------------
         // Thread t converts rows t and t + 64 of the tile.  For chunk `part` of a raw group,
         // the 68 bytes of its two blocks start at byte 68*part; the five 16-byte words from
@@ -349,6 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (part == CHUNKS_PER_GROUP - 1) mbar_arrive(&bars.raw_empty[rs]);
             }
             if (!ok) break;
+        }
         }
     } else {
         // ------------------------------ fold warps ------------------------------
@@ -487,6 +501,33 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 
 }  // namespace
 
+namespace {
+
+template <bool DOTS, bool REPACKED>
+cudaError_t launch_kernel(const CUtensorMap &tm_w, const CUtensorMap &tm_x, const CUtensorMap &tm_xd,
+                          const CUtensorMap &tm_wd, float *y, int32_t *dots, int64_t m, int64_t n,
+                          int64_t k, int *status, cudaStream_t stream)
+{
+    auto kern = gemm_q8_0_kernel<DOTS, REPACKED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    const dim3 grid((unsigned)((n + BM - 1) / BM), (unsigned)((m + BN - 1) / BN));
+    kern<<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n, (int)k, status);
+    return cudaGetLastError();
+}
+
+bool encode_activation(CUtensorMap *tm_x, CUtensorMap *tm_xd, const uint16_t *xqh, const float *xdt,
+                       int64_t m, int64_t k, int64_t ldm)
+{
+    return encode_2d(tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xqh, (uint64_t)k, (uint64_t)m, (uint64_t)k * 2,
+                     KC, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_2d(tm_xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xdt, (uint64_t)m, (uint64_t)(k / QK),
+                     (uint64_t)ldm * 4, BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
                              const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
                              int64_t k, int64_t ldm, cudaStream_t stream)
@@ -496,27 +537,28 @@ cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint
     // Raw weights viewed as uint16 elements: a 272-byte group is 136 elements (16-byte multiple).
     if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, row_bytes / 2, (uint64_t)n, row_bytes,
                    GROUP_BYTES / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xqh, (uint64_t)k, (uint64_t)m,
-                   (uint64_t)k * 2, KC, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tm_xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xdt, (uint64_t)m, (uint64_t)(k / QK),
-                   (uint64_t)ldm * 4, BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((n + BM - 1) / BM), (unsigned)((m + BN - 1) / BN));
-    cudaError_t e;
-    if (dots) {
-        e = cudaFuncSetAttribute(gemm_q8_0_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        cudaFuncSetAttribute(gemm_q8_0_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-        gemm_q8_0_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, y, dots, (int)m, (int)n, (int)k, dev.status);
-    } else {
-        e = cudaFuncSetAttribute(gemm_q8_0_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        cudaFuncSetAttribute(gemm_q8_0_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-        gemm_q8_0_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, y, dots, (int)m, (int)n, (int)k, dev.status);
-    }
-    return cudaGetLastError();
+    return dots ? launch_kernel<true, false>(tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, dev.status, stream)
+                : launch_kernel<false, false>(tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, dev.status, stream);
+}
+
+cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq16, const float *wdt,
+                                      int64_t ldn, const uint16_t *xqh, const float *xdt, float *y,
+                                      int32_t *dots, int64_t m, int64_t n, int64_t k, int64_t ldm,
+                                      cudaStream_t stream)
+{
+    CUtensorMap tm_w, tm_x, tm_xd, tm_wd;
+    // The weight planes have the activation's layouts: binary16 [n][k] tiles of 64 k x 128
+    // rows with the 128-byte swizzle, and f32 scales [k/32][ldn] in boxes of 128 rows x 2 blocks.
+    if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, wq16, (uint64_t)k, (uint64_t)n, (uint64_t)k * 2,
+                   KC, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tm_wd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, wdt, (uint64_t)n, (uint64_t)(k / QK),
+                   (uint64_t)ldn * 4, BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm))
+        return cudaErrorInvalidValue;
+    return dots ? launch_kernel<true, true>(tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, dev.status, stream)
+                : launch_kernel<false, true>(tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, dev.status, stream);
 }
 
 }  // namespace q8

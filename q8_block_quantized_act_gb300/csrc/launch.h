@@ -23,6 +23,8 @@ cudaError_t launch_quantize_q8_0(const DeviceInfo &dev, const float *w, uint8_t 
                                  int64_t k, cudaStream_t stream);
 cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
                                     int64_t n, int64_t k, cudaStream_t stream);
+cudaError_t launch_repack_q8_0(const DeviceInfo &dev, const uint8_t *w, uint16_t *wq16, float *wdt,
+                               int64_t ldn, int64_t n, int64_t k, cudaStream_t stream);
 
 // GEMV: returns cudaErrorInvalidValue when m*k is too large for the shared-memory plan.
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);
@@ -35,5 +37,9 @@ cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8
 cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
                              const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
                              int64_t k, int64_t ldm, cudaStream_t stream);
+cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq16, const float *wdt,
+                                      int64_t ldn, const uint16_t *xqh, const float *xdt, float *y,
+                                      int32_t *dots, int64_t m, int64_t n, int64_t k, int64_t ldm,
+                                      cudaStream_t stream);
 
 }  // namespace q8

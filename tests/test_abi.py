@@ -45,6 +45,8 @@ def test_workspace_query(L):
     assert q8.q8act_gemm_workspace_bytes(16, -256) == 0
     assert q8.q8act_mmq_ldm(1) == 4 and q8.q8act_mmq_ldm(4) == 4 and q8.q8act_mmq_ldm(5) == 8
     assert q8.q8act_mmq_ldm(0) == 0
+    assert q8.q8act_repack_ldn(1) == 4 and q8.q8act_repack_ldn(4096) == 4096
+    assert q8.q8act_repack_ldn(4097) == 4100 and q8.q8act_repack_ldn(0) == 0
 
 
 A = 1 << 20          # a fake, 16-byte aligned address: never dereferenced by these calls
@@ -76,6 +78,14 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_dequant_q8_0_f16(A, MIS, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
     (lambda: q8.q8act_debug_gemv_block_dots(A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
     (lambda: q8.q8act_debug_gemm_block_dots(A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_repack_q8_0(A, A, None, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_repack_q8_0(A, A, A, 8, 300, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_repack_q8_0(A, MIS, A, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_gemm_q8_0_repacked(A, None, A, A, 16, 8, 256, A, 1 << 30, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemm_q8_0_repacked(A, A, A, A, 16, 8, 256, A, 16, S0), q8.Q8ACT_ERR_WORKSPACE),
+    (lambda: q8.q8act_gemm_q8_0_repacked(A, A, A, A, 16, 8, 255, A, 1 << 30, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemm_q8_0_repacked(A, MIS, A, A, 16, 8, 256, A, 1 << 30, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_debug_gemm_repacked_block_dots(A, A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
 ])
 def test_host_side_refusals(L, call, want):
     assert call() == want
