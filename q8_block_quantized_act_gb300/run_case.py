@@ -4,7 +4,8 @@
     python -m q8_block_quantized_act_gb300.run_case gemm --m 512 --n 4096 --k 4096 --reps 2
 
 Kernels: quantize (q8_1), quantize_mmq, quantize_q8_0, gemv, gemm (fused quantize),
-gemm_preq, dequant.  Inputs are the seeded synthetic ones of q8_block_quantized_act_gb300.inputs;
+gemm_preq, gemm_repacked (fused quantize, load-time repacked weights), repack, dequant.
+Inputs are the seeded synthetic ones of q8_block_quantized_act_gb300.inputs;
 one warm-up launch precedes the `--reps` launches.
 """
 from __future__ import annotations
@@ -15,7 +16,7 @@ import argparse
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", choices=("quantize", "quantize_mmq", "quantize_q8_0", "gemv", "gemm",
-                                       "gemm_preq", "dequant"))
+                                       "gemm_preq", "gemm_repacked", "repack", "dequant"))
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=4096)
@@ -31,12 +32,13 @@ def main(argv=None):
     dev = torch.device("cuda")
     m, n, k = a.m, a.n, a.k
     x = torch.from_numpy(inputs.activations_f32(m, k)).to(dev)
-    need_w = a.kernel in ("gemv", "gemm", "gemm_preq", "dequant")
+    need_w = a.kernel in ("gemv", "gemm", "gemm_preq", "gemm_repacked", "repack", "dequant")
     w = q8.quantize_q8_0(torch.from_numpy(inputs.weights_f32(n, k)).to(dev)) if need_w else None
     w32 = torch.from_numpy(inputs.weights_f32(n, k)).to(dev) if a.kernel == "quantize_q8_0" else None
     xq, xd = q8.quantize_q8_1(x)
     xqh, xdt = q8.quantize_q8_1_mmq(x)
-    ws = q8.gemm_workspace(m, k, dev) if a.kernel == "gemm" else None
+    ws = q8.gemm_workspace(m, k, dev) if a.kernel in ("gemm", "gemm_repacked") else None
+    wq16, wdt = q8.repack_q8_0(w, n, k) if a.kernel in ("gemm_repacked", "repack") else (None, None)
     torch.cuda.synchronize()
 
     def once():
@@ -52,6 +54,10 @@ def main(argv=None):
             q8.gemm_q8_0(w, x, n, ws=ws)
         elif a.kernel == "gemm_preq":
             q8.gemm_q8_0_preq(w, xqh, xdt, n)
+        elif a.kernel == "gemm_repacked":
+            q8.gemm_q8_0_repacked(wq16, wdt, x, ws=ws)
+        elif a.kernel == "repack":
+            q8.check(q8.q8act_repack_q8_0(w, wq16, wdt, n, k))
         else:
             q8.dequant_q8_0_f16(w, n, k)
 
