@@ -117,9 +117,20 @@ int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, 
                     int64_t n, int64_t k, void *stream);
 
 /*
- * Workspace bytes q8act_gemm_q8_0 needs for an m x k activation (the MMQ-layout quants
- * and scales).  Returns 0 when the dimensions are invalid (as memra_fp8_blk_q8_0_bytes in
- * fp8_ffi.rs returns 0 on bad dims).
+ * Bytes of the workspace region that lets a fused GEMM split its last wave: when the
+ * 128 x 128 output tiles fill the GPU's SMs unevenly and the last wave would be less than
+ * half full, those tiles are cut into k pieces on the idle SMs, the pieces park partial
+ * tiles here and the last piece to finish adds them in piece order (a fixed order: the result
+ * does not depend on timing).  160 partial tiles of 64 KiB plus 160 counters.
+ */
+#define Q8ACT_GEMM_SPLIT_BYTES ((size_t)160 * 65536 + 160 * 4)
+
+/*
+ * Workspace bytes for the fused GEMMs on an m x k activation: the MMQ-layout quants and
+ * scales plus Q8ACT_GEMM_SPLIT_BYTES.  A workspace of at least
+ * q8act_gemm_workspace_bytes(m, k) - Q8ACT_GEMM_SPLIT_BYTES is accepted (the last wave is
+ * then never split).  Returns 0 when the dimensions are invalid (as
+ * memra_fp8_blk_q8_0_bytes in fp8_ffi.rs returns 0 on bad dims).
  */
 size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k);
 
@@ -128,7 +139,8 @@ size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k);
  * (fp8_ffi.rs memra_fp8_pp_gemm: one C-ABI call, quantize + GEMM on one stream, caller-owned
  * workspace):
  *   w [n rows of Q8_0 blocks], x [m][k] f32, y [m][n] f32 (overwritten),
- *   ws: device workspace of at least q8act_gemm_workspace_bytes(m, k) bytes.
+ *   ws: device workspace of q8act_gemm_workspace_bytes(m, k) bytes (at least that minus
+ *   Q8ACT_GEMM_SPLIT_BYTES; see there).
  *   m >= 1 (the pages route m >= 16 here; smaller m is accepted).
  */
 int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k,

@@ -16,7 +16,7 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401  (re-exported ABI)
     EXPORTED, LIB_PATH, Q8ACT_ERR_ALIGN, Q8ACT_ERR_CUDA_BASE, Q8ACT_ERR_DEVICE, Q8ACT_ERR_DIMS,
     Q8ACT_ERR_NULL, Q8ACT_ERR_TIMEOUT, Q8ACT_ERR_WORKSPACE, Q8ACT_GEMV_MAX_M, Q8ACT_MAX_K,
-    Q8ACT_NOALLOC_WS_BYTES, Q8ACT_OK, Q8ActError, check, lib, q8act_debug_gemm_block_dots, q8act_debug_gemv_block_dots,
+    Q8ACT_NOALLOC_WS_BYTES, Q8ACT_GEMM_SPLIT_BYTES, Q8ACT_OK, Q8ActError, check, lib, q8act_debug_gemm_block_dots, q8act_debug_gemv_block_dots,
     q8act_dequant_q8_0_f16, q8act_device_status, q8act_gemm_q8_0, q8act_gemm_q8_0_preq,
     q8act_gemm_q8_0_noalloc, q8act_gemm_workspace_bytes, q8act_gemv_q8_0, q8act_mmq_ldm, q8act_quantize_q8_0,
     q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror,

@@ -38,6 +38,7 @@ EXPORTED = (
     "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
+Q8ACT_GEMM_SPLIT_BYTES = 160 * 65536 + 160 * 4
 
 
 class Q8ActError(RuntimeError):

@@ -191,16 +191,24 @@ int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int
     return gemv_common(w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
 }
 
+// Workspace of the fused GEMMs: [binary16 quants][block-major scales][split region].  The
+// first two are required; with the split region as well, a launch whose last wave would be
+// less than half full cuts those tiles into k pieces.
+static size_t act_bytes(int64_t m, int64_t k)
+{
+    const size_t quants = (size_t)m * (size_t)k * 2;
+    const size_t scales = (size_t)(k / q8::QK) * (size_t)q8act_mmq_ldm(m) * 4;
+    return ((quants + 255) / 256 * 256) + ((scales + 255) / 256 * 256);
+}
+
 size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k)
 {
     if (check_k(k) != Q8ACT_OK || m < 1 || m * k > kMaxGemmElems) return 0;
-    const size_t quants = (size_t)m * (size_t)k * 2;
-    const size_t scales = (size_t)(k / q8::QK) * (size_t)q8act_mmq_ldm(m) * 4;
-    return ((quants + 255) / 256 * 256) + scales;
+    return act_bytes(m, k) + Q8ACT_GEMM_SPLIT_BYTES;
 }
 
 static int gemm_core(const void *w, const uint16_t *xqh, const float *xdt, float *y, int32_t *dots, int64_t m,
-                     int64_t n, int64_t k, void *stream)
+                     int64_t n, int64_t k, void *split_ws, size_t split_bytes, void *stream)
 {
     if (!w || !xqh || !xdt || (!y && !dots)) return Q8ACT_ERR_NULL;
     if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
@@ -210,7 +218,7 @@ static int gemm_core(const void *w, const uint16_t *xqh, const float *xdt, float
     int rc = current_device(&dev);
     if (rc) return rc;
     return cuda_rc(q8::launch_gemm_q8_0(*dev, static_cast<const uint8_t *>(w), xqh, xdt, y, dots, m, n, k,
-                                        q8act_mmq_ldm(m), (cudaStream_t)stream));
+                                        q8act_mmq_ldm(m), split_ws, split_bytes, (cudaStream_t)stream));
 }
 
 int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k, void *ws,
@@ -218,25 +226,26 @@ int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t 
 {
     if (!w || !x || !y) return Q8ACT_ERR_NULL;
     if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
-    const size_t need = q8act_gemm_workspace_bytes(m, k);
+    const size_t need = act_bytes(m, k);
     if (!ws || ws_bytes < need) return Q8ACT_ERR_WORKSPACE;
     if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(ws)) return Q8ACT_ERR_ALIGN;
     uint16_t *xqh = static_cast<uint16_t *>(ws);
     float *xdt = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k * 2 + 255) / 256 * 256);
     int rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
     if (rc) return rc;
-    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, stream);
+    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, static_cast<uint8_t *>(ws) + need, ws_bytes - need, stream);
 }
 
 int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, float *y, int64_t m, int64_t n,
                          int64_t k, void *stream)
 {
     if (!y) return Q8ACT_ERR_NULL;
-    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, stream);
+    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, nullptr, 0, stream);
 }
 
 static int gemm_repacked_core(const uint16_t *wq16, const float *wdt, const uint16_t *xqh, const float *xdt,
-                              float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, void *stream)
+                              float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, void *split_ws,
+                              size_t split_bytes, void *stream)
 {
     if (!wq16 || !wdt || !xqh || !xdt || (!y && !dots)) return Q8ACT_ERR_NULL;
     if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
@@ -247,7 +256,7 @@ static int gemm_repacked_core(const uint16_t *wq16, const float *wdt, const uint
     int rc = current_device(&dev);
     if (rc) return rc;
     return cuda_rc(q8::launch_gemm_q8_0_repacked(*dev, wq16, wdt, q8act_repack_ldn(n), xqh, xdt, y, dots, m, n, k,
-                                                 q8act_mmq_ldm(m), (cudaStream_t)stream));
+                                                 q8act_mmq_ldm(m), split_ws, split_bytes, (cudaStream_t)stream));
 }
 
 int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float *x, float *y, int64_t m,
@@ -255,7 +264,7 @@ int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float
 {
     if (!wq16 || !wdt || !x || !y) return Q8ACT_ERR_NULL;
     if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
-    const size_t need = q8act_gemm_workspace_bytes(m, k);
+    const size_t need = act_bytes(m, k);
     if (!ws || ws_bytes < need) return Q8ACT_ERR_WORKSPACE;
     if (!aligned16(wq16) || !aligned16(wdt) || !aligned16(x) || !aligned16(y) || !aligned16(ws))
         return Q8ACT_ERR_ALIGN;
@@ -263,7 +272,8 @@ int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float
     float *xdt = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k * 2 + 255) / 256 * 256);
     int rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
     if (rc) return rc;
-    return gemm_repacked_core(wq16, wdt, xqh, xdt, y, nullptr, m, n, k, stream);
+    return gemm_repacked_core(wq16, wdt, xqh, xdt, y, nullptr, m, n, k, static_cast<uint8_t *>(ws) + need,
+                              ws_bytes - need, stream);
 }
 
 int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt, const uint16_t *xqh, int32_t *D,
@@ -271,7 +281,8 @@ int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt,
 {
     if (!D) return Q8ACT_ERR_NULL;
     // The dot stage needs a readable (unused) activation-scale array: reuse the quants.
-    return gemm_repacked_core(wq16, wdt, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, stream);
+    return gemm_repacked_core(wq16, wdt, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, nullptr, 0,
+                              stream);
 }
 
 int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, int64_t m, int64_t n, int64_t k,
@@ -280,7 +291,7 @@ int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, 
     if (!D) return Q8ACT_ERR_NULL;
     // The dot stage needs a readable (unused) scale array of the right shape: reuse the
     // quants, which are larger than the scale array.
-    return gemm_core(w, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, stream);
+    return gemm_core(w, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, nullptr, 0, stream);
 }
 
 int q8act_device_status(void *stream)

@@ -182,6 +182,20 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
     }
 }
 
+// Work split of one launch.  Tiles (128 weight rows x 128 tokens, row tile fastest) below
+// tiles_full are done by one CTA each over the whole of k.  When the remaining tiles fill less
+// than half of a wave, each of them is cut into `pieces` k ranges (whole 256-wide groups) on
+// separate CTAs, which write partial tiles to `partial`; the piece that finishes last (counted
+// in `counters`) adds the partial tiles in piece order and stores the result, so the output
+// does not depend on which piece finishes first.
+struct Split {
+    int ntn;             // tiles along n
+    int tiles_full;
+    int pieces;          // 1: no split
+    float *partial;      // float4 [leftover tile][piece][8][512 fold threads]
+    unsigned *counters;  // [leftover tile], zero on entry, zero again on exit
+};
+
 // REPACKED: the weights come as the load-time repacked planes (binary16 quants [n][k] and
 // f32 scales [k/32][ldn]) and are loaded by TMA exactly like the activation; the converter
 // warps have nothing to do.
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_xd,
                      const __grid_constant__ CUtensorMap tm_wd, float *__restrict__ y,
-                     int32_t *__restrict__ dots, int m, int n, int k, int *status)
+                     int32_t *__restrict__ dots, int m, int n, int k, Split sp, int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -202,9 +216,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * BM;
-    const int tok0 = blockIdx.y * BN;
-    const int nkc = k / KC;
+    // This CTA's tile and k range; kc below counts the CTA's own chunks, kg0 + kc is the
+    // chunk's place in k.
+    const int ngroups_all = k / (KC * CHUNKS_PER_GROUP);
+    int tile, piece = -1, g0 = 0, g1 = ngroups_all;
+    if ((int)blockIdx.x < sp.tiles_full) {
+        tile = blockIdx.x;
+    } else {
+        const int j = blockIdx.x - sp.tiles_full;
+        tile = sp.tiles_full + j / sp.pieces;
+        piece = j % sp.pieces;
+        g0 = piece * ngroups_all / sp.pieces;
+        g1 = (piece + 1) * ngroups_all / sp.pieces;
+    }
+    const int row0 = (tile % sp.ntn) * BM;
+    const int tok0 = (tile / sp.ntn) * BN;
+    const int kg0 = g0 * CHUNKS_PER_GROUP;
+    const int nkc = (g1 - g0) * CHUNKS_PER_GROUP;
     const int nb = k / QK;
 
     if (threadIdx.x == 0) {
@@ -240,27 +268,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             int issued_raw = 0, issued_act = 0, issued_sc = 0;
             for (int kc = 0; kc < nkc; ++kc) {
                 if (!REPACKED && (kc & (CHUNKS_PER_GROUP - 1)) == 0) {
-                    const int g = kc / CHUNKS_PER_GROUP;
+                    const int g = kc / CHUNKS_PER_GROUP;       // local group (ring position)
                     const int rs = g % RAW_STAGES;
                     if (!wait_or_abort(&bars.raw_empty[rs], ((g / RAW_STAGES) & 1) ^ 1, status, abort_flag)) break;
                     mbar_arrive_expect_tx(&bars.raw_full[rs], RAW_TILE_BYTES);
-                    tma_load_2d(smem + OFF_RAW + rs * RAW_TILE_BYTES, &tm_w, g * (GROUP_BYTES / 2), row0,
+                    tma_load_2d(smem + OFF_RAW + rs * RAW_TILE_BYTES, &tm_w, (g0 + g) * (GROUP_BYTES / 2), row0,
                                 &bars.raw_full[rs]);
                     ++issued_raw;
                 }
                 const int st = kc % STAGES;
                 if (!wait_or_abort(&bars.stage_empty[st], ((kc / STAGES) & 1) ^ 1, status, abort_flag)) break;
                 mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES + (REPACKED ? A_TILE_BYTES : 0));
-                tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, kc * KC, tok0, &bars.stage_full[st]);
+                tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, (kg0 + kc) * KC, tok0, &bars.stage_full[st]);
                 if (REPACKED)
-                    tma_load_2d(smem + OFF_A + st * A_TILE_BYTES, &tm_w, kc * KC, row0, &bars.stage_full[st]);
+                    tma_load_2d(smem + OFF_A + st * A_TILE_BYTES, &tm_w, (kg0 + kc) * KC, row0, &bars.stage_full[st]);
                 ++issued_act;
                 const int ss = kc % SC_STAGES;
                 if (!wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) break;
                 mbar_arrive_expect_tx(&bars.sc_full[ss], 2 * BN * 4 + (REPACKED ? 2 * BM * 4 : 0));
-                tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES, &tm_xd, tok0, 2 * kc, &bars.sc_full[ss]);
+                tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES, &tm_xd, tok0, 2 * (kg0 + kc), &bars.sc_full[ss]);
                 if (REPACKED)
-                    tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4, &tm_wd, row0, 2 * kc, &bars.sc_full[ss]);
+                    tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4, &tm_wd, row0, 2 * (kg0 + kc), &bars.sc_full[ss]);
                 ++issued_sc;
             }
             // Drain: never leave with a copy into this CTA's shared memory in flight.
@@ -387,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {
-                const int b = 2 * kc + blk;
+                const int b = 2 * (kg0 + kc) + blk;
                 // Both 16-lane halves of this warp's 32 x 32 slice of the block's accumulator.
                 uint32_t d0[16], d1[16];
                 const uint32_t tcol = (uint32_t)((2 * pr + blk) * BN + FOLD_COLS * cq);
@@ -439,17 +467,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) mbar_arrive(&bars.sc_empty[ss]);
         }
         if (!DOTS && !*abort_flag) {
+            if (piece >= 0) {
+                // A piece of a split tile: park the partial sums, thread index fastest, so that
+                // every warp store is one contiguous 512-byte run.
+                float4 *dst = reinterpret_cast<float4 *>(sp.partial) +
+                              ((int64_t)(tile - sp.tiles_full) * sp.pieces + piece) * (2 * NJ * NUM_FOLD_WARPS * 32) +
+                              fw * 32 + lane;
 #pragma unroll
-            for (int hl = 0; hl < 2; ++hl)
+                for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                for (int j = 0; j < NJ; ++j)
+                    for (int j = 0; j < NJ; ++j)
+                        __stcg(dst + (hl * NJ + j) * (NUM_FOLD_WARPS * 32),
+                               make_float4(acc[hl][j][0].x, acc[hl][j][0].y, acc[hl][j][1].x, acc[hl][j][1].y));
+                __threadfence();
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
-                        const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
-                        const float2 v = acc[hl][j][e >> 1];
-                        if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = (e & 1) ? v.y : v.x;
-                    }
+                for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
+                            const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
+                            const float2 v = acc[hl][j][e >> 1];
+                            if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = (e & 1) ? v.y : v.x;
+                        }
+            }
         }
     }
 
@@ -459,6 +502,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS) : "memory");
+    }
+    if (DOTS || piece < 0) return;
+
+    // ---- split tile: the last piece to finish adds the partial tiles in piece order ----
+    volatile int *last = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
+    if (threadIdx.x == 0) {
+        const int lt = tile - sp.tiles_full;
+        const unsigned before = atomicAdd(&sp.counters[lt], 1u);
+        const bool is_last = before == (unsigned)sp.pieces - 1;
+        if (is_last) sp.counters[lt] = 0;   // ready for the next launch
+        __threadfence();
+        *last = is_last ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*last || *abort_flag || warp < NUM_CONV_WARPS || warp >= NUM_CONV_WARPS + NUM_FOLD_WARPS) return;
+    {
+        const int fw = warp - NUM_CONV_WARPS;
+        const int quarter = warp & 3;
+        const int cq = fw >> 2;
+        const int tr = lane >> 2;
+        const int tc = 2 * (lane & 3);
+        constexpr int NJ = FOLD_COLS / 8;
+        constexpr int FT = NUM_FOLD_WARPS * 32;
+        const float4 *src = reinterpret_cast<const float4 *>(sp.partial) +
+                            (int64_t)(tile - sp.tiles_full) * sp.pieces * (2 * NJ * FT) + fw * 32 + lane;
+        const int64_t piece_stride = 2 * NJ * FT;   // in float4
+        float4 sum[2 * NJ];
+#pragma unroll
+        for (int i = 0; i < 2 * NJ; ++i) sum[i] = __ldcg(src + i * FT);
+        for (int pc = 1; pc < sp.pieces; ++pc) {
+#pragma unroll
+            for (int i = 0; i < 2 * NJ; ++i) {
+                const float4 v = __ldcg(src + pc * piece_stride + i * FT);
+                sum[i].x = __fadd_rn(sum[i].x, v.x);
+                sum[i].y = __fadd_rn(sum[i].y, v.y);
+                sum[i].z = __fadd_rn(sum[i].z, v.z);
+                sum[i].w = __fadd_rn(sum[i].w, v.w);
+            }
+        }
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
+                    const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
+                    const float4 v = sum[hl * NJ + j];
+                    const float val = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+                    if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = val;
+                }
     }
 }
 
@@ -503,17 +597,58 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 
 namespace {
 
+}  // namespace
+
+size_t gemm_split_bytes();
+
+namespace {
+
+constexpr int kMaxSplitUnits = 160;   // CTAs of a split last wave (>= the SM count)
+constexpr size_t kPartialBytes = (size_t)kMaxSplitUnits * NUM_FOLD_WARPS * 32 * 32 * 4;
+
+// One CTA per tile; if the last wave would be less than half full, its tiles are cut into
+// k pieces that fill it (needs the split region of the workspace).
+Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, void *split_ws,
+                 size_t split_bytes, int64_t *grid, cudaStream_t stream, cudaError_t *err)
+{
+    Split sp{};
+    const int64_t ntn = (n + BM - 1) / BM, ntm = (m + BN - 1) / BN, tiles = ntn * ntm;
+    sp.ntn = (int)ntn;
+    sp.tiles_full = (int)tiles;
+    sp.pieces = 1;
+    *grid = tiles;
+    *err = cudaSuccess;
+    const int64_t slots = dev.num_sms < kMaxSplitUnits ? dev.num_sms : kMaxSplitUnits;
+    const int64_t rem = tiles % slots;
+    const int64_t ngroups = k / (KC * CHUNKS_PER_GROUP);
+    if (!split_ws || split_bytes < gemm_split_bytes() || rem == 0 || 2 * rem > slots) return sp;
+    int64_t pieces = slots / rem;
+    if (pieces > ngroups) pieces = ngroups;
+    if (pieces < 2) return sp;
+    sp.tiles_full = (int)(tiles - rem);
+    sp.pieces = (int)pieces;
+    sp.partial = static_cast<float *>(split_ws);
+    sp.counters = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(split_ws) + kPartialBytes);
+    *grid = sp.tiles_full + rem * pieces;
+    *err = cudaMemsetAsync(sp.counters, 0, (size_t)rem * sizeof(unsigned), stream);
+    return sp;
+}
+
 template <bool DOTS, bool REPACKED>
-cudaError_t launch_kernel(const CUtensorMap &tm_w, const CUtensorMap &tm_x, const CUtensorMap &tm_xd,
-                          const CUtensorMap &tm_wd, float *y, int32_t *dots, int64_t m, int64_t n,
-                          int64_t k, int *status, cudaStream_t stream)
+cudaError_t launch_kernel(const DeviceInfo &dev, const CUtensorMap &tm_w, const CUtensorMap &tm_x,
+                          const CUtensorMap &tm_xd, const CUtensorMap &tm_wd, float *y, int32_t *dots,
+                          int64_t m, int64_t n, int64_t k, void *split_ws, size_t split_bytes,
+                          cudaStream_t stream)
 {
     auto kern = gemm_q8_0_kernel<DOTS, REPACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    const dim3 grid((unsigned)((n + BM - 1) / BM), (unsigned)((m + BN - 1) / BN));
-    kern<<<grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n, (int)k, status);
+    int64_t grid = 0;
+    const Split sp = plan_split(dev, m, n, k, DOTS ? nullptr : split_ws, split_bytes, &grid, stream, &e);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n,
+                                                          (int)k, sp, dev.status);
     return cudaGetLastError();
 }
 
@@ -528,9 +663,17 @@ bool encode_activation(CUtensorMap *tm_x, CUtensorMap *tm_xd, const uint16_t *xq
 
 }  // namespace
 
+size_t gemm_split_bytes()
+{
+    static_assert(kPartialBytes + (size_t)kMaxSplitUnits * sizeof(unsigned) == Q8ACT_GEMM_SPLIT_BYTES,
+                  "split region size");
+    return Q8ACT_GEMM_SPLIT_BYTES;
+}
+
 cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
                              const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
-                             int64_t k, int64_t ldm, cudaStream_t stream)
+                             int64_t k, int64_t ldm, void *split_ws, size_t split_bytes,
+                             cudaStream_t stream)
 {
     CUtensorMap tm_w, tm_x, tm_xd;
     const uint64_t row_bytes = (uint64_t)k / QK * Q8_0_BYTES;
@@ -539,14 +682,15 @@ cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint
                    GROUP_BYTES / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm))
         return cudaErrorInvalidValue;
-    return dots ? launch_kernel<true, false>(tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, dev.status, stream)
-                : launch_kernel<false, false>(tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, dev.status, stream);
+    return dots ? launch_kernel<true, false>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, nullptr, 0, stream)
+                : launch_kernel<false, false>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, split_ws,
+                                              split_bytes, stream);
 }
 
 cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq16, const float *wdt,
                                       int64_t ldn, const uint16_t *xqh, const float *xdt, float *y,
                                       int32_t *dots, int64_t m, int64_t n, int64_t k, int64_t ldm,
-                                      cudaStream_t stream)
+                                      void *split_ws, size_t split_bytes, cudaStream_t stream)
 {
     CUtensorMap tm_w, tm_x, tm_xd, tm_wd;
     // The weight planes have the activation's layouts: binary16 [n][k] tiles of 64 k x 128
@@ -557,8 +701,9 @@ cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq1
                    (uint64_t)ldn * 4, BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm))
         return cudaErrorInvalidValue;
-    return dots ? launch_kernel<true, true>(tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, dev.status, stream)
-                : launch_kernel<false, true>(tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, dev.status, stream);
+    return dots ? launch_kernel<true, true>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, nullptr, 0, stream)
+                : launch_kernel<false, true>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, split_ws,
+                                             split_bytes, stream);
 }
 
 }  // namespace q8

@@ -40,16 +40,47 @@ def test_gemm_matches_oracle(m, n, k, kind):
     assert_within_tolerance(y, y64, S)
 
 
+def _min_workspace(m, k):
+    """A workspace without the last-wave split region (the call then never splits)."""
+    return torch.empty(q8.q8act_gemm_workspace_bytes(m, k) - q8.Q8ACT_GEMM_SPLIT_BYTES,
+                       dtype=torch.uint8, device="cuda")
+
+
 def test_gemm_preq_equals_fused():
+    """Without the split region the fused call is the quantizer followed by the pre-quantized
+    GEMM, bit for bit."""
     ensure_built()
     m, n, k = 200, 260, 1024
     _, x, wb, xq, xd = problem(m, n, k, "token_scales")
     w_d, x_d = cuda(wb), cuda(x)
-    y_fused = host(q8.gemm_q8_0(w_d, x_d, n))
+    y_fused = host(q8.gemm_q8_0(w_d, x_d, n, ws=_min_workspace(m, k)))
     xqh, xdt = q8.quantize_q8_1_mmq(x_d)
     y_pre = host(q8.gemm_q8_0_preq(w_d, xqh, xdt, n))
     device_ok()
     assert np.array_equal(y_fused.view(np.uint32), y_pre.view(np.uint32))
+
+
+@pytest.mark.parametrize("m,n,k", [
+    (200, 260, 1024),     # 6 tiles: every tile cut into the 4 groups of k
+    (1, 64, 4096),        # one tile cut into 16 pieces
+    (512, 5152, 4096),    # 164 tiles on 152 SMs: the 12 leftover tiles cut into 12 pieces
+    (130, 1200, 2048),    # 20 tiles, 8 pieces each, ragged in m and n
+])
+def test_gemm_last_wave_split(m, n, k):
+    """The split last wave: within 1e-5 * S of the oracle, deterministic, and within the same
+    bound of the unsplit result (only the order of the fold's f32 additions differs)."""
+    ensure_built()
+    _, x, wb, xq, xd = problem(m, n, k, "token_scales")
+    w_d, x_d = cuda(wb), cuda(x)
+    y_split = host(q8.gemm_q8_0(w_d, x_d, n))
+    y_again = host(q8.gemm_q8_0(w_d, x_d, n))
+    y_whole = host(q8.gemm_q8_0(w_d, x_d, n, ws=_min_workspace(m, k)))
+    device_ok()
+    rows = sample_rows(n, 256)
+    _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
+    assert_within_tolerance(y_split[:, rows], y64, S)
+    assert_within_tolerance(y_whole[:, rows], y64, S)
+    assert np.array_equal(y_split.view(np.uint32), y_again.view(np.uint32)), "not deterministic"
 
 
 @pytest.mark.parametrize("m,n", [(512, 4096), (512, 5152), (2048, 20480), (512, 64448)])
