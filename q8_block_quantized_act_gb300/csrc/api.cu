@@ -171,6 +171,9 @@ static int gemv_common(const void *w, const int8_t *xq, const float *xd, float *
     const q8::DeviceInfo *dev;
     int rc = current_device(&dev);
     if (rc) return rc;
+    if (q8::gemv_mma_supported(*dev, m, k))
+        return cuda_rc(q8::launch_gemv_q8_0_mma(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
+                                                (cudaStream_t)stream));
     if (!q8::gemv_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
     return cuda_rc(q8::launch_gemv_q8_0(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
                                         (cudaStream_t)stream));

@@ -1,0 +1,400 @@
+// gemv_mma.cu -- the multi-token GEMV (3 <= m <= 16: speculative verify and small batches)
+// on the warp-level tensor-core MMA.
+//
+// The dp4a GEMV re-reads the activation from shared memory for every row it folds, so above
+// m = 1 it is bound by shared-memory bandwidth.  Here a warp computes a 16-row x 8-token tile
+// of block dots with two mma.sync m16n8k16 (f16 in, f32 accumulate): each row fragment is read
+// once for 8 tokens, each token fragment once for 16 rows.  The quants enter as exact binary16
+// integers and every partial sum of a 32-wide block dot is an integer below 2^19, exact in
+// f32, so the block dot is the exact integer (the int8 mma.sync runs at a third of the f16
+// rate on this part).
+//
+// Per (row, token) the fold is the dp4a kernel's, operation for operation: acc = 0, then
+// acc = fma(d_w * d_a, D, acc) over the 8 blocks of each 256-wide group in order, then the
+// groups' sums combined by the same fixed tree (pairwise when the group count divides 32, else
+// left to right).  Token t's result is therefore bitwise the same for every m, and the same as
+// the m = 1 kernel's (the pages' decode == verify law, fp8_ffi.rs and f16_ffi.rs module docs).
+//
+// Layout: persistent CTAs; a producer warp copies R weight rows per chunk with one
+// cp.async.bulk per row into row slots padded to 16 (mod 128) bytes, so that the 8 rows a
+// warp reads at once fall in distinct banks.  The activation (int8) and its scales sit in
+// shared memory for the whole kernel, padded the same way.  Each MMA warp hands its weight
+// stage back as soon as its reads are done and parks its per-group partial sums in a partial
+// slot ([group][token][row]); reducer warps combine a chunk's partials in the fixed order and
+// store y while the MMA warps go on with the next chunk.  Every hand-off is an mbarrier with
+// a bounded wait; there is no CTA-wide barrier in the loop.
+#include "common.cuh"
+#include "launch.h"
+
+namespace q8 {
+namespace {
+
+constexpr int NW = 16;                   // MMA warps
+constexpr int NR = 3;                    // reducer warps
+constexpr int PRODUCER = NW + NR;        // bulk-copy producer warp
+constexpr int THREADS = (NW + NR + 1) * 32;
+constexpr int MAX_STAGES = 3;
+constexpr int MAX_ITEMS = 4;             // (16-row tile, group) items per warp and chunk
+
+struct MPlan {
+    int G;              // 256-wide groups per row
+    int RT;             // 16-row tiles per chunk
+    int R;              // rows per chunk (16 * RT)
+    int items;          // RT * G
+    int stages;
+    int warp_tree;      // 1: combine groups pairwise (G divides 32), else left to right
+    uint32_t row_bytes; // Q8_0 bytes per row
+    uint32_t rs;        // padded row slot in shared memory (16 mod 128)
+    uint32_t xs;        // padded activation row (16 mod 128)
+    uint32_t stage_bytes;
+    uint32_t part_bytes; // one partial slot: [G][8 mt][R] f32
+    int nparts;          // partial slots (1 or 2)
+    int64_t nchunks;
+    size_t off_x, off_xd, off_part, off_bar, smem;
+};
+
+MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap)
+{
+    MPlan p{};
+    p.G = (int)(k / 256);
+    p.RT = (NW + p.G - 1) / p.G;
+    if (p.RT < 1) p.RT = 1;
+    p.R = 16 * p.RT;
+    p.items = p.RT * p.G;
+    p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
+    p.rs = p.row_bytes + (uint32_t)((16 - (int64_t)(p.row_bytes % 128) + 128) % 128);
+    p.xs = (uint32_t)k + 16;
+    p.stage_bytes = (uint32_t)p.R * p.rs;
+    p.nchunks = (n + p.R - 1) / p.R;
+    p.warp_tree = (p.G <= 32 && 32 % p.G == 0) ? 1 : 0;
+    p.part_bytes = (uint32_t)((size_t)p.G * 8 * mt * p.R * 4);
+    const size_t x_bytes = (size_t)8 * mt * p.xs;
+    const size_t xd_bytes = (size_t)(k / QK) * 8 * mt * 4;
+    const size_t bars = 2 * (MAX_STAGES + 2) * 8 + 64;
+    // two stages and one partial slot at least; then a second slot, then a third stage
+    p.stages = 2;
+    p.nparts = 1;
+    auto total = [&]() {
+        return (size_t)p.stages * p.stage_bytes + x_bytes + xd_bytes + (size_t)p.nparts * p.part_bytes + bars;
+    };
+    if (total() > smem_cap) p.stages = 0;
+    if (p.stages) {
+        p.nparts = 2;
+        if (total() > smem_cap) p.nparts = 1;
+        ++p.stages;
+        if (total() > smem_cap) --p.stages;
+    }
+    p.off_x = (size_t)p.stages * p.stage_bytes;   // multiple of 16
+    p.off_xd = p.off_x + x_bytes;
+    p.off_part = (p.off_xd + xd_bytes + 15) & ~(size_t)15;
+    p.off_bar = p.off_part + (size_t)p.nparts * p.part_bytes;
+    p.smem = p.off_bar + 2 * (MAX_STAGES + 2) * 8;
+    return p;
+}
+
+bool mplan_ok(const MPlan &p, int)
+{
+    return p.stages >= 2 && (p.items + NW - 1) / NW <= MAX_ITEMS;
+}
+
+// Four signed bytes -> two f16x2 words holding the same integers (exact): (b ^ 0x80) is q + 128,
+// the binary16 pattern 0x64uu is 1024 + uu, and 1152 is subtracted.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t q4, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = q4 ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x5342);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                              const float (&c)[4])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// The quants of row `row` (in its slot) of block j of group g that this lane feeds to the
+// MMA: bytes 4c..4c+3 (lo) and 16+4c..16+4c+3 (hi) of the block's 32.
+__device__ __forceinline__ void load_row_quants(const uint8_t *rowp, int g, int j, int c, uint32_t &lo,
+                                                uint32_t &hi)
+{
+    const int bo = g * GROUP_BYTES + j * Q8_0_BYTES;   // block start (2 mod 4 when j is odd)
+    if ((j & 1) == 0) {
+        // quants start at bo + 2, 2 mod 4: two aligned words each, bytes 2..5 of the pair
+        const uint8_t *q = rowp + bo + 4 * c;
+        lo = __byte_perm(lds32(q), lds32(q + 4), 0x5432);
+        hi = __byte_perm(lds32(q + 16), lds32(q + 20), 0x5432);
+    } else {
+        const uint8_t *q = rowp + bo + 2 + 4 * c;       // word aligned
+        lo = lds32(q);
+        hi = lds32(q + 16);
+    }
+}
+
+template <int MT, bool DOTS>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemv_mma_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq,
+                    const float *__restrict__ xd, float *__restrict__ y, int32_t *__restrict__ dots,
+                    int m, int n, int k, MPlan p, int *status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *xs8 = smem + p.off_x;                                   // int8 [8 MT][xs]
+    float *xds = reinterpret_cast<float *>(smem + p.off_xd);         // f32 [k/32][8 MT]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + MAX_STAGES;
+    uint64_t *pfull = empty + MAX_STAGES;
+    uint64_t *pempty = pfull + 2;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int G = p.G;
+    const int nb = k / QK;
+    constexpr int TOK = 8 * MT;
+
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NW);
+        }
+        for (int s = 0; s < p.nparts; ++s) {
+            mbar_init(&pfull[s], NW);
+            mbar_init(&pempty[s], NR);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int64_t my_chunks =
+        blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (warp == PRODUCER) {
+        // ---------------- producer: one bulk copy per weight row into its padded slot ----------
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();   // the weights are read once
+            int64_t issued = 0;
+            for (int64_t i = 0; i < my_chunks; ++i) {
+                const int s = (int)(i % p.stages);
+                if (!mbar_wait(&empty[s], (uint32_t)(((i / p.stages) & 1) ^ 1), status)) break;
+                const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+                const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)rows * p.row_bytes);
+                uint8_t *dst = smem + (size_t)s * p.stage_bytes;
+                for (int r = 0; r < rows; ++r)
+                    bulk_g2s_hint(dst + (size_t)r * p.rs, w + (row0 + r) * (int64_t)p.row_bytes, p.row_bytes,
+                                  &full[s], policy);
+                ++issued;
+            }
+            for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
+                mbar_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+        }
+        return;
+    }
+
+    if (warp >= NW) {
+        // ---------------- reducers: combine the groups of each chunk in the fixed order -------
+        if (DOTS) return;
+        const int rtid = tid - NW * 32;
+        for (int64_t i = 0; i < my_chunks; ++i) {
+            const int ps = (int)(i % p.nparts);
+            const bool ok = mbar_wait(&pfull[ps], (uint32_t)((i / p.nparts) & 1), status);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+            const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+            const float *part = reinterpret_cast<const float *>(smem + p.off_part + (size_t)ps * p.part_bytes);
+            const size_t gstride = (size_t)TOK * p.R;
+            for (int idx = rtid; idx < rows * m; idx += NR * 32) {
+                const int t = idx / rows, r = idx - t * rows;   // rows fastest: consecutive addresses
+                const float *pr = part + (size_t)t * p.R + r;
+                float sum;
+                if (p.warp_tree) {
+                    // pairwise: ((p0 + p1) + (p2 + p3)) + ..., the dp4a kernel's butterfly order
+                    float v[32];
+#pragma unroll
+                    for (int gg = 0; gg < 32; ++gg) v[gg] = gg < G ? pr[gg * gstride] : 0.0f;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        if (o >= G) break;
+#pragma unroll
+                        for (int gg = 0; gg < 32; gg += 2 * o)
+                            if (gg < G) v[gg] = __fadd_rn(v[gg], v[gg + o]);
+                    }
+                    sum = v[0];
+                } else {
+                    sum = pr[0];
+                    for (int gg = 1; gg < G; ++gg) sum = __fadd_rn(sum, pr[gg * gstride]);
+                }
+                y[(int64_t)t * n + row0 + r] = sum;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[ps]);
+        }
+        return;
+    }
+
+    // ---------------- MMA warps: the activation cache (tokens >= m read as zero) -------------
+    for (int idx = tid; idx < TOK * (k / 16); idx += NW * 32) {
+        const int t = idx / (k / 16), c16 = idx - t * (k / 16);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (t < m) v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + c16 * 16);
+        *reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 16) = v;
+    }
+    for (int idx = tid; idx < nb * TOK; idx += NW * 32) {
+        const int b = idx / TOK, t = idx - b * TOK;
+        xds[idx] = t < m ? xd[(int64_t)t * nb + b] : 0.0f;
+    }
+    named_bar_sync(1, NW * 32);
+
+    const int gl = lane >> 2;     // fragment group: row within an 8-row half, token within 8
+    const int c = lane & 3;       // fragment column pair
+    for (int64_t i = 0; i < my_chunks; ++i) {
+        const int s = (int)(i % p.stages);
+        const bool ok = mbar_wait(&full[s], (uint32_t)((i / p.stages) & 1), status);
+        if (__any_sync(0xffffffffu, !ok)) break;
+        const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+        const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+        const uint8_t *stage = smem + (size_t)s * p.stage_bytes;
+
+        float acc[MAX_ITEMS][MT][4];
+#pragma unroll
+        for (int q = 0; q < MAX_ITEMS; ++q)
+#pragma unroll
+            for (int tg = 0; tg < MT; ++tg)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[q][tg][e] = 0.0f;
+
+#pragma unroll
+        for (int q = 0; q < MAX_ITEMS; ++q) {
+            const int it = warp + q * NW;
+            if (it >= p.items) break;
+            const int rt = it / G, g = it - rt * G;
+            const uint8_t *r0p = stage + (size_t)(16 * rt + gl) * p.rs;
+            const uint8_t *r1p = r0p + (size_t)8 * p.rs;
+#pragma unroll 2
+            for (int j = 0; j < GROUP_BLOCKS; ++j) {
+                uint32_t w0lo, w0hi, w1lo, w1hi;
+                load_row_quants(r0p, g, j, c, w0lo, w0hi);
+                load_row_quants(r1p, g, j, c, w1lo, w1hi);
+                // A fragments: k16 step 0 takes bytes 4c..4c+3, step 1 bytes 16+4c..16+4c+3
+                uint32_t a0[4], a1[4];
+                s8x4_to_f16x2x2(w0lo, a0[0], a0[2]);
+                s8x4_to_f16x2x2(w1lo, a0[1], a0[3]);
+                s8x4_to_f16x2x2(w0hi, a1[0], a1[2]);
+                s8x4_to_f16x2x2(w1hi, a1[1], a1[3]);
+                const int bo = g * GROUP_BYTES + j * Q8_0_BYTES;
+                const float dw0 = half_bits_to_float(*reinterpret_cast<const uint16_t *>(r0p + bo));
+                const float dw1 = half_bits_to_float(*reinterpret_cast<const uint16_t *>(r1p + bo));
+                const int b = g * GROUP_BLOCKS + j;
+#pragma unroll
+                for (int tg = 0; tg < MT; ++tg) {
+                    const uint8_t *xp = xs8 + (size_t)(8 * tg + gl) * p.xs + 32 * b + 4 * c;
+                    uint32_t b0lo, b0hi, b1lo, b1hi;
+                    s8x4_to_f16x2x2(lds32(xp), b0lo, b0hi);
+                    s8x4_to_f16x2x2(lds32(xp + 16), b1lo, b1hi);
+                    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                    float d[4];
+                    mma_f16_16816(d, a0, b0lo, b0hi, zero);
+                    float D[4];
+                    mma_f16_16816(D, a1, b1lo, b1hi, d);
+                    // D[0]: (row gl, token 2c), D[1]: (gl, 2c+1), D[2]: (gl+8, 2c), D[3]: (gl+8, 2c+1)
+                    if (DOTS) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = 16 * rt + gl + 8 * (e >> 1);
+                            const int t = 8 * tg + 2 * c + (e & 1);
+                            if (r < rows && t < m)
+                                dots[((int64_t)t * n + row0 + r) * nb + b] = __float2int_rn(D[e]);
+                        }
+                    } else {
+                        const float2 da = *reinterpret_cast<const float2 *>(xds + b * TOK + 8 * tg + 2 * c);
+                        acc[q][tg][0] = __fmaf_rn(__fmul_rn(dw0, da.x), D[0], acc[q][tg][0]);
+                        acc[q][tg][1] = __fmaf_rn(__fmul_rn(dw0, da.y), D[1], acc[q][tg][1]);
+                        acc[q][tg][2] = __fmaf_rn(__fmul_rn(dw1, da.x), D[2], acc[q][tg][2]);
+                        acc[q][tg][3] = __fmaf_rn(__fmul_rn(dw1, da.y), D[3], acc[q][tg][3]);
+                    }
+                }
+            }
+        }
+        // this warp's reads of the stage are done
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (DOTS) continue;
+
+        // park the group sums in partial slot ps ([group][token][row]) once the reducers are
+        // done with the slot's previous chunk
+        const int ps = (int)(i % p.nparts);
+        const bool free_ok = i < p.nparts ||
+                             mbar_wait(&pempty[ps], (uint32_t)(((i / p.nparts) & 1) ^ 1), status);
+        if (__any_sync(0xffffffffu, !free_ok)) break;
+        float *part = reinterpret_cast<float *>(smem + p.off_part + (size_t)ps * p.part_bytes);
+#pragma unroll
+        for (int q = 0; q < MAX_ITEMS; ++q) {
+            const int it = warp + q * NW;
+            if (it >= p.items) break;
+            const int rt = it / G, g = it - rt * G;
+#pragma unroll
+            for (int tg = 0; tg < MT; ++tg)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 16 * rt + gl + 8 * (e >> 1);
+                    const int t = 8 * tg + 2 * c + (e & 1);
+                    part[((size_t)g * TOK + t) * p.R + r] = acc[q][tg][e];
+                }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[ps]);
+    }
+}
+
+template <int MT, bool DOTS>
+cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
+                      int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+{
+    const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin);
+    if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
+    auto kern = gemv_mma_kernel<MT, DOTS>;
+    static bool attr_done = false;
+    static size_t attr_smem = 0;
+    if (!attr_done || attr_smem < p.smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+        if (e != cudaSuccess) return e;
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        attr_done = true;
+        attr_smem = p.smem;
+    }
+    const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
+    kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n, (int)k, p, dev.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k)
+{
+    // at m = 2 the dp4a kernel is still the faster one (both give the same bits)
+    if (m < 3 || m > 16) return false;
+    const int mt = m > 8 ? 2 : 1;
+    return mplan_ok(make_mplan(mt, 1 << 20, k, dev.max_smem_optin), mt);
+}
+
+cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
+                                 float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+{
+    if (m > 8)
+        return dots ? launch_mt<2, true>(dev, w, xq, xd, y, dots, m, n, k, stream)
+                    : launch_mt<2, false>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    return dots ? launch_mt<1, true>(dev, w, xq, xd, y, dots, m, n, k, stream)
+                : launch_mt<1, false>(dev, w, xq, xd, y, dots, m, n, k, stream);
+}
+
+}  // namespace q8
