@@ -35,6 +35,7 @@ constexpr int PRODUCER = NW + NR;        // bulk-copy producer warp
 constexpr int THREADS = (NW + NR + 1) * 32;
 constexpr int MAX_STAGES = 3;
 constexpr int MAX_ITEMS = 4;             // (16-row tile, group) items per warp and chunk
+constexpr int MAX_DEVICES = 16;
 
 struct MPlan {
     int G;              // 256-wide groups per row
@@ -363,14 +364,14 @@ cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
     const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
     auto kern = gemv_mma_kernel<MT, DOTS>;
-    static bool attr_done = false;
-    static size_t attr_smem = 0;
-    if (!attr_done || attr_smem < p.smem) {
+    // the attributes are per device: set them once per device (and again for a larger plan)
+    static size_t attr_smem[MAX_DEVICES] = {};
+    const bool cache = dev.device >= 0 && dev.device < MAX_DEVICES;
+    if (!cache || attr_smem[dev.device] < p.smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
         if (e != cudaSuccess) return e;
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        attr_done = true;
-        attr_smem = p.smem;
+        if (cache) attr_smem[dev.device] = p.smem;
     }
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
     kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n, (int)k, p, dev.status);
