@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "q8act.h"
 
 namespace q8 {
@@ -177,6 +179,26 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h16)
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c)
 {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+// ---------------------------------------------------------------------------------------
+// Host: a kernel's dynamic shared-memory limit and the largest carveout, set once per device
+// (and again when a launch needs more), not on every call -- the driver calls cost microseconds
+// of host time, as much as a small kernel runs.
+// ---------------------------------------------------------------------------------------
+constexpr int kAttrDevices = 16;
+
+template <auto Kern>
+cudaError_t set_kernel_smem(int device, size_t smem)
+{
+    static std::atomic<size_t> done[kAttrDevices];
+    const bool cache = device >= 0 && device < kAttrDevices;
+    if (cache && done[device].load(std::memory_order_relaxed) >= smem && smem > 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaFuncSetAttribute(Kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (cache) done[device].store(smem, std::memory_order_relaxed);
+    return cudaSuccess;
 }
 
 }  // namespace q8

@@ -176,9 +176,8 @@ cudaError_t launch_stream(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16
     }
     if (p.stages < 2) return cudaErrorInvalidValue;
     auto kern = dequant_q8_0_f16_kernel<REPACK>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    cudaError_t e = set_kernel_smem<dequant_q8_0_f16_kernel<REPACK>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
     kern<<<(int)grid, THREADS, p.smem, stream>>>(w, reinterpret_cast<uint4 *>(w16), wdt, ldn, (int)n,

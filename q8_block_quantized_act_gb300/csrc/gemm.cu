@@ -641,9 +641,8 @@ cudaError_t launch_kernel(const DeviceInfo &dev, const CUtensorMap &tm_w, const 
                           cudaStream_t stream)
 {
     auto kern = gemm_q8_0_kernel<DOTS, REPACKED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = set_kernel_smem<gemm_q8_0_kernel<DOTS, REPACKED>>(dev.device, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     int64_t grid = 0;
     const Split sp = plan_split(dev, m, n, k, DOTS ? nullptr : split_ws, split_bytes, &grid, stream, &e);
     if (e != cudaSuccess) return e;

@@ -289,10 +289,8 @@ cudaError_t launch_m(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, 
     const Plan p = choose_plan(M, n, k, dev.max_smem_optin);
     if (p.stages < 2) return cudaErrorInvalidValue;
     auto kern = gemv_q8_0_kernel<M, DOTS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p.smem);
+    cudaError_t e = set_kernel_smem<gemv_q8_0_kernel<M, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
     kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)n, (int)k, p,

@@ -35,7 +35,6 @@ constexpr int PRODUCER = NW + NR;        // bulk-copy producer warp
 constexpr int THREADS = (NW + NR + 1) * 32;
 constexpr int MAX_STAGES = 3;
 constexpr int MAX_ITEMS = 4;             // (16-row tile, group) items per warp and chunk
-constexpr int MAX_DEVICES = 16;
 
 struct MPlan {
     int G;              // 256-wide groups per row
@@ -364,15 +363,8 @@ cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
     const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
     auto kern = gemv_mma_kernel<MT, DOTS>;
-    // the attributes are per device: set them once per device (and again for a larger plan)
-    static size_t attr_smem[MAX_DEVICES] = {};
-    const bool cache = dev.device >= 0 && dev.device < MAX_DEVICES;
-    if (!cache || attr_smem[dev.device] < p.smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-        if (e != cudaSuccess) return e;
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        if (cache) attr_smem[dev.device] = p.smem;
-    }
+    cudaError_t e = set_kernel_smem<gemv_mma_kernel<MT, DOTS>>(dev.device, p.smem);
+    if (e != cudaSuccess) return e;
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
     kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n, (int)k, p, dev.status);
     return cudaGetLastError();
