@@ -62,6 +62,8 @@ extern "C" {
    i.e. the whole m < 16 range that the pages keep on the dp4a/MMVQ chain (fp8_ffi.rs and
    f16_ffi.rs module docs; m >= 16 is prefill). */
 #define Q8ACT_GEMV_MAX_M 15
+/* Largest number of weight matrices in one grouped GEMV call. */
+#define Q8ACT_GEMV_MAX_GROUP 8
 
 /* Library version, major*10000 + minor*100 + patch. */
 int q8act_version(void);
@@ -115,6 +117,17 @@ int q8act_quantize_q8_0(const float *w, void *wq, int64_t n, int64_t k, void *st
  */
 int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m,
                     int64_t n, int64_t k, void *stream);
+
+/*
+ * Grouped GEMV: count (1..Q8ACT_GEMV_MAX_GROUP) Q8_0 weight matrices that share one
+ * activation, streamed by one launch (the pages' fused multi-matrix decode GEMVs -- qkv with
+ * gate, the stacked experts' gate+up -- for weights kept in separate buffers; decode_kernel_
+ * census.rs).  w[i] is n[i] rows of Q8_0 blocks, y[i] [m][n[i]] f32 (overwritten); xq, xd,
+ * m, k as for q8act_gemv_q8_0.  w, y and n are HOST arrays of count entries; each y[i] is
+ * bitwise what q8act_gemv_q8_0 gives for w[i].
+ */
+int q8act_gemv_q8_0_group(const void *const *w, float *const *y, const int64_t *n, int count,
+                          const int8_t *xq, const float *xd, int64_t m, int64_t k, void *stream);
 
 /*
  * Bytes of the workspace region that lets a fused GEMM split its last wave: when the

@@ -20,7 +20,8 @@ from ._lib import (  # noqa: F401  (re-exported ABI)
     q8act_dequant_q8_0_f16, q8act_device_status, q8act_gemm_q8_0, q8act_gemm_q8_0_preq,
     q8act_gemm_q8_0_noalloc, q8act_gemm_workspace_bytes, q8act_gemv_q8_0, q8act_mmq_ldm, q8act_quantize_q8_0,
     q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror,
-    q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots)
+    q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots,
+    q8act_gemv_q8_0_group, Q8ACT_GEMV_MAX_GROUP)
 
 QK = 32
 Q8_0_BYTES = 34
@@ -67,6 +68,16 @@ def gemv_q8_0(w, xq, xd, n: int, out=None):
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
     check(q8act_gemv_q8_0(w, xq, xd, y, m, n, k), "q8act_gemv_q8_0")
     return y
+
+
+def gemv_q8_0_group(ws, xq, xd, ns, outs=None):
+    """Grouped decode GEMV: weight matrices ws (Q8_0 bytes of ns[i] rows each) sharing the
+    q8_1 activation (xq, xd) of m tokens, one launch; returns the list of outputs."""
+    import torch
+    m, k = xq.shape
+    ys = outs if outs is not None else [torch.empty((m, n), dtype=torch.float32, device=xq.device) for n in ns]
+    check(q8act_gemv_q8_0_group(ws, ys, ns, xq, xd, m, k), "q8act_gemv_q8_0_group")
+    return ys
 
 
 def gemm_workspace(m: int, k: int, device):

@@ -28,6 +28,7 @@ Q8ACT_ERR_TIMEOUT = -6
 Q8ACT_ERR_CUDA_BASE = 1000
 Q8ACT_MAX_K = 65536
 Q8ACT_GEMV_MAX_M = 15
+Q8ACT_GEMV_MAX_GROUP = 8
 
 EXPORTED = (
     "q8act_version", "q8act_strerror", "q8act_quantize_q8_1", "q8act_quantize_q8_1_mmq",
@@ -35,7 +36,7 @@ EXPORTED = (
     "q8act_gemm_q8_0", "q8act_gemm_q8_0_preq", "q8act_dequant_q8_0_f16",
     "q8act_debug_gemv_block_dots", "q8act_debug_gemm_block_dots", "q8act_device_status",
     "q8act_gemm_q8_0_noalloc", "q8act_repack_q8_0", "q8act_repack_ldn",
-    "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots",
+    "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots", "q8act_gemv_q8_0_group",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 Q8ACT_GEMM_SPLIT_BYTES = 160 * 65536 + 160 * 4
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
                 "q8act_repack_ldn": ([I64], I64),
                 "q8act_gemm_q8_0_repacked": ([P, P, P, P, I64, I64, I64, P, SZ, P], I32),
                 "q8act_debug_gemm_repacked_block_dots": ([P, P, P, P, I64, I64, I64, P], I32),
+                "q8act_gemv_q8_0_group": ([P, P, P, I32, P, P, I64, I64, P], I32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -197,3 +199,15 @@ def q8act_gemm_q8_0_repacked(wq16, wdt, x, y, m, n, k, ws, ws_bytes, stream=None
 def q8act_debug_gemm_repacked_block_dots(wq16, wdt, xqh, D, m, n, k, stream=None) -> int:
     return lib().q8act_debug_gemm_repacked_block_dots(_p(wq16), _p(wdt), _p(xqh), _p(D), m, n, k,
                                                       _s(stream))
+
+
+def q8act_gemv_q8_0_group(w, y, n, xq, xd, m, k, stream=None) -> int:
+    """w, y: sequences of tensors (or device addresses), n: sequence of row counts; the
+    pointer and size arrays are marshalled into host memory for the call."""
+    count = len(w)
+    Parr = ctypes.c_void_p * max(count, 1)
+    Narr = ctypes.c_int64 * max(count, 1)
+    wa = Parr(*[_p(v) for v in w])
+    ya = Parr(*[_p(v) for v in y])
+    na = Narr(*[int(v) for v in n])
+    return lib().q8act_gemv_q8_0_group(wa, ya, na, count, _p(xq), _p(xd), m, k, _s(stream))

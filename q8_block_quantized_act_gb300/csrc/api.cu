@@ -186,6 +186,26 @@ int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, 
     return gemv_common(w, xq, xd, y, nullptr, m, n, k, stream);
 }
 
+int q8act_gemv_q8_0_group(const void *const *w, float *const *y, const int64_t *n, int count, const int8_t *xq,
+                          const float *xd, int64_t m, int64_t k, void *stream)
+{
+    if (!w || !y || !n || !xq || !xd) return Q8ACT_ERR_NULL;
+    if (count < 1 || count > Q8ACT_GEMV_MAX_GROUP) return Q8ACT_ERR_DIMS;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_MAX_M) return Q8ACT_ERR_DIMS;
+    for (int i = 0; i < count; ++i) {
+        if (!w[i] || !y[i]) return Q8ACT_ERR_NULL;
+        if (n[i] < 1 || n[i] > INT32_MAX / 2 || n[i] * k > ((int64_t)1 << 36)) return Q8ACT_ERR_DIMS;
+        if (!aligned16(w[i]) || !aligned16(y[i])) return Q8ACT_ERR_ALIGN;
+    }
+    if (!aligned16(xq) || !aligned16(xd)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if (!q8::gemv_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
+    return cuda_rc(q8::launch_gemv_q8_0_group(*dev, reinterpret_cast<const uint8_t *const *>(w), y, n, count, xq, xd,
+                                              m, k, (cudaStream_t)stream));
+}
+
 int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n, int64_t k,
                                 void *stream)
 {

@@ -88,6 +88,38 @@ Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
     return p;
 }
 
+// Several weight matrices that share the activation, streamed by one launch (the census's
+// stacked expert gate+up and the fused qkv shapes, as separate buffers): chunk c belongs to
+// matrix i when first_chunk[i] <= c < first_chunk[i + 1].  A single GEMV is a group of one.
+struct Group {
+    int count;
+    const uint8_t *w[Q8ACT_GEMV_MAX_GROUP];
+    float *y[Q8ACT_GEMV_MAX_GROUP];
+    int n[Q8ACT_GEMV_MAX_GROUP];
+    int64_t first_chunk[Q8ACT_GEMV_MAX_GROUP + 1];
+};
+
+struct ChunkRef {
+    const uint8_t *w;
+    float *y;
+    int n;
+    int64_t row0;
+    int rows;
+};
+
+__device__ __forceinline__ ChunkRef chunk_ref(const Group &grp, int64_t chunk, int R)
+{
+    int mi = 0;
+    while (mi + 1 < grp.count && chunk >= grp.first_chunk[mi + 1]) ++mi;
+    ChunkRef c;
+    c.w = grp.w[mi];
+    c.y = grp.y[mi];
+    c.n = grp.n[mi];
+    c.row0 = (chunk - grp.first_chunk[mi]) * R;
+    c.rows = (int)((c.n - c.row0) < R ? (c.n - c.row0) : R);
+    return c;
+}
+
 __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
 {
     uint32_t r;
@@ -104,9 +136,9 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
 
 template <int M, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 2)
-    gemv_q8_0_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq,
-                     const float *__restrict__ xd, float *__restrict__ y,
-                     int32_t *__restrict__ dots, int n, int k, Plan p, int *status)
+    gemv_q8_0_kernel(const __grid_constant__ Group grp, const int8_t *__restrict__ xq,
+                     const float *__restrict__ xd, int32_t *__restrict__ dots, int k, Plan p,
+                     int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem + p.off_x);
@@ -156,12 +188,10 @@ __global__ void __launch_bounds__(THREADS, 2)
                 const int s = (int)(i % p.stages);
                 const uint32_t ph = (uint32_t)((i / p.stages) & 1);
                 if (!mbar_wait(&empty[s], ph ^ 1, status)) break;
-                const int64_t chunk = blockIdx.x + i * gridDim.x;
-                const int64_t row0 = chunk * p.R;
-                const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
-                const uint32_t bytes = (uint32_t)rows * p.row_bytes;
+                const ChunkRef cr = chunk_ref(grp, blockIdx.x + i * gridDim.x, p.R);
+                const uint32_t bytes = (uint32_t)cr.rows * p.row_bytes;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_g2s_hint(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, bytes, &full[s],
+                bulk_g2s_hint(smem + (size_t)s * p.chunk_bytes, cr.w + cr.row0 * p.row_bytes, bytes, &full[s],
                               policy);
                 ++issued;
             }
@@ -181,9 +211,11 @@ __global__ void __launch_bounds__(THREADS, 2)
         // whole warp when they are reduced with shuffles.
         if (p.warp_reduce ? __any_sync(0xffffffffu, !ok) : bar_red_or(1, CONSUMERS, !ok)) break;
 
-        const int64_t chunk = blockIdx.x + i * gridDim.x;
-        const int64_t row0 = chunk * p.R;
-        const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+        const ChunkRef cr = chunk_ref(grp, blockIdx.x + i * gridDim.x, p.R);
+        const int64_t row0 = cr.row0;
+        const int rows = cr.rows;
+        const int n = cr.n;
+        float *__restrict__ y = cr.y;
         const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
         float *pbuf = part + (size_t)(i & 1) * p.U * M;
 
@@ -283,42 +315,45 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 template <int M, bool DOTS>
-cudaError_t launch_m(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
-                     float *y, int32_t *dots, int64_t n, int64_t k, cudaStream_t stream)
+cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const float *xd,
+                     int32_t *dots, int64_t k, cudaStream_t stream)
 {
-    const Plan p = choose_plan(M, n, k, dev.max_smem_optin);
+    int64_t nmax = 0;
+    for (int i = 0; i < grp.count; ++i) nmax = grp.n[i] > nmax ? grp.n[i] : nmax;
+    Plan p = choose_plan(M, nmax, k, dev.max_smem_optin);
     if (p.stages < 2) return cudaErrorInvalidValue;
+    grp.first_chunk[0] = 0;
+    for (int i = 0; i < grp.count; ++i) grp.first_chunk[i + 1] = grp.first_chunk[i] + (grp.n[i] + p.R - 1) / p.R;
+    p.nchunks = grp.first_chunk[grp.count];
     auto kern = gemv_q8_0_kernel<M, DOTS>;
     cudaError_t e = set_kernel_smem<gemv_q8_0_kernel<M, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)n, (int)k, p,
-                                                  dev.status);
+    kern<<<(int)grid, THREADS, p.smem, stream>>>(grp, xq, xd, dots, (int)k, p, dev.status);
     return cudaGetLastError();
 }
 
 template <bool DOTS>
-cudaError_t dispatch(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
-                     float *y, int32_t *dots, int64_t m, int64_t n, int64_t k,
-                     cudaStream_t stream)
+cudaError_t dispatch(const DeviceInfo &dev, const Group &grp, const int8_t *xq, const float *xd,
+                     int32_t *dots, int64_t m, int64_t k, cudaStream_t stream)
 {
     switch (m) {
-    case 1: return launch_m<1, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 2: return launch_m<2, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 3: return launch_m<3, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 4: return launch_m<4, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 5: return launch_m<5, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 6: return launch_m<6, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 7: return launch_m<7, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 8: return launch_m<8, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 9: return launch_m<9, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 10: return launch_m<10, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 11: return launch_m<11, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 12: return launch_m<12, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 13: return launch_m<13, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 14: return launch_m<14, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
-    case 15: return launch_m<15, DOTS>(dev, w, xq, xd, y, dots, n, k, stream);
+    case 1: return launch_m<1, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 2: return launch_m<2, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 3: return launch_m<3, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 4: return launch_m<4, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 5: return launch_m<5, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 6: return launch_m<6, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 7: return launch_m<7, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 8: return launch_m<8, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 9: return launch_m<9, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 10: return launch_m<10, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 11: return launch_m<11, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 12: return launch_m<12, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 13: return launch_m<13, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 14: return launch_m<14, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 15: return launch_m<15, DOTS>(dev, grp, xq, xd, dots, k, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -335,8 +370,28 @@ cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8
                              const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
                              int64_t k, cudaStream_t stream)
 {
-    if (dots) return dispatch<true>(dev, w, xq, xd, y, dots, m, n, k, stream);
-    return dispatch<false>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    Group grp{};
+    grp.count = 1;
+    grp.w[0] = w;
+    grp.y[0] = y;
+    grp.n[0] = (int)n;
+    if (dots) return dispatch<true>(dev, grp, xq, xd, dots, m, k, stream);
+    return dispatch<false>(dev, grp, xq, xd, dots, m, k, stream);
+}
+
+cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,
+                                   const int64_t *n, int count, const int8_t *xq, const float *xd,
+                                   int64_t m, int64_t k, cudaStream_t stream)
+{
+    if (count < 1 || count > Q8ACT_GEMV_MAX_GROUP) return cudaErrorInvalidValue;
+    Group grp{};
+    grp.count = count;
+    for (int i = 0; i < count; ++i) {
+        grp.w[i] = w[i];
+        grp.y[i] = y[i];
+        grp.n[i] = (int)n[i];
+    }
+    return dispatch<false>(dev, grp, xq, xd, nullptr, m, k, stream);
 }
 
 }  // namespace q8

@@ -28,6 +28,9 @@ cudaError_t launch_repack_q8_0(const DeviceInfo &dev, const uint8_t *w, uint16_t
 
 // GEMV: returns cudaErrorInvalidValue when m*k is too large for the shared-memory plan.
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);
+cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,
+                                   const int64_t *n, int count, const int8_t *xq, const float *xd,
+                                   int64_t m, int64_t k, cudaStream_t stream);
 // The tensor-core GEMV for 3 <= m <= 16 (bitwise the same results as launch_gemv_q8_0).
 bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k);
 cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,

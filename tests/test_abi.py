@@ -86,6 +86,12 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_gemm_q8_0_repacked(A, A, A, A, 16, 8, 255, A, 1 << 30, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemm_q8_0_repacked(A, MIS, A, A, 16, 8, 256, A, 1 << 30, S0), q8.Q8ACT_ERR_ALIGN),
     (lambda: q8.q8act_debug_gemm_repacked_block_dots(A, A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemv_q8_0_group([], [], [], A, A, 1, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0_group([A] * 9, [A] * 9, [8] * 9, A, A, 1, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0_group([A, None], [A, A], [8, 8], A, A, 1, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemv_q8_0_group([A, A], [A, A], [8, 0], A, A, 1, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0_group([A, MIS], [A, A], [8, 8], A, A, 1, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_gemv_q8_0_group([A], [A], [8], A, A, q8.Q8ACT_GEMV_MAX_M + 1, 256, S0), q8.Q8ACT_ERR_DIMS),
 ])
 def test_host_side_refusals(L, call, want):
     assert call() == want

@@ -87,3 +87,21 @@ def test_gemv_k_limit(m, kmax):
     out = torch.zeros((m, 8), dtype=torch.float32, device="cuda")
     rc = q8.q8act_gemv_q8_0(w, aq, ad, out, m, 8, k)
     assert rc == q8.Q8ACT_ERR_DIMS
+
+
+@pytest.mark.parametrize("m,k,ns", [(1, 4096, (4096, 5152, 777)), (2, 1280, (4096, 33)),
+                                    (4, 4096, (64, 4096, 20480, 1)), (9, 2048, (300, 200, 100))])
+def test_gemv_group_equals_single_calls(m, k, ns):
+    """One grouped launch gives each matrix bitwise the result of its own GEMV."""
+    ensure_built()
+    ws = [problem(m, n, k, wseed=10 + i)[2] for i, n in enumerate(ns)]
+    _, _, _, xq, xd = problem(m, 8, k, "outliers")
+    xq_d, xd_d = cuda(xq), cuda(xd)
+    w_d = [cuda(wb) for wb in ws]
+    ys = [host(t) for t in q8.gemv_q8_0_group(w_d, xq_d, xd_d, list(ns))]
+    singles = [host(q8.gemv_q8_0(wd, xq_d, xd_d, n)) for wd, n in zip(w_d, ns)]
+    device_ok()
+    for i, (a, b) in enumerate(zip(ys, singles)):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), f"matrix {i}"
+    _, y64, S = oracle.matmul(ws[-1], xq, xd, k)
+    assert_within_tolerance(ys[-1], y64, S)
