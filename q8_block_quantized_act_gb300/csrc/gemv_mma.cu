@@ -45,7 +45,7 @@ struct MPlan {
     int warp_tree;      // 1: combine groups pairwise (G divides 32), else left to right
     uint32_t row_bytes; // Q8_0 bytes per row
     uint32_t rs;        // padded row slot in shared memory (16 mod 128)
-    uint32_t xs;        // padded activation row (16 mod 128)
+    uint32_t xs;        // padded activation row of the cache
     uint32_t stage_bytes;
     uint32_t part_bytes; // one partial slot: [G][8 mt][R] f32
     int nparts;          // partial slots (1 or 2)
@@ -63,7 +63,9 @@ MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap)
     p.items = p.RT * p.G;
     p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
     p.rs = p.row_bytes + (uint32_t)((16 - (int64_t)(p.row_bytes % 128) + 128) % 128);
-    p.xs = (uint32_t)k + 16;
+    // one token group (m <= 8): the cache holds binary16 (converted once), rows 32 (mod 128)
+    // bytes apart; two groups: int8, converted per use, rows 16 (mod 128) apart
+    p.xs = mt == 1 ? (uint32_t)(2 * k + 32) : (uint32_t)k + 16;
     p.stage_bytes = (uint32_t)p.R * p.rs;
     p.nchunks = (n + p.R - 1) / p.R;
     p.warp_tree = (p.G <= 32 && 32 % p.G == 0) ? 1 : 0;
@@ -149,7 +151,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     int m, int n, int k, MPlan p, int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *xs8 = smem + p.off_x;                                   // int8 [8 MT][xs]
+    // activation cache [8 MT][xs]: binary16 when MT == 1, int8 otherwise
+    uint8_t *xs8 = smem + p.off_x;
+    constexpr bool XH = MT == 1;
     float *xds = reinterpret_cast<float *>(smem + p.off_xd);         // f32 [k/32][8 MT]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + MAX_STAGES;
@@ -247,7 +251,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int t = idx / (k / 16), c16 = idx - t * (k / 16);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (t < m) v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + c16 * 16);
-        *reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 16) = v;
+        if (XH) {
+            uint4 h0, h1;
+            s8x4_to_f16x2x2(v.x, h0.x, h0.y);
+            s8x4_to_f16x2x2(v.y, h0.z, h0.w);
+            s8x4_to_f16x2x2(v.z, h1.x, h1.y);
+            s8x4_to_f16x2x2(v.w, h1.z, h1.w);
+            uint4 *dst = reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 32);
+            dst[0] = h0;
+            dst[1] = h1;
+        } else {
+            *reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 16) = v;
+        }
     }
     for (int idx = tid; idx < nb * TOK; idx += NW * 32) {
         const int b = idx / TOK, t = idx - b * TOK;
@@ -297,10 +312,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int b = g * GROUP_BLOCKS + j;
 #pragma unroll
                 for (int tg = 0; tg < MT; ++tg) {
-                    const uint8_t *xp = xs8 + (size_t)(8 * tg + gl) * p.xs + 32 * b + 4 * c;
                     uint32_t b0lo, b0hi, b1lo, b1hi;
-                    s8x4_to_f16x2x2(lds32(xp), b0lo, b0hi);
-                    s8x4_to_f16x2x2(lds32(xp + 16), b1lo, b1hi);
+                    if (XH) {
+                        const uint8_t *xp = xs8 + (size_t)gl * p.xs + 2 * (32 * b + 4 * c);
+                        const uint2 v0 = *reinterpret_cast<const uint2 *>(xp);
+                        const uint2 v1 = *reinterpret_cast<const uint2 *>(xp + 32);
+                        b0lo = v0.x; b0hi = v0.y; b1lo = v1.x; b1hi = v1.y;
+                    } else {
+                        const uint8_t *xp = xs8 + (size_t)(8 * tg + gl) * p.xs + 32 * b + 4 * c;
+                        s8x4_to_f16x2x2(lds32(xp), b0lo, b0hi);
+                        s8x4_to_f16x2x2(lds32(xp + 16), b1lo, b1hi);
+                    }
                     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
                     float d[4];
                     mma_f16_16816(d, a0, b0lo, b0hi, zero);
@@ -316,11 +338,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 dots[((int64_t)t * n + row0 + r) * nb + b] = __float2int_rn(D[e]);
                         }
                     } else {
+                        // acc = fma(d_w * d_a, D, acc) per lane, two lanes per instruction
                         const float2 da = *reinterpret_cast<const float2 *>(xds + b * TOK + 8 * tg + 2 * c);
-                        acc[q][tg][0] = __fmaf_rn(__fmul_rn(dw0, da.x), D[0], acc[q][tg][0]);
-                        acc[q][tg][1] = __fmaf_rn(__fmul_rn(dw0, da.y), D[1], acc[q][tg][1]);
-                        acc[q][tg][2] = __fmaf_rn(__fmul_rn(dw1, da.x), D[2], acc[q][tg][2]);
-                        acc[q][tg][3] = __fmaf_rn(__fmul_rn(dw1, da.y), D[3], acc[q][tg][3]);
+                        const float2 s0 = __fmul2_rn(make_float2(dw0, dw0), da);
+                        const float2 s1 = __fmul2_rn(make_float2(dw1, dw1), da);
+                        const float2 r0 = __ffma2_rn(s0, make_float2(D[0], D[1]), make_float2(acc[q][tg][0], acc[q][tg][1]));
+                        const float2 r1 = __ffma2_rn(s1, make_float2(D[2], D[3]), make_float2(acc[q][tg][2], acc[q][tg][3]));
+                        acc[q][tg][0] = r0.x; acc[q][tg][1] = r0.y;
+                        acc[q][tg][2] = r1.x; acc[q][tg][3] = r1.y;
                     }
                 }
             }
