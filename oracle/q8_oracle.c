@@ -139,6 +139,8 @@ static float quantize_block(const float *v, int8_t *q)
             continue;
         }
         float r = roundf(v[i] / d);
+        if (r != r)          /* NaN (a NaN entry, or inf / inf): out of contract, quantized to 0 */
+            r = 0.0f;
         if (r > 127.0f)
             r = 127.0f;
         if (r < -127.0f)

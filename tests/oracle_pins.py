@@ -277,6 +277,20 @@ def pin_repack(o, seed=9):
         assert np.array_equal(prod.astype(np.float16).view(np.uint16), o.dequant_f16(wb, k))
 
 
+def pin_nonfinite_inputs(o):
+    """Out-of-contract entries do not poison a block: a NaN entry is skipped by amax and
+    quantizes to 0; an infinite entry makes d infinite, so every finite entry quantizes to 0
+    and the infinite one (inf / inf) too."""
+    v = np.zeros((1, QK), np.float32)
+    v[0, :4] = [np.nan, 127.0, -63.5, 1.0]
+    q, d = o.quantize_q8_1(v)
+    assert d[0, 0] == np.float32(1.0)
+    assert q[0, :4].tolist() == [0, 127, -64, 1]
+    v[0, 0] = np.inf
+    q, d = o.quantize_q8_1(v)
+    assert np.isinf(d[0, 0]) and not q.any()
+
+
 ALL_PINS = [
     pin_f16_decode_exhaustive,
     pin_f16_encode_vs_numpy,
@@ -289,4 +303,5 @@ ALL_PINS = [
     pin_fold_bruteforce,
     pin_dequant_vs_numpy,
     pin_repack,
+    pin_nonfinite_inputs,
 ]

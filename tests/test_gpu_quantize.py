@@ -55,6 +55,27 @@ def test_quantize_q8_1_edge_cases():
     assert np.all(np.isfinite(host(xd)))
 
 
+def test_quantize_nonfinite_inputs():
+    """NaN and infinite entries are out of contract: no fault, and the same quants and scales
+    as the oracle (NaN entries quantize to 0; a block with an infinity gets d = inf, q = 0)."""
+    ensure_built()
+    x = edge_rows(256)
+    x[0, 3] = np.nan
+    x[0, 40] = np.nan
+    x[1, 100] = np.inf
+    x[2, 200] = -np.inf
+    x[3, 128:160] = np.nan               # a whole block of NaNs (d = 0)
+    x[3, 7] = np.nan                     # and one NaN in an otherwise finite block
+    xq_ref, xd_ref = oracle.quantize_q8_1(x)
+    xq, xd = q8.quantize_q8_1(cuda(x))
+    xqh, xdt = q8.quantize_q8_1_mmq(cuda(x))
+    device_ok()
+    assert np.array_equal(host(xq), xq_ref)
+    assert np.array_equal(host(xd).view(np.uint32), xd_ref.view(np.uint32))
+    assert np.array_equal(host(xqh).view(np.float16).astype(np.float32), xq_ref.astype(np.float32))
+    assert np.array_equal(host(xdt)[:, :x.shape[0]].T.copy().view(np.uint32), xd_ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("m,k", [(1, 256), (5, 512), (130, 4096), (512, 4096)])
 def test_quantize_q8_1_mmq_layout(m, k):
     ensure_built()
