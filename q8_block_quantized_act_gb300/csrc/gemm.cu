@@ -26,7 +26,6 @@ namespace q8 {
 namespace {
 
 constexpr int BM = 128;            // weight rows per tile
-constexpr int BN = 128;            // tokens per tile
 constexpr int KC = 64;             // k per chunk (one 128-byte swizzle row of binary16)
 constexpr int CHUNKS_PER_GROUP = 4;  // a 256-wide raw weight group feeds 4 chunks
 
@@ -34,34 +33,41 @@ constexpr int STAGES = 4;          // k chunks in flight: activation tile + conv
 constexpr int RAW_STAGES = 2;
 constexpr int SC_STAGES = 8;
 constexpr int D_PAIRS = 2;         // TMEM accumulator buffers, handed over in pairs (one chunk)
-constexpr int TMEM_COLS = 512;
-
-constexpr int ACT_TILE_BYTES = BN * KC * 2;        // 16384
 constexpr int A_TILE_BYTES = BM * KC * 2;          // 16384
 constexpr int RAW_TILE_BYTES = BM * GROUP_BYTES;   // 34816
-constexpr int SC_SLOT_BYTES = 2 * BN * 4 + 2 * BM * 4;  // act scales [2][BN], weight scales [2][BM]
-
-constexpr int OFF_ACT = 0;
-constexpr int OFF_A = OFF_ACT + STAGES * ACT_TILE_BYTES;
-constexpr int OFF_RAW = OFF_A + STAGES * A_TILE_BYTES;
-constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_TILE_BYTES;
-constexpr int OFF_BAR = OFF_SC + SC_STAGES * SC_SLOT_BYTES;
 constexpr int NUM_BARS = 2 * (STAGES + RAW_STAGES + SC_STAGES + D_PAIRS) + 1;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte base alignment
+constexpr int FOLD_COLS = 32;                      // columns per fold warp
+constexpr int RP_BN = 128;                         // tokens per tile of the repacked GEMM
 
-constexpr int NUM_CONV_WARPS = 2;
-constexpr int NUM_FOLD_WARPS = 16;
-constexpr int PRODUCER_WARP = NUM_CONV_WARPS + NUM_FOLD_WARPS;   // 18
-constexpr int MMA_WARP = PRODUCER_WARP + 1;                      // 19
-constexpr int THREADS = (MMA_WARP + 1) * 32;                     // 640 (20 warps)
-constexpr int FOLD_COLS = 32;                                    // columns per fold warp
-
-static_assert(OFF_A % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_SC % 128 == 0, "alignment");
-
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B binary16 (bits 7-9,
-// 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// Tile shapes.  128 tokens per tile, one CTA per SM: with 2 converter warps for raw Q8_0
+// input, without them for repacked weights; 16 fold warps.  Narrower tiles (64 tokens, two CTAs
+// per SM, 8 fold warps) are expressible but measured slower: half the work per MMA instruction
+// and twice the weight-tile traffic outweigh the overlap of the two CTAs' folds.
+template <int BN_, bool CONV>
+struct Cfg {
+    static constexpr int BN = BN_;                               // tokens per tile
+    static constexpr int TMEM_COLS = 2 * D_PAIRS * BN;           // four accumulator buffers
+    static constexpr int ACT_TILE_BYTES = BN * KC * 2;
+    static constexpr int SC_SLOT_BYTES = 2 * BN * 4 + 2 * BM * 4;  // act scales [2][BN], weight scales [2][BM]
+    static constexpr int RAW_ST = CONV ? RAW_STAGES : 0;
+    static constexpr int OFF_ACT = 0;
+    static constexpr int OFF_A = OFF_ACT + STAGES * ACT_TILE_BYTES;
+    static constexpr int OFF_RAW = OFF_A + STAGES * A_TILE_BYTES;
+    static constexpr int OFF_SC = OFF_RAW + RAW_ST * RAW_TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_SC + SC_STAGES * SC_SLOT_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte base alignment
+    static constexpr int NUM_CONV_WARPS = CONV ? 2 : 0;
+    static constexpr int NUM_FOLD_WARPS = 4 * BN / FOLD_COLS;
+    static constexpr int PRODUCER_WARP = NUM_CONV_WARPS + NUM_FOLD_WARPS;
+    static constexpr int MMA_WARP = PRODUCER_WARP + 1;
+    static constexpr int THREADS = (MMA_WARP + 1) * 32;
+    static constexpr int CTAS_PER_SM = BN == 128 ? 1 : 2;
+    // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B binary16 (bits 7-9,
+    // 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+    static constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    static_assert(OFF_A % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_SC % 128 == 0, "alignment");
+};
 
 // Shared-memory matrix descriptor for a K-major operand stored in 128-byte swizzled rows
 // (8-row atoms of 1024 bytes): start address >> 4 (bits 0-13), leading byte offset
@@ -76,14 +82,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                            uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -199,14 +205,20 @@ struct Split {
 // REPACKED: the weights come as the load-time repacked planes (binary16 quants [n][k] and
 // f32 scales [k/32][ldn]) and are loaded by TMA exactly like the activation; the converter
 // warps have nothing to do.
-template <bool DOTS, bool REPACKED>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool DOTS, bool REPACKED, int BN_T>
+__global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPACKED>::CTAS_PER_SM)
     gemm_q8_0_kernel(const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_xd,
                      const __grid_constant__ CUtensorMap tm_wd, float *__restrict__ y,
                      int32_t *__restrict__ dots, int m, int n, int k, Split sp, int *status)
 {
+    using C = Cfg<BN_T, !REPACKED>;
+    constexpr int BN = C::BN, TMEM_COLS = C::TMEM_COLS, ACT_TILE_BYTES = C::ACT_TILE_BYTES;
+    constexpr int SC_SLOT_BYTES = C::SC_SLOT_BYTES, OFF_ACT = C::OFF_ACT, OFF_A = C::OFF_A, OFF_RAW = C::OFF_RAW;
+    constexpr int OFF_SC = C::OFF_SC, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
+    constexpr int NUM_CONV_WARPS = C::NUM_CONV_WARPS, NUM_FOLD_WARPS = C::NUM_FOLD_WARPS;
+    constexpr int PRODUCER_WARP = C::PRODUCER_WARP, MMA_WARP = C::MMA_WARP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         constexpr uint32_t conv_arrivals = REPACKED ? 0 : 32 * NUM_CONV_WARPS;
         for (int s = 0; s < STAGES; ++s) { mbar_init(&bars.stage_full[s], 1 + conv_arrivals); mbar_init(&bars.stage_empty[s], 1); }
-        for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], 32 * NUM_CONV_WARPS); }
+        for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], REPACKED ? 1 : 32 * NUM_CONV_WARPS); }
         for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + conv_arrivals); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
         for (int s = 0; s < D_PAIRS; ++s) { mbar_init(&bars.pair_full[s], 1); mbar_init(&bars.pair_empty[s], NUM_FOLD_WARPS); }
         mbar_init(bars.mma_done, 1);
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const uint32_t off = (uint32_t)(h * 64 + kk * 32);
-                        tc_mma_f16(d_tmem, smem_desc_sw128(a_addr + off), smem_desc_sw128(b_addr + off), kk);
+                        tc_mma_f16(d_tmem, smem_desc_sw128(a_addr + off), smem_desc_sw128(b_addr + off), C::IDESC, kk);
                     }
                 }
                 tc_commit(&bars.pair_full[pr]);
@@ -604,11 +616,11 @@ size_t gemm_split_bytes();
 namespace {
 
 constexpr int kMaxSplitUnits = 160;   // CTAs of a split last wave (>= the SM count)
-constexpr size_t kPartialBytes = (size_t)kMaxSplitUnits * NUM_FOLD_WARPS * 32 * 32 * 4;
+constexpr size_t kPartialBytes = (size_t)kMaxSplitUnits * BM * 128 * 4;   // a 128 x 128 f32 tile each
 
 // One CTA per tile; if the last wave would be less than half full, its tiles are cut into
 // k pieces that fill it (needs the split region of the workspace).
-Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, void *split_ws,
+Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, int BN, int ctas_per_sm, void *split_ws,
                  size_t split_bytes, int64_t *grid, cudaStream_t stream, cudaError_t *err)
 {
     Split sp{};
@@ -618,7 +630,8 @@ Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, void *s
     sp.pieces = 1;
     *grid = tiles;
     *err = cudaSuccess;
-    const int64_t slots = dev.num_sms < kMaxSplitUnits ? dev.num_sms : kMaxSplitUnits;
+    const int64_t cap = (int64_t)dev.num_sms * ctas_per_sm;
+    const int64_t slots = cap < kMaxSplitUnits ? cap : kMaxSplitUnits;
     const int64_t rem = tiles % slots;
     const int64_t ngroups = k / (KC * CHUNKS_PER_GROUP);
     if (!split_ws || split_bytes < gemm_split_bytes() || rem == 0 || 2 * rem > slots) return sp;
@@ -634,30 +647,32 @@ Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, void *s
     return sp;
 }
 
-template <bool DOTS, bool REPACKED>
+template <bool DOTS, bool REPACKED, int BN_T>
 cudaError_t launch_kernel(const DeviceInfo &dev, const CUtensorMap &tm_w, const CUtensorMap &tm_x,
                           const CUtensorMap &tm_xd, const CUtensorMap &tm_wd, float *y, int32_t *dots,
                           int64_t m, int64_t n, int64_t k, void *split_ws, size_t split_bytes,
                           cudaStream_t stream)
 {
-    auto kern = gemm_q8_0_kernel<DOTS, REPACKED>;
-    cudaError_t e = set_kernel_smem<gemm_q8_0_kernel<DOTS, REPACKED>>(dev.device, SMEM_BYTES);
+    using C = Cfg<BN_T, !REPACKED>;
+    auto kern = gemm_q8_0_kernel<DOTS, REPACKED, BN_T>;
+    cudaError_t e = set_kernel_smem<gemm_q8_0_kernel<DOTS, REPACKED, BN_T>>(dev.device, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int64_t grid = 0;
-    const Split sp = plan_split(dev, m, n, k, DOTS ? nullptr : split_ws, split_bytes, &grid, stream, &e);
+    const Split sp = plan_split(dev, m, n, k, BN_T, C::CTAS_PER_SM, DOTS ? nullptr : split_ws, split_bytes, &grid,
+                                stream, &e);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n,
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n,
                                                           (int)k, sp, dev.status);
     return cudaGetLastError();
 }
 
 bool encode_activation(CUtensorMap *tm_x, CUtensorMap *tm_xd, const uint16_t *xqh, const float *xdt,
-                       int64_t m, int64_t k, int64_t ldm)
+                       int64_t m, int64_t k, int64_t ldm, int bn)
 {
     return encode_2d(tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xqh, (uint64_t)k, (uint64_t)m, (uint64_t)k * 2,
-                     KC, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                     KC, bn, CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode_2d(tm_xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xdt, (uint64_t)m, (uint64_t)(k / QK),
-                     (uint64_t)ldm * 4, BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+                     (uint64_t)ldm * 4, bn, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -679,10 +694,10 @@ cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint
     // Raw weights viewed as uint16 elements: a 272-byte group is 136 elements (16-byte multiple).
     if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, row_bytes / 2, (uint64_t)n, row_bytes,
                    GROUP_BYTES / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm))
+        !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm, 128))
         return cudaErrorInvalidValue;
-    return dots ? launch_kernel<true, false>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, nullptr, 0, stream)
-                : launch_kernel<false, false>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, split_ws,
+    return dots ? launch_kernel<true, false, 128>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, nullptr, 0, stream)
+                : launch_kernel<false, false, 128>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, split_ws,
                                               split_bytes, stream);
 }
 
@@ -698,10 +713,10 @@ cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq1
                    KC, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tm_wd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, wdt, (uint64_t)n, (uint64_t)(k / QK),
                    (uint64_t)ldn * 4, BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm))
+        !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm, RP_BN))
         return cudaErrorInvalidValue;
-    return dots ? launch_kernel<true, true>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, nullptr, 0, stream)
-                : launch_kernel<false, true>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, split_ws,
+    return dots ? launch_kernel<true, true, RP_BN>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, nullptr, 0, stream)
+                : launch_kernel<false, true, RP_BN>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, split_ws,
                                              split_bytes, stream);
 }
 

@@ -43,16 +43,21 @@ def test_gemm_repacked_block_dots_exact(m, n, k):
     (300, 520, 2048, "outliers"),
 ])
 def test_gemm_repacked_matches_oracle_and_raw(m, n, k, kind):
+    """Within 1e-5 * S of the oracle; and, with the last-wave split off (the two paths tile
+    differently, so a split cuts k at different places), bitwise the raw-Q8_0 GEMM."""
     ensure_built()
     _, x, wb, xq, xd = problem(m, n, k, kind)
     w_d, x_d = cuda(wb), cuda(x)
     wq16, wdt = q8.repack_q8_0(w_d, n, k)
     y = host(q8.gemm_q8_0_repacked(wq16, wdt, x_d))
-    y_raw = host(q8.gemm_q8_0(w_d, x_d, n))
+    small = torch.empty(q8.q8act_gemm_workspace_bytes(m, k) - q8.Q8ACT_GEMM_SPLIT_BYTES,
+                        dtype=torch.uint8, device="cuda")
+    y_whole = host(q8.gemm_q8_0_repacked(wq16, wdt, x_d, ws=small))
+    y_raw = host(q8.gemm_q8_0(w_d, x_d, n, ws=small))
     device_ok()
     _, y64, S = oracle.matmul(wb, xq, xd, k)
     assert_within_tolerance(y, y64, S)
-    assert np.array_equal(y.view(np.uint32), y_raw.view(np.uint32))
+    assert np.array_equal(y_whole.view(np.uint32), y_raw.view(np.uint32))
 
 
 @pytest.mark.parametrize("m,n", [(512, 4096), (2048, 20480)])
