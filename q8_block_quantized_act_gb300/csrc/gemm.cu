@@ -314,22 +314,26 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
     } else if (warp == MMA_WARP) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
+            // Descriptors of stage 0; a stage or a k step inside the 128-byte row only moves
+            // the 14-bit start-address field (all of shared memory is below 256 KB).
+            const uint64_t adesc0 = smem_desc_sw128(smem_u32(smem + OFF_A));
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + OFF_ACT));
             for (int kc = 0; kc < nkc; ++kc) {
                 const int st = kc % STAGES;
                 const int pr = kc & 1;
                 if (!wait_or_abort(&bars.stage_full[st], (kc / STAGES) & 1, status, abort_flag)) break;
                 if (!wait_or_abort(&bars.pair_empty[pr], ((kc >> 1) & 1) ^ 1, status, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + OFF_A + st * A_TILE_BYTES);
-                const uint32_t b_addr = smem_u32(smem + OFF_ACT + st * ACT_TILE_BYTES);
+                const uint64_t ad = adesc0 + (uint64_t)(st * (A_TILE_BYTES >> 4));
+                const uint64_t bd = bdesc0 + (uint64_t)(st * (ACT_TILE_BYTES >> 4));
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     // block 2kc+h -> accumulator buffer 2*pr+h
                     const uint32_t d_tmem = tmem_base + (uint32_t)((2 * pr + h) * BN);
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t off = (uint32_t)(h * 64 + kk * 32);
-                        tc_mma_f16(d_tmem, smem_desc_sw128(a_addr + off), smem_desc_sw128(b_addr + off), C::IDESC, kk);
+                        const uint64_t off = (uint64_t)((h * 64 + kk * 32) >> 4);
+                        tc_mma_f16(d_tmem, ad + off, bd + off, C::IDESC, kk);
                     }
                 }
                 tc_commit(&bars.pair_full[pr]);
