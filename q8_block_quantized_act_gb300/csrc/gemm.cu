@@ -12,13 +12,17 @@
 // tensor pipe runs ahead into other accumulator buffers while a block is being folded.
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N, TMEM columns), full k.
-// Warp roles (640 threads, 20 warps: a multiple of 4, so registers are not rounded away):
+// Warp roles, raw Q8_0 weights (640 threads, 20 warps: a multiple of 4, so registers are not
+// rounded away):
 //   warps 0-1   converters: raw Q8_0 rows (TMA, 272-byte groups) -> binary16 A tiles in the
 //               128-byte-swizzled K-major layout + f32 weight scales (two rows per thread)
 //   warps 2-17  fold: each owns 32 TMEM lanes (its warp index mod 4) x 32 columns;
 //               tcgen05.ld (16x256b) of a block's D, acc += (d_w * d_a) * D in packed f32x2
 //   warp 18     producer: TMA of activation tiles, activation scales and raw weight groups
 //   warp 19     TMEM allocator + single-thread MMA issuer
+// Repacked weights (608 threads): no converters; warps 0-15 fold, 16 producer (TMA of both
+// operand tiles and both scale vectors), 17 allocator + issuer of even chunks, 18 issuer of
+// odd chunks; six operand stages instead of four.
 #include "common.cuh"
 #include "launch.h"
 
@@ -29,13 +33,13 @@ constexpr int BM = 128;            // weight rows per tile
 constexpr int KC = 64;             // k per chunk (one 128-byte swizzle row of binary16)
 constexpr int CHUNKS_PER_GROUP = 4;  // a 256-wide raw weight group feeds 4 chunks
 
-constexpr int STAGES = 4;          // k chunks in flight: activation tile + converted weight tile
+constexpr int MAX_STAGES = 6;      // k chunks in flight: activation tile + weight tile
 constexpr int RAW_STAGES = 2;
 constexpr int SC_STAGES = 8;
 constexpr int D_PAIRS = 2;         // TMEM accumulator buffers, handed over in pairs (one chunk)
 constexpr int A_TILE_BYTES = BM * KC * 2;          // 16384
 constexpr int RAW_TILE_BYTES = BM * GROUP_BYTES;   // 34816
-constexpr int NUM_BARS = 2 * (STAGES + RAW_STAGES + SC_STAGES + D_PAIRS) + 1;
+constexpr int NUM_BARS = 2 * (MAX_STAGES + RAW_STAGES + SC_STAGES + D_PAIRS) + 1;
 constexpr int FOLD_COLS = 32;                      // columns per fold warp
 constexpr int RP_BN = 128;                         // tokens per tile of the repacked GEMM
 
@@ -46,6 +50,11 @@ constexpr int RP_BN = 128;                         // tokens per tile of the rep
 template <int BN_, bool CONV>
 struct Cfg {
     static constexpr int BN = BN_;                               // tokens per tile
+    // Operand stages: the raw path's shared memory also holds the raw weight groups; the
+    // repacked path spends it on a deeper ring, which two MMA issuers need to stay fed.
+    static constexpr int STAGES = CONV ? 4 : 6;
+    static_assert(STAGES <= MAX_STAGES && STAGES % D_PAIRS == 0,
+                  "a stage must always belong to the same accumulator pair");
     static constexpr int TMEM_COLS = 2 * D_PAIRS * BN;           // four accumulator buffers
     static constexpr int ACT_TILE_BYTES = BN * KC * 2;
     static constexpr int SC_SLOT_BYTES = 2 * BN * 4 + 2 * BM * 4;  // act scales [2][BN], weight scales [2][BM]
@@ -60,8 +69,11 @@ struct Cfg {
     static constexpr int NUM_CONV_WARPS = CONV ? 2 : 0;
     static constexpr int NUM_FOLD_WARPS = 4 * BN / FOLD_COLS;
     static constexpr int PRODUCER_WARP = NUM_CONV_WARPS + NUM_FOLD_WARPS;
-    static constexpr int MMA_WARP = PRODUCER_WARP + 1;
-    static constexpr int THREADS = (MMA_WARP + 1) * 32;
+    static constexpr int MMA_WARP = PRODUCER_WARP + 1;          // TMEM allocator, issues even chunks
+    // One MMA issuer per accumulator pair; with converter warps a second issuer would push the
+    // CTA to 21 warps and the register budget below 96.
+    static constexpr int NUM_MMA_WARPS = CONV ? 1 : D_PAIRS;
+    static constexpr int THREADS = (MMA_WARP + NUM_MMA_WARPS) * 32;
     static constexpr int CTAS_PER_SM = BN == 128 ? 1 : 2;
     // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B binary16 (bits 7-9,
     // 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -158,8 +170,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
 {
     uint64_t *b = reinterpret_cast<uint64_t *>(base);
     Bars r;
-    r.stage_full = b; b += STAGES;
-    r.stage_empty = b; b += STAGES;
+    r.stage_full = b; b += MAX_STAGES;
+    r.stage_empty = b; b += MAX_STAGES;
     r.raw_full = b; b += RAW_STAGES;
     r.raw_empty = b; b += RAW_STAGES;
     r.sc_full = b; b += SC_STAGES;
@@ -218,7 +230,8 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
     constexpr int SC_SLOT_BYTES = C::SC_SLOT_BYTES, OFF_ACT = C::OFF_ACT, OFF_A = C::OFF_A, OFF_RAW = C::OFF_RAW;
     constexpr int OFF_SC = C::OFF_SC, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
     constexpr int NUM_CONV_WARPS = C::NUM_CONV_WARPS, NUM_FOLD_WARPS = C::NUM_FOLD_WARPS;
-    constexpr int PRODUCER_WARP = C::PRODUCER_WARP, MMA_WARP = C::MMA_WARP;
+    constexpr int PRODUCER_WARP = C::PRODUCER_WARP, MMA_WARP = C::MMA_WARP, NUM_MMA_WARPS = C::NUM_MMA_WARPS;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
         for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], REPACKED ? 1 : 32 * NUM_CONV_WARPS); }
         for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + conv_arrivals); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
         for (int s = 0; s < D_PAIRS; ++s) { mbar_init(&bars.pair_full[s], 1); mbar_init(&bars.pair_empty[s], NUM_FOLD_WARPS); }
-        mbar_init(bars.mma_done, 1);
+        mbar_init(bars.mma_done, NUM_MMA_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -311,14 +324,18 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
             for (int i = issued_sc > SC_STAGES ? issued_sc - SC_STAGES : 0; i < issued_sc; ++i)
                 mbar_wait(&bars.sc_full[i % SC_STAGES], (i / SC_STAGES) & 1, status);
         }
-    } else if (warp == MMA_WARP) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp >= MMA_WARP) {
+        // ------------------------------ MMA issuers ------------------------------
+        // With two issuers, chunk kc goes to the issuer of accumulator pair kc & 1, so one
+        // issuer's waits and commits overlap the other's MMAs and the tensor pipe stays fed.
+        // A commit tracks the MMAs of its own thread only, which is all that the pair's and
+        // the stage's barriers need (a stage, like a pair, is only ever used by one issuer).
         if (lane == 0) {
             // Descriptors of stage 0; a stage or a k step inside the 128-byte row only moves
             // the 14-bit start-address field (all of shared memory is below 256 KB).
             const uint64_t adesc0 = smem_desc_sw128(smem_u32(smem + OFF_A));
             const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + OFF_ACT));
-            for (int kc = 0; kc < nkc; ++kc) {
+            for (int kc = warp - MMA_WARP; kc < nkc; kc += NUM_MMA_WARPS) {
                 const int st = kc % STAGES;
                 const int pr = kc & 1;
                 if (!wait_or_abort(&bars.stage_full[st], (kc / STAGES) & 1, status, abort_flag)) break;
@@ -339,7 +356,7 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                 tc_commit(&bars.pair_full[pr]);
                 tc_commit(&bars.stage_empty[st]);
             }
-            // All MMAs issued by this thread have completed once this arrives.
+            // All MMAs of both issuers have completed once this phase completes.
             tc_commit(bars.mma_done);
             mbar_wait(bars.mma_done, 0, status);
         }
