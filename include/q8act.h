@@ -155,6 +155,12 @@ size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k);
  *   ws: device workspace of q8act_gemm_workspace_bytes(m, k) bytes (at least that minus
  *   Q8ACT_GEMM_SPLIT_BYTES; see there).
  *   m >= 1 (the pages route m >= 16 here; smaller m is accepted).
+ * Enqueued on `stream`: at most one memset of the split counters, the quantizer kernel, then
+ * the GEMM kernel as a programmatic dependent of the quantizer (it starts its set-up while
+ * the quantizer finishes and waits for it before reading the activation).  The call is
+ * ordered after everything earlier on the stream, and later work on the stream is ordered
+ * after the GEMM, exactly as for plain launches.  q8act_gemm_q8_0_repacked and
+ * q8act_gemm_q8_0_noalloc do the same.
  */
 int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k,
                     void *ws, size_t ws_bytes, void *stream);

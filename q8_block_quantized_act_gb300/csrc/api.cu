@@ -230,8 +230,10 @@ size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k)
     return act_bytes(m, k) + Q8ACT_GEMM_SPLIT_BYTES;
 }
 
+// pdl: the stream's previous operation is the MMQ quantizer of the same call, enqueued after
+// q8::gemm_prepare_split; the GEMM is then launched as its programmatic dependent.
 static int gemm_core(const void *w, const uint16_t *xqh, const float *xdt, float *y, int32_t *dots, int64_t m,
-                     int64_t n, int64_t k, void *split_ws, size_t split_bytes, void *stream)
+                     int64_t n, int64_t k, void *split_ws, size_t split_bytes, bool pdl, void *stream)
 {
     if (!w || !xqh || !xdt || (!y && !dots)) return Q8ACT_ERR_NULL;
     if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
@@ -241,7 +243,7 @@ static int gemm_core(const void *w, const uint16_t *xqh, const float *xdt, float
     int rc = current_device(&dev);
     if (rc) return rc;
     return cuda_rc(q8::launch_gemm_q8_0(*dev, static_cast<const uint8_t *>(w), xqh, xdt, y, dots, m, n, k,
-                                        q8act_mmq_ldm(m), split_ws, split_bytes, (cudaStream_t)stream));
+                                        q8act_mmq_ldm(m), split_ws, split_bytes, pdl, (cudaStream_t)stream));
 }
 
 int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k, void *ws,
@@ -254,21 +256,27 @@ int q8act_gemm_q8_0(const void *w, const float *x, float *y, int64_t m, int64_t 
     if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(ws)) return Q8ACT_ERR_ALIGN;
     uint16_t *xqh = static_cast<uint16_t *>(ws);
     float *xdt = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k * 2 + 255) / 256 * 256);
-    int rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
+    void *split_ws = static_cast<uint8_t *>(ws) + need;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
     if (rc) return rc;
-    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, static_cast<uint8_t *>(ws) + need, ws_bytes - need, stream);
+    rc = cuda_rc(q8::gemm_prepare_split(*dev, m, n, k, false, split_ws, ws_bytes - need, (cudaStream_t)stream));
+    if (rc) return rc;
+    rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
+    if (rc) return rc;
+    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, split_ws, ws_bytes - need, true, stream);
 }
 
 int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, float *y, int64_t m, int64_t n,
                          int64_t k, void *stream)
 {
     if (!y) return Q8ACT_ERR_NULL;
-    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, nullptr, 0, stream);
+    return gemm_core(w, xqh, xdt, y, nullptr, m, n, k, nullptr, 0, false, stream);
 }
 
 static int gemm_repacked_core(const uint16_t *wq16, const float *wdt, const uint16_t *xqh, const float *xdt,
                               float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, void *split_ws,
-                              size_t split_bytes, void *stream)
+                              size_t split_bytes, bool pdl, void *stream)
 {
     if (!wq16 || !wdt || !xqh || !xdt || (!y && !dots)) return Q8ACT_ERR_NULL;
     if (check_gemm_dims(m, n, k) != Q8ACT_OK) return Q8ACT_ERR_DIMS;
@@ -279,7 +287,7 @@ static int gemm_repacked_core(const uint16_t *wq16, const float *wdt, const uint
     int rc = current_device(&dev);
     if (rc) return rc;
     return cuda_rc(q8::launch_gemm_q8_0_repacked(*dev, wq16, wdt, q8act_repack_ldn(n), xqh, xdt, y, dots, m, n, k,
-                                                 q8act_mmq_ldm(m), split_ws, split_bytes, (cudaStream_t)stream));
+                                                 q8act_mmq_ldm(m), split_ws, split_bytes, pdl, (cudaStream_t)stream));
 }
 
 int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float *x, float *y, int64_t m,
@@ -293,10 +301,15 @@ int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float
         return Q8ACT_ERR_ALIGN;
     uint16_t *xqh = static_cast<uint16_t *>(ws);
     float *xdt = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k * 2 + 255) / 256 * 256);
-    int rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
+    void *split_ws = static_cast<uint8_t *>(ws) + need;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
     if (rc) return rc;
-    return gemm_repacked_core(wq16, wdt, xqh, xdt, y, nullptr, m, n, k, static_cast<uint8_t *>(ws) + need,
-                              ws_bytes - need, stream);
+    rc = cuda_rc(q8::gemm_prepare_split(*dev, m, n, k, true, split_ws, ws_bytes - need, (cudaStream_t)stream));
+    if (rc) return rc;
+    rc = q8act_quantize_q8_1_mmq(x, xqh, xdt, m, k, stream);
+    if (rc) return rc;
+    return gemm_repacked_core(wq16, wdt, xqh, xdt, y, nullptr, m, n, k, split_ws, ws_bytes - need, true, stream);
 }
 
 int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt, const uint16_t *xqh, int32_t *D,
@@ -305,7 +318,7 @@ int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt,
     if (!D) return Q8ACT_ERR_NULL;
     // The dot stage needs a readable (unused) activation-scale array: reuse the quants.
     return gemm_repacked_core(wq16, wdt, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, nullptr, 0,
-                              stream);
+                              false, stream);
 }
 
 int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, int64_t m, int64_t n, int64_t k,
@@ -314,7 +327,7 @@ int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, 
     if (!D) return Q8ACT_ERR_NULL;
     // The dot stage needs a readable (unused) scale array of the right shape: reuse the
     // quants, which are larger than the scale array.
-    return gemm_core(w, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, nullptr, 0, stream);
+    return gemm_core(w, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, nullptr, 0, false, stream);
 }
 
 int q8act_device_status(void *stream)

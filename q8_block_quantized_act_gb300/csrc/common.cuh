@@ -79,6 +79,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // try_wait with a suspend-time hint: the waiting thread is parked by the hardware until the
 // phase completes or about `hint_ns` nanoseconds pass, instead of spinning on the issue slots
 // that the working warps of the same SM sub-partition need.
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may start while the previous kernel of the stream still runs; it must pass
+// griddep_wait() before touching what that kernel writes (the wait returns once that grid
+// has completed and its writes are visible; without a prerequisite grid it returns at once).
+// griddep_launch_dependents() lets such a dependent grid start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
 {
     uint32_t ok;

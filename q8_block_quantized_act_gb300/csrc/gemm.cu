@@ -303,6 +303,10 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                 }
                 const int st = kc % STAGES;
                 if (!wait_or_abort(&bars.stage_empty[st], ((kc / STAGES) & 1) ^ 1, status, abort_flag)) break;
+                // The activation may come from the kernel just before this one in the stream
+                // (launched as its programmatic dependent): everything above -- barriers, TMEM,
+                // the first raw weight group -- overlaps that kernel's tail.
+                if (kc == 0) griddep_wait();
                 mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES + (REPACKED ? A_TILE_BYTES : 0));
                 tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, (kg0 + kc) * KC, tok0, &bars.stage_full[st]);
                 if (REPACKED)
@@ -642,7 +646,7 @@ constexpr size_t kPartialBytes = (size_t)kMaxSplitUnits * BM * 128 * 4;   // a 1
 // One CTA per tile; if the last wave would be less than half full, its tiles are cut into
 // k pieces that fill it (needs the split region of the workspace).
 Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, int BN, int ctas_per_sm, void *split_ws,
-                 size_t split_bytes, int64_t *grid, cudaStream_t stream, cudaError_t *err)
+                 size_t split_bytes, bool zero_counters, int64_t *grid, cudaStream_t stream, cudaError_t *err)
 {
     Split sp{};
     const int64_t ntn = (n + BM - 1) / BM, ntm = (m + BN - 1) / BN, tiles = ntn * ntm;
@@ -664,14 +668,16 @@ Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, int BN,
     sp.partial = static_cast<float *>(split_ws);
     sp.counters = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(split_ws) + kPartialBytes);
     *grid = sp.tiles_full + rem * pieces;
-    *err = cudaMemsetAsync(sp.counters, 0, (size_t)rem * sizeof(unsigned), stream);
+    if (zero_counters) *err = cudaMemsetAsync(sp.counters, 0, (size_t)rem * sizeof(unsigned), stream);
     return sp;
 }
 
+// pdl: launch as a programmatic dependent of the stream's previous kernel (the activation
+// quantizer of the same call); the split counters were then zeroed before that kernel.
 template <bool DOTS, bool REPACKED, int BN_T>
 cudaError_t launch_kernel(const DeviceInfo &dev, const CUtensorMap &tm_w, const CUtensorMap &tm_x,
                           const CUtensorMap &tm_xd, const CUtensorMap &tm_wd, float *y, int32_t *dots,
-                          int64_t m, int64_t n, int64_t k, void *split_ws, size_t split_bytes,
+                          int64_t m, int64_t n, int64_t k, void *split_ws, size_t split_bytes, bool pdl,
                           cudaStream_t stream)
 {
     using C = Cfg<BN_T, !REPACKED>;
@@ -679,12 +685,25 @@ cudaError_t launch_kernel(const DeviceInfo &dev, const CUtensorMap &tm_w, const 
     cudaError_t e = set_kernel_smem<gemm_q8_0_kernel<DOTS, REPACKED, BN_T>>(dev.device, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int64_t grid = 0;
-    const Split sp = plan_split(dev, m, n, k, BN_T, C::CTAS_PER_SM, DOTS ? nullptr : split_ws, split_bytes, &grid,
-                                stream, &e);
+    const Split sp = plan_split(dev, m, n, k, BN_T, C::CTAS_PER_SM, DOTS ? nullptr : split_ws, split_bytes, !pdl,
+                                &grid, stream, &e);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n,
-                                                          (int)k, sp, dev.status);
-    return cudaGetLastError();
+    if (!pdl) {
+        kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m,
+                                                              (int)n, (int)k, sp, dev.status);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_xd, tm_wd, y, dots, (int)m, (int)n, (int)k, sp, dev.status);
 }
 
 bool encode_activation(CUtensorMap *tm_x, CUtensorMap *tm_xd, const uint16_t *xqh, const float *xdt,
@@ -705,9 +724,19 @@ size_t gemm_split_bytes()
     return Q8ACT_GEMM_SPLIT_BYTES;
 }
 
+cudaError_t gemm_prepare_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, bool repacked,
+                               void *split_ws, size_t split_bytes, cudaStream_t stream)
+{
+    int64_t grid = 0;
+    cudaError_t e = cudaSuccess;
+    const int ctas = repacked ? Cfg<RP_BN, false>::CTAS_PER_SM : Cfg<128, true>::CTAS_PER_SM;
+    plan_split(dev, m, n, k, repacked ? RP_BN : 128, ctas, split_ws, split_bytes, true, &grid, stream, &e);
+    return e;
+}
+
 cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
                              const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
-                             int64_t k, int64_t ldm, void *split_ws, size_t split_bytes,
+                             int64_t k, int64_t ldm, void *split_ws, size_t split_bytes, bool pdl,
                              cudaStream_t stream)
 {
     CUtensorMap tm_w, tm_x, tm_xd;
@@ -717,15 +746,16 @@ cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint
                    GROUP_BYTES / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm, 128))
         return cudaErrorInvalidValue;
-    return dots ? launch_kernel<true, false, 128>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, nullptr, 0, stream)
+    return dots ? launch_kernel<true, false, 128>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, nullptr, 0, pdl,
+                                                  stream)
                 : launch_kernel<false, false, 128>(dev, tm_w, tm_x, tm_xd, tm_xd, y, dots, m, n, k, split_ws,
-                                              split_bytes, stream);
+                                                   split_bytes, pdl, stream);
 }
 
 cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq16, const float *wdt,
                                       int64_t ldn, const uint16_t *xqh, const float *xdt, float *y,
                                       int32_t *dots, int64_t m, int64_t n, int64_t k, int64_t ldm,
-                                      void *split_ws, size_t split_bytes, cudaStream_t stream)
+                                      void *split_ws, size_t split_bytes, bool pdl, cudaStream_t stream)
 {
     CUtensorMap tm_w, tm_x, tm_xd, tm_wd;
     // The weight planes have the activation's layouts: binary16 [n][k] tiles of 64 k x 128
@@ -736,9 +766,10 @@ cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq1
                    (uint64_t)ldn * 4, BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_activation(&tm_x, &tm_xd, xqh, xdt, m, k, ldm, RP_BN))
         return cudaErrorInvalidValue;
-    return dots ? launch_kernel<true, true, RP_BN>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, nullptr, 0, stream)
+    return dots ? launch_kernel<true, true, RP_BN>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, nullptr, 0, pdl,
+                                                   stream)
                 : launch_kernel<false, true, RP_BN>(dev, tm_w, tm_x, tm_xd, tm_wd, y, dots, m, n, k, split_ws,
-                                             split_bytes, stream);
+                                                    split_bytes, pdl, stream);
 }
 
 }  // namespace q8

@@ -43,13 +43,19 @@ cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8
 // With dots != nullptr the fold is replaced by a store of the block dots D[m][n][k/32].
 // Bytes of the optional workspace region that lets a GEMM split its last partial wave.
 size_t gemm_split_bytes();
+// pdl: launch as a programmatic dependent of the stream's previous kernel, which must be the
+// MMQ quantizer producing xqh / xdt (it lets the GEMM start early; the GEMM waits for it
+// before reading them), with gemm_prepare_split already enqueued before that quantizer.
+// Without pdl the launch is ordinary and zeroes the split counters itself.
+cudaError_t gemm_prepare_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, bool repacked,
+                               void *split_ws, size_t split_bytes, cudaStream_t stream);
 cudaError_t launch_gemm_q8_0(const DeviceInfo &dev, const uint8_t *w, const uint16_t *xqh,
                              const float *xdt, float *y, int32_t *dots, int64_t m, int64_t n,
-                             int64_t k, int64_t ldm, void *split_ws, size_t split_bytes,
+                             int64_t k, int64_t ldm, void *split_ws, size_t split_bytes, bool pdl,
                              cudaStream_t stream);
 cudaError_t launch_gemm_q8_0_repacked(const DeviceInfo &dev, const uint16_t *wq16, const float *wdt,
                                       int64_t ldn, const uint16_t *xqh, const float *xdt, float *y,
                                       int32_t *dots, int64_t m, int64_t n, int64_t k, int64_t ldm,
-                                      void *split_ws, size_t split_bytes, cudaStream_t stream);
+                                      void *split_ws, size_t split_bytes, bool pdl, cudaStream_t stream);
 
 }  // namespace q8

@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__
                                                                 int64_t m, int chunks_per_row,
                                                                 int64_t ldm)
 {
+    // The GEMM that consumes this layout may be launched as a programmatic dependent: let it
+    // start its prologue (it waits for this grid before reading the activation).
+    griddep_launch_dependents();
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= chunks_per_row) return;
     for (int64_t t = blockIdx.y; t < m; t += gridDim.y) {
