@@ -261,9 +261,9 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
     const int nb = k / QK;
 
     if (threadIdx.x == 0) {
-        constexpr uint32_t conv_arrivals = REPACKED ? 0 : 32 * NUM_CONV_WARPS;
+        constexpr uint32_t conv_arrivals = REPACKED ? 0 : NUM_CONV_WARPS;     // one lane per converter warp
         for (int s = 0; s < STAGES; ++s) { mbar_init(&bars.stage_full[s], 1 + conv_arrivals); mbar_init(&bars.stage_empty[s], 1); }
-        for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], REPACKED ? 1 : 32 * NUM_CONV_WARPS); }
+        for (int s = 0; s < RAW_STAGES; ++s) { mbar_init(&bars.raw_full[s], 1); mbar_init(&bars.raw_empty[s], REPACKED ? 1 : NUM_CONV_WARPS); }
         for (int s = 0; s < SC_STAGES; ++s) { mbar_init(&bars.sc_full[s], 1 + conv_arrivals); mbar_init(&bars.sc_empty[s], NUM_FOLD_WARPS); }
         for (int s = 0; s < D_PAIRS; ++s) { mbar_init(&bars.pair_full[s], 1); mbar_init(&bars.pair_empty[s], NUM_FOLD_WARPS); }
         mbar_init(bars.mma_done, NUM_MMA_WARPS);
@@ -371,7 +371,9 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
         // ------------------------------ converters ------------------------------
         // Thread t converts rows t and t + 64 of the tile.  For chunk `part` of a raw group,
         // the 68 bytes of its two blocks start at byte 68*part; the five 16-byte words from
-        // byte 64*part cover them, the data starting at word `part` of that window.
+        // byte 64*part cover them, the data starting at word `part` of that window.  Both
+        // rows' words are read before the waits for the destination slots, and each warp
+        // reports a finished chunk with one arrival (after every lane's proxy fence).
         const int ngroups = nkc / CHUNKS_PER_GROUP;
         for (int g = 0; g < ngroups; ++g) {
             const int rs = g % RAW_STAGES;
@@ -382,6 +384,17 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                 const int kc = g * CHUNKS_PER_GROUP + part;
                 const int aslot = kc % STAGES;
                 const int ss = kc % SC_STAGES;
+                uint32_t wv[2][20];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        smem + OFF_RAW + rs * RAW_TILE_BYTES + (threadIdx.x + 64 * rr) * GROUP_BYTES + 64 * part);
+#pragma unroll
+                    for (int c = 0; c < 5; ++c) {
+                        const uint4 v = src[c];
+                        wv[rr][4 * c + 0] = v.x; wv[rr][4 * c + 1] = v.y; wv[rr][4 * c + 2] = v.z; wv[rr][4 * c + 3] = v.w;
+                    }
+                }
                 if (!wait_or_abort(&bars.stage_empty[aslot], ((kc / STAGES) & 1) ^ 1, status, abort_flag) ||
                     !wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) {
                     ok = false;
@@ -391,14 +404,6 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int r = threadIdx.x + 64 * rr;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        smem + OFF_RAW + rs * RAW_TILE_BYTES + r * GROUP_BYTES + 64 * part);
-                    uint32_t wv[20];
-#pragma unroll
-                    for (int c = 0; c < 5; ++c) {
-                        const uint4 v = src[c];
-                        wv[4 * c + 0] = v.x; wv[4 * c + 1] = v.y; wv[4 * c + 2] = v.z; wv[4 * c + 3] = v.w;
-                    }
                     // block 2*part: scale in the low half of data word 0, quants straddle words;
                     // block 2*part+1: scale in the high half of data word 8, quants in words 9..16.
                     const int w0 = part;
@@ -407,24 +412,27 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                     const int sw = r & 7;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint32_t q0 = __byte_perm(wv[w0 + 2 * c], wv[w0 + 2 * c + 1], 0x5432);
-                        const uint32_t q1 = __byte_perm(wv[w0 + 2 * c + 1], wv[w0 + 2 * c + 2], 0x5432);
+                        const uint32_t q0 = __byte_perm(wv[rr][w0 + 2 * c], wv[rr][w0 + 2 * c + 1], 0x5432);
+                        const uint32_t q1 = __byte_perm(wv[rr][w0 + 2 * c + 1], wv[rr][w0 + 2 * c + 2], 0x5432);
                         const uint2 lo = bytes_to_f16x4(q0), hi = bytes_to_f16x4(q1);
                         *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
                     }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint2 lo = bytes_to_f16x4(wv[w1 + 1 + 2 * c]);
-                        const uint2 hi = bytes_to_f16x4(wv[w1 + 2 + 2 * c]);
+                        const uint2 lo = bytes_to_f16x4(wv[rr][w1 + 1 + 2 * c]);
+                        const uint2 hi = bytes_to_f16x4(wv[rr][w1 + 2 + 2 * c]);
                         *reinterpret_cast<uint4 *>(arow + (((c + 4) ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
                     }
-                    wsc[r] = half_bits_to_float(wv[w0] & 0xffffu);
-                    wsc[BM + r] = half_bits_to_float(wv[w1] >> 16);
+                    wsc[r] = half_bits_to_float(wv[rr][w0] & 0xffffu);
+                    wsc[BM + r] = half_bits_to_float(wv[rr][w1] >> 16);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars.stage_full[aslot]);
-                mbar_arrive(&bars.sc_full[ss]);
-                if (part == CHUNKS_PER_GROUP - 1) mbar_arrive(&bars.raw_empty[rs]);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars.stage_full[aslot]);
+                    mbar_arrive(&bars.sc_full[ss]);
+                    if (part == CHUNKS_PER_GROUP - 1) mbar_arrive(&bars.raw_empty[rs]);
+                }
             }
             if (!ok) break;
         }
