@@ -14,6 +14,11 @@ it with gcc and exposes numpy-facing wrappers:
     block_dots(w, xq, k, rows=None)   O3  exact int32 D[t, r, b]
     matmul(w, xq, xd, k, rows=None)   O4  (y32, y64, S) with S = sum_b |d_w d_a D|
     dequant_f16(w, k)                 O5  Q8_0 -> fp16 bits [n, k]
+    repack_q8_0(w, k, ldn)            O6  Q8_0 -> exact binary16 quant plane + f32 scale plane
+    quantize_q4_0(w)                  O7a f32 [n,k] -> Q4_0 bytes [n, k/32*18] (data preparation)
+    dequant_q4_0_f16(w, k)            O7b Q4_0 -> fp16 bits [n, k]
+    block_dots_q4_0(w, xq, k, rows)   O7c exact int32 D[t, r, b] of Q4_0 weights
+    matmul_q4_0(w, xq, xd, k, rows)   O7d (y32, y64, S) over Q4_0 weights
 
 Each C function cites the page passage it follows (memra-engine docs.rs pages:
 accprobe_bench.rs, decode_kernel_census.rs, f16_ffi.rs).
@@ -36,6 +41,7 @@ _LIB = None
 
 QK = 32
 Q8_0_BYTES = 34
+Q4_0_BYTES = 18
 
 
 def build(force: bool = False) -> str:
@@ -63,9 +69,15 @@ def _bind(lib):
     lib.oracle_matmul.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P, P]
     lib.oracle_dequant_f16.argtypes = [P, P, I64, I64]
     lib.oracle_repack_q8_0.argtypes = [P, P, P, I64, I64, I64]
+    lib.oracle_quantize_q4_0.argtypes = [P, P, I64, I64]
+    lib.oracle_dequant_q4_0_f16.argtypes = [P, P, I64, I64]
+    lib.oracle_block_dots_q4_0.argtypes = [P, P, P, I64, I64, I64, P, I64]
+    lib.oracle_matmul_q4_0.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P, P]
     for name in ("oracle_f32_to_f16_array", "oracle_f16_to_f32_array",
                  "oracle_quantize_q8_1", "oracle_quantize_q8_0", "oracle_block_dots",
-                 "oracle_matmul", "oracle_dequant_f16", "oracle_repack_q8_0"):
+                 "oracle_matmul", "oracle_dequant_f16", "oracle_repack_q8_0",
+                 "oracle_quantize_q4_0", "oracle_dequant_q4_0_f16", "oracle_block_dots_q4_0",
+                 "oracle_matmul_q4_0"):
         getattr(lib, name).restype = None
     return lib
 
@@ -208,10 +220,61 @@ def repack_q8_0(w: np.ndarray, k: int, ldn: int | None = None, _o: Oracle | None
     return wq16, wdt
 
 
+def quantize_q4_0(w: np.ndarray, _o: Oracle | None = None) -> np.ndarray:
+    """O7a: f32 weights [n, k] -> Q4_0 bytes uint8 [n, k/32*18] (data preparation)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    _check_k(k)
+    out = np.empty((n, k // QK * Q4_0_BYTES), dtype=np.uint8)
+    (_o or _DEFAULT).lib().oracle_quantize_q4_0(_ptr(w), _ptr(out), n, k)
+    return out
+
+
+def dequant_q4_0_f16(w: np.ndarray, k: int, _o: Oracle | None = None) -> np.ndarray:
+    """O7b: Q4_0 bytes -> fp16 bits uint16 [n, k]."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    n = w.size // (k // QK * Q4_0_BYTES)
+    out = np.empty((n, k), dtype=np.uint16)
+    (_o or _DEFAULT).lib().oracle_dequant_q4_0_f16(_ptr(w), _ptr(out), n, k)
+    return out
+
+
+def block_dots_q4_0(w: np.ndarray, xq: np.ndarray, k: int, rows=None, _o: Oracle | None = None) -> np.ndarray:
+    """O7c: exact int32 block dots D[t, j, b] of Q4_0 weight rows ``rows`` (default: all)."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    n = w.size // (k // QK * Q4_0_BYTES)
+    m = xq.size // k
+    rows, nr = _rows_arg(rows, n)
+    D = np.empty((m, nr, k // QK), dtype=np.int32)
+    (_o or _DEFAULT).lib().oracle_block_dots_q4_0(_ptr(w), _ptr(xq), _ptr(D), m, n, k, _ptr(rows), nr)
+    return D
+
+
+def matmul_q4_0(w: np.ndarray, xq: np.ndarray, xd: np.ndarray, k: int, rows=None, _o: Oracle | None = None):
+    """O7d: returns (y32 f32 [m, nr], y64 f64 [m, nr], S f64 [m, nr]) over Q4_0 weights."""
+    _check_k(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xd = np.ascontiguousarray(xd, dtype=np.float32)
+    n = w.size // (k // QK * Q4_0_BYTES)
+    m = xq.size // k
+    rows, nr = _rows_arg(rows, n)
+    y32 = np.empty((m, nr), dtype=np.float32)
+    y64 = np.empty((m, nr), dtype=np.float64)
+    S = np.empty((m, nr), dtype=np.float64)
+    (_o or _DEFAULT).lib().oracle_matmul_q4_0(_ptr(w), _ptr(xq), _ptr(xd), m, n, k, _ptr(rows), nr,
+                              _ptr(y32), _ptr(y64), _ptr(S))
+    return y32, y64, S
+
+
 _DEFAULT = Oracle()
 
 _PUBLIC = ("f32_to_f16", "f16_to_f32", "quantize_q8_0", "quantize_q8_1", "block_dots",
-           "matmul", "dequant_f16", "repack_q8_0")
+           "matmul", "dequant_f16", "repack_q8_0", "quantize_q4_0", "dequant_q4_0_f16",
+           "block_dots_q4_0", "matmul_q4_0")
 
 
 def bound(o: Oracle):

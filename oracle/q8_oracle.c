@@ -281,3 +281,132 @@ void oracle_repack_q8_0(const uint8_t *w, uint16_t *wq16, float *wdt, int64_t n,
             wdt[b * ldn + r] = block_scale(blk);
         }
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* O7: Q4_0 weights, [f16_ffi] memra_q4_0_dequant_f16 ("GGUF Q4_0 18B blocks -> row-major */
+/* fp16 mirror").  The page names the GGUF format and its 18-byte block; the layout read  */
+/* here is that format's: an fp16 scale d (little endian) at +0, then 16 bytes, element i */
+/* (i < 16) in the low nibble of byte 2 + i and element i + 16 in its high nibble, value  */
+/* d * (nibble - 8).                                                                      */
+/* ------------------------------------------------------------------------------------ */
+#define Q4_0_BYTES 18
+
+static int q4_0_value(const uint8_t *blk, int i)
+{
+    uint8_t byte = blk[2 + (i & 15)];
+    int nib = (i < 16) ? (byte & 0x0f) : (byte >> 4);
+    return nib - 8;
+}
+
+static const uint8_t *q4_0_block_ptr(const uint8_t *w, int64_t r, int64_t b, int64_t nb)
+{
+    return w + (r * nb + b) * Q4_0_BYTES;
+}
+
+/* O7a: Q4_0 writer (data preparation; the pages give no quantizer for it): per block
+   amax = max |v|, d = amax / 7 (f32), q = clamp(round_half_away(v / d), -8, 7), stored as
+   the nibble q + 8 with fp16(d); a block whose d is 0 stores d = 0 and nibbles 8. */
+void oracle_quantize_q4_0(const float *w, uint8_t *out, int64_t n, int64_t k)
+{
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            const float *v = w + r * k + b * QK;
+            uint8_t *blk = out + (r * nb + b) * Q4_0_BYTES;
+            float amax = 0.0f;
+            for (int i = 0; i < QK; i++) {
+                float a = fabsf(v[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            float d = amax / 7.0f;
+            int nib[QK];
+            for (int i = 0; i < QK; i++) {
+                float q = 0.0f;
+                if (d != 0.0f) {
+                    q = roundf(v[i] / d);
+                    if (q != q)
+                        q = 0.0f;
+                    if (q > 7.0f)
+                        q = 7.0f;
+                    if (q < -8.0f)
+                        q = -8.0f;
+                }
+                nib[i] = (int)q + 8;
+            }
+            uint16_t h = oracle_f32_to_f16(d);
+            blk[0] = (uint8_t)(h & 0xff);
+            blk[1] = (uint8_t)(h >> 8);
+            for (int i = 0; i < 16; i++)
+                blk[2 + i] = (uint8_t)(nib[i] | (nib[i + 16] << 4));
+        }
+}
+
+/* O7b: Q4_0 -> fp16 row-major dequant: w16[r][32b+i] = fp16_rn(f32(d) * (nibble - 8)).
+   The f32 product of an 11-bit significand and an integer in [-8, 7] is exact. */
+void oracle_dequant_q4_0_f16(const uint8_t *w, uint16_t *out, int64_t n, int64_t k)
+{
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = q4_0_block_ptr(w, r, b, nb);
+            float dw = block_scale(blk);
+            for (int i = 0; i < QK; i++)
+                out[r * k + b * QK + i] = oracle_f32_to_f16(dw * (float)q4_0_value(blk, i));
+        }
+}
+
+static int32_t q4_0_block_dot(const uint8_t *blk, const int8_t *xq)
+{
+    int32_t s = 0;
+    for (int i = 0; i < QK; i++)
+        s += (int32_t)q4_0_value(blk, i) * (int32_t)xq[i];
+    return s;
+}
+
+/* O7c: exact block dots of Q4_0 weights with q8_1 quants, as O3. */
+void oracle_block_dots_q4_0(const uint8_t *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n,
+                            int64_t k, const int64_t *rows, int64_t nrows)
+{
+    int64_t nb = k / QK;
+    int64_t nr = rows ? nrows : n;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t j = 0; j < nr; j++) {
+            int64_t r = rows ? rows[j] : j;
+            for (int64_t b = 0; b < nb; b++)
+                D[(t * nr + j) * nb + b] = q4_0_block_dot(q4_0_block_ptr(w, r, b, nb), xq + t * k + b * QK);
+        }
+}
+
+/* O7d: the fold of O4 over Q4_0 blocks (y32 in f32, ascending b; y64 and S in double). */
+void oracle_matmul_q4_0(const uint8_t *w, const int8_t *xq, const float *xd, int64_t m, int64_t n,
+                        int64_t k, const int64_t *rows, int64_t nrows, float *y32, double *y64,
+                        double *S)
+{
+    int64_t nb = k / QK;
+    int64_t nr = rows ? nrows : n;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t j = 0; j < nr; j++) {
+            int64_t r = rows ? rows[j] : j;
+            float acc32 = 0.0f;
+            double acc64 = 0.0, abs64 = 0.0;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *blk = q4_0_block_ptr(w, r, b, nb);
+                int32_t dot = q4_0_block_dot(blk, xq + t * k + b * QK);
+                float dw = block_scale(blk);
+                float da = xd[t * nb + b];
+                float s = dw * da;
+                float term = s * (float)dot;
+                acc32 = acc32 + term;
+                double term64 = (double)dw * (double)da * (double)dot;
+                acc64 += term64;
+                abs64 += fabs(term64);
+            }
+            if (y32)
+                y32[t * nr + j] = acc32;
+            if (y64)
+                y64[t * nr + j] = acc64;
+            if (S)
+                S[t * nr + j] = abs64;
+        }
+}

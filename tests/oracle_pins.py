@@ -291,6 +291,102 @@ def pin_nonfinite_inputs(o):
     assert np.isinf(d[0, 0]) and not q.any()
 
 
+# ---------------------------------------------------------------------------------------
+# O7: Q4_0 (the GGUF 18-byte block named by f16_ffi.rs memra_q4_0_dequant_f16)
+# ---------------------------------------------------------------------------------------
+def parse_q4_0(wb: np.ndarray, n: int, k: int):
+    """Decode Q4_0 bytes with numpy alone: (d float64 [n, k/32], signed values int64
+    [n, k/32, 32]) -- element i < 16 from the low nibble of quant byte i, element i + 16
+    from its high nibble, minus 8."""
+    nb = k // QK
+    blocks = np.ascontiguousarray(wb).reshape(n, nb, 18)
+    d = np.ascontiguousarray(blocks[:, :, 0:2]).view("<f2").reshape(n, nb).astype(np.float64)
+    qs = blocks[:, :, 2:].astype(np.int64)
+    q = np.concatenate([qs & 0x0F, qs >> 4], axis=2) - 8
+    return d, q
+
+
+def pin_q4_0_layout_golden(o):
+    g = _golden("q4_0_block_layout.json")
+    for blk in g["blocks"]:
+        raw = np.frombuffer(bytes.fromhex(blk["bytes"].replace(" ", "")), dtype=np.uint8)
+        assert raw.size == 18
+        h = o.dequant_q4_0_f16(raw.reshape(1, 18), QK)[0]
+        d = float(raw[:2].view("<f2")[0])
+        for i, v in blk["values"].items():
+            # a one-hot activation picks element i's signed value out of the block dot
+            onehot = np.zeros((1, QK), np.int8)
+            onehot[0, int(i)] = 1
+            D = int(o.block_dots_q4_0(raw.reshape(1, 18), onehot, QK)[0, 0, 0])
+            assert d * D == v, (i, d * D, v)
+        for i, bits in blk["f16"].items():
+            assert int(h[int(i)]) == int(bits, 16), (i, hex(h[int(i)]), bits)
+        xq = np.zeros((1, QK), np.int8)
+        for i, x in blk["xq"].items():
+            xq[0, int(i)] = x
+        assert o.block_dots_q4_0(raw.reshape(1, 18), xq, QK)[0, 0, 0] == blk["dot"]
+
+
+def pin_q4_0_dequant_vs_numpy(o, seed=10):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n, k = 9, 768
+    w = _rand_blocks(rng, n, k, lo=-12, hi=8)
+    wb = o.quantize_q4_0(w)
+    d, q = parse_q4_0(wb, n, k)
+    prod = (d.astype(np.float32)[:, :, None] * q.astype(np.float32)).reshape(n, k)
+    with np.errstate(over="ignore"):
+        ref = prod.astype(np.float16).view(np.uint16)
+    assert np.array_equal(o.dequant_q4_0_f16(wb, k), ref)
+
+
+def pin_q4_0_writer_invariants(o, seed=11):
+    """The Q4_0 writer (data preparation): nibbles stay in 1..15 (values -7..7), a block's
+    largest magnitude maps to +-7, a zero block stores d = 0 and nibbles 8, negating the
+    input negates the values, and every value is within half a step of the input."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n, k = 7, 512
+    w = _rand_blocks(rng, n, k, lo=-10, hi=10)
+    wb = o.quantize_q4_0(w)
+    d, q = parse_q4_0(wb, n, k)
+    assert q.min() >= -7 and q.max() <= 7
+    wblk = w.reshape(n, k // QK, QK).astype(np.float64)
+    amax = np.abs(wblk).max(axis=2)
+    nz = amax > 0
+    assert (np.abs(q).max(axis=2)[nz] == 7).all()
+    assert (d[~nz] == 0).all() and (q[~nz] == 0).all()
+    d32 = (amax / 7.0).astype(np.float32).astype(np.float64)   # the f32 divisor
+    err = np.abs(wblk - d32[:, :, None] * q)
+    assert (err <= 0.5 * d32[:, :, None] * (1 + 1e-6) + 1e-30).all()
+    wb_neg = o.quantize_q4_0(-w)
+    d2, q2 = parse_q4_0(wb_neg, n, k)
+    assert np.array_equal(d2, d) and np.array_equal(q2, -q)
+
+
+def pin_q4_0_dots_and_fold_bruteforce(o, seed=12):
+    """Block dots equal numpy int64 dots of the decoded values; the fold (y64) equals the
+    plain float64 dot of the dequantized operands; y32 is within the f32 summation bound."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for m, n, k in [(1, 5, 32), (3, 8, 256), (2, 4, 1024)]:
+        w = _rand_blocks(rng, n, k, lo=-6, hi=6)
+        x = rng.standard_normal((m, k)).astype(np.float32)
+        wb = o.quantize_q4_0(w)
+        xq, xd = o.quantize_q8_1(x)
+        d, q = parse_q4_0(wb, n, k)
+        nb = k // QK
+        D = o.block_dots_q4_0(wb, xq, k)
+        ref = np.einsum("rbi,tbi->trb", q, xq.astype(np.int64).reshape(m, nb, QK))
+        assert np.array_equal(D.astype(np.int64), ref)
+        y32, y64, S = o.matmul_q4_0(wb, xq, xd, k)
+        wv = (d[:, :, None] * q).reshape(n, k)
+        xv = (xd.astype(np.float64)[:, :, None] * xq.astype(np.float64).reshape(m, nb, QK)).reshape(m, k)
+        plain = xv @ wv.T
+        assert np.all(np.abs(y64 - plain) <= 1e-12 * np.maximum(S, 1e-300))
+        assert np.all(np.abs(y32.astype(np.float64) - y64) <= (nb + 2) * 2.0 ** -23 * S + 1e-30)
+        rows = np.array([n - 1, 0], dtype=np.int64)
+        sy32, sy64, _ = o.matmul_q4_0(wb, xq, xd, k, rows=rows)
+        assert np.array_equal(sy32, y32[:, rows]) and np.array_equal(sy64, y64[:, rows])
+
+
 ALL_PINS = [
     pin_f16_decode_exhaustive,
     pin_f16_encode_vs_numpy,
@@ -304,4 +400,8 @@ ALL_PINS = [
     pin_dequant_vs_numpy,
     pin_repack,
     pin_nonfinite_inputs,
+    pin_q4_0_layout_golden,
+    pin_q4_0_dequant_vs_numpy,
+    pin_q4_0_writer_invariants,
+    pin_q4_0_dots_and_fold_bruteforce,
 ]

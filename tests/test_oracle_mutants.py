@@ -32,6 +32,16 @@ MUTANTS = {
     "repack_scales_row_major": ("wdt[b * ldn + r] = block_scale(blk);", "wdt[r * nb + b] = block_scale(blk);"),
     "repack_offset_binary": ("wq16[r * k + b * QK + i] = oracle_f32_to_f16((float)wq[i]);",
                              "wq16[r * k + b * QK + i] = oracle_f32_to_f16((float)(wq[i] + 128));"),
+    "q4_nibble_halves_swapped": ("int nib = (i < 16) ? (byte & 0x0f) : (byte >> 4);",
+                                 "int nib = (i < 16) ? (byte >> 4) : (byte & 0x0f);"),
+    "q4_consecutive_pairs": ("uint8_t byte = blk[2 + (i & 15)];\n    int nib = (i < 16) ? (byte & 0x0f) : (byte >> 4);",
+                             "uint8_t byte = blk[2 + (i >> 1)];\n    int nib = (i & 1) ? (byte >> 4) : (byte & 0x0f);"),
+    "q4_bias_7": ("return nib - 8;", "return nib - 7;"),
+    "q4_writer_divisor_8": ("float d = amax / 7.0f;", "float d = amax / 8.0f;"),
+    "q4_dropped_last_block": ("for (int64_t b = 0; b < nb; b++) {\n                const uint8_t *blk = q4_0_block_ptr(w, r, b, nb);\n                int32_t dot",
+                              "for (int64_t b = 0; b < nb - 1; b++) {\n                const uint8_t *blk = q4_0_block_ptr(w, r, b, nb);\n                int32_t dot"),
+    "q4_dequant_unrounded_scale": ("out[r * k + b * QK + i] = oracle_f32_to_f16(dw * (float)q4_0_value(blk, i));",
+                                   "out[r * k + b * QK + i] = oracle_f32_to_f16(dw * 1.0001f * (float)q4_0_value(blk, i));"),
 }
 
 
