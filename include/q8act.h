@@ -246,6 +246,32 @@ int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt,
                                          int64_t k, void *stream);
 
 /*
+ * Q4_0 weights -- the GGUF Q4_0 block named by memra-engine 0.81.0 f16_ffi.rs
+ * (memra_q4_0_dequant_f16: "GGUF Q4_0 18B blocks -> row-major fp16 mirror").  A row of k
+ * weights is k/32 blocks of 18 bytes: the binary16 scale d (little endian), then 16 bytes
+ * holding element i (i < 16) in the low nibble of byte i and element i + 16 in its high
+ * nibble, each as q + 8; the weight is d * q with q in -8..7.  k: a positive multiple of 256
+ * (rows are then 16-byte multiples); pointers 16-byte aligned; errors as for the Q8_0 calls.
+ *
+ * q8act_quantize_q4_0: data preparation (the pages give no Q4_0 quantizer): per block
+ *   d = amax / 7 (f32), q = clamp(round_half_away(v / d), -8, 7), fp16(d) stored; a block
+ *   whose d is 0 stores d = 0 and q = 0.  w [n][k] f32 -> wq, n * k / 32 * 18 bytes.
+ * q8act_dequant_q4_0_f16: w16[r][32b+i] = fp16_rn(f32(d) * q) (the exact product, rounded
+ *   once), row-major [n][k]; the f16_ffi.rs memra_q4_0_dequant_f16 call.
+ * q8act_gemv_q4_0: y[t][r] = sum_b d_w * d_a * D with D the exact int32 dot of block b's
+ *   4-bit values with the q8_1 quants, folded in f32 exactly as q8act_gemv_q8_0 folds
+ *   (ascending blocks within each 256-wide group, then the fixed group order), so token t's
+ *   result is bitwise the same for every m.  Arguments as q8act_gemv_q8_0; 1 <= m <= 15.
+ * q8act_debug_gemv_q4_0_block_dots: that GEMV's exact block dots D[t][r][b] (test hook).
+ */
+int q8act_quantize_q4_0(const float *w, void *wq, int64_t n, int64_t k, void *stream);
+int q8act_dequant_q4_0_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
+int q8act_gemv_q4_0(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m,
+                    int64_t n, int64_t k, void *stream);
+int q8act_debug_gemv_q4_0_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m,
+                                     int64_t n, int64_t k, void *stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device-side status word that kernels set
  * when a pipeline wait times out.  Returns Q8ACT_OK, Q8ACT_ERR_TIMEOUT, or a CUDA error code.
  */

@@ -21,10 +21,12 @@ from ._lib import (  # noqa: F401  (re-exported ABI)
     q8act_gemm_q8_0_noalloc, q8act_gemm_workspace_bytes, q8act_gemv_q8_0, q8act_mmq_ldm, q8act_quantize_q8_0,
     q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror,
     q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots,
-    q8act_gemv_q8_0_group, Q8ACT_GEMV_MAX_GROUP)
+    q8act_gemv_q8_0_group, Q8ACT_GEMV_MAX_GROUP, q8act_quantize_q4_0, q8act_dequant_q4_0_f16,
+    q8act_gemv_q4_0, q8act_debug_gemv_q4_0_block_dots)
 
 QK = 32
 Q8_0_BYTES = 34
+Q4_0_BYTES = 18
 
 
 def row_bytes(k: int) -> int:
@@ -141,3 +143,34 @@ def dequant_q8_0_f16(w, n: int, k: int, out=None):
 def device_status(stream=None) -> None:
     """Synchronize and raise if a kernel recorded a pipeline timeout since the last check."""
     check(q8act_device_status(stream), "q8act_device_status")
+
+
+def row_bytes_q4_0(k: int) -> int:
+    """Bytes of one Q4_0 row of k values (k/32 blocks of 18 bytes)."""
+    return k // QK * Q4_0_BYTES
+
+
+def quantize_q4_0(w):
+    """f32 [n, k] CUDA tensor -> Q4_0 bytes, uint8 [n, k/32*18] (data preparation)."""
+    import torch
+    n, k = w.shape
+    out = torch.empty((n, row_bytes_q4_0(k)), dtype=torch.uint8, device=w.device)
+    check(q8act_quantize_q4_0(w, out, n, k), "q8act_quantize_q4_0")
+    return out
+
+
+def dequant_q4_0_f16(w, n: int, k: int, out=None):
+    """Q4_0 bytes -> row-major float16 [n, k]."""
+    import torch
+    w16 = out if out is not None else torch.empty((n, k), dtype=torch.float16, device=w.device)
+    check(q8act_dequant_q4_0_f16(w, w16, n, k), "q8act_dequant_q4_0_f16")
+    return w16
+
+
+def gemv_q4_0(w, xq, xd, n: int, out=None):
+    """Q4_0 weights x pre-quantized q8_1 activation: y f32 [m, n] (1 <= m <= 15)."""
+    import torch
+    m, k = xq.shape
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    check(q8act_gemv_q4_0(w, xq, xd, y, m, n, k), "q8act_gemv_q4_0")
+    return y

@@ -37,6 +37,7 @@ EXPORTED = (
     "q8act_debug_gemv_block_dots", "q8act_debug_gemm_block_dots", "q8act_device_status",
     "q8act_gemm_q8_0_noalloc", "q8act_repack_q8_0", "q8act_repack_ldn",
     "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots", "q8act_gemv_q8_0_group",
+    "q8act_quantize_q4_0", "q8act_dequant_q4_0_f16", "q8act_gemv_q4_0", "q8act_debug_gemv_q4_0_block_dots",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 Q8ACT_GEMM_SPLIT_BYTES = 160 * 65536 + 160 * 4
@@ -85,6 +86,10 @@ def lib() -> ctypes.CDLL:
                 "q8act_gemm_q8_0_repacked": ([P, P, P, P, I64, I64, I64, P, SZ, P], I32),
                 "q8act_debug_gemm_repacked_block_dots": ([P, P, P, P, I64, I64, I64, P], I32),
                 "q8act_gemv_q8_0_group": ([P, P, P, I32, P, P, I64, I64, P], I32),
+                "q8act_quantize_q4_0": ([P, P, I64, I64, P], I32),
+                "q8act_dequant_q4_0_f16": ([P, P, I64, I64, P], I32),
+                "q8act_gemv_q4_0": ([P, P, P, P, I64, I64, I64, P], I32),
+                "q8act_debug_gemv_q4_0_block_dots": ([P, P, P, I64, I64, I64, P], I32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -211,3 +216,19 @@ def q8act_gemv_q8_0_group(w, y, n, xq, xd, m, k, stream=None) -> int:
     ya = Parr(*[_p(v) for v in y])
     na = Narr(*[int(v) for v in n])
     return lib().q8act_gemv_q8_0_group(wa, ya, na, count, _p(xq), _p(xd), m, k, _s(stream))
+
+
+def q8act_quantize_q4_0(w, wq, n, k, stream=None) -> int:
+    return lib().q8act_quantize_q4_0(_p(w), _p(wq), n, k, _s(stream))
+
+
+def q8act_dequant_q4_0_f16(w, w16, n, k, stream=None) -> int:
+    return lib().q8act_dequant_q4_0_f16(_p(w), _p(w16), n, k, _s(stream))
+
+
+def q8act_gemv_q4_0(w, xq, xd, y, m, n, k, stream=None) -> int:
+    return lib().q8act_gemv_q4_0(_p(w), _p(xq), _p(xd), _p(y), m, n, k, _s(stream))
+
+
+def q8act_debug_gemv_q4_0_block_dots(w, xq, D, m, n, k, stream=None) -> int:
+    return lib().q8act_debug_gemv_q4_0_block_dots(_p(w), _p(xq), _p(D), m, n, k, _s(stream))

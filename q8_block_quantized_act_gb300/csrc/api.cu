@@ -214,6 +214,63 @@ int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int
     return gemv_common(w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
 }
 
+// ---- Q4_0 (GGUF 18-byte blocks) ----
+
+int q8act_quantize_q4_0(const float *w, void *wq, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !wq) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || n < 1 || n * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(wq)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_quantize_q4_0(*dev, w, static_cast<uint8_t *>(wq), n, k, (cudaStream_t)stream));
+}
+
+int q8act_dequant_q4_0_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !w16) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || n < 1 || n * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(w16)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_dequant_q4_0_f16(*dev, static_cast<const uint8_t *>(w), static_cast<uint16_t *>(w16), n, k,
+                                               (cudaStream_t)stream));
+}
+
+static int gemv_q4_0_common(const void *w, const int8_t *xq, const float *xd, float *y, int32_t *dots, int64_t m,
+                            int64_t n, int64_t k, void *stream)
+{
+    if (!w || !xq || !xd || (!y && !dots)) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_MAX_M || n < 1 || n > INT32_MAX / 2 ||
+        n * k > ((int64_t)1 << 36))
+        return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(xq) || !aligned16(xd) || (y && !aligned16(y)) || (dots && !aligned16(dots)))
+        return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if (!q8::gemv_q4_0_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
+    return cuda_rc(q8::launch_gemv_q4_0(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
+                                        (cudaStream_t)stream));
+}
+
+int q8act_gemv_q4_0(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m, int64_t n, int64_t k,
+                    void *stream)
+{
+    if (!y) return Q8ACT_ERR_NULL;
+    return gemv_q4_0_common(w, xq, xd, y, nullptr, m, n, k, stream);
+}
+
+int q8act_debug_gemv_q4_0_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n, int64_t k,
+                                     void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    // As for Q8_0: the dot stage reads (and ignores) a scale array; the quants are readable.
+    return gemv_q4_0_common(w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
+}
+
 // Workspace of the fused GEMMs: [binary16 quants][block-major scales][split region].  The
 // first two are required; with the split region as well, a launch whose last wave would be
 // less than half full cuts those tiles into k pieces.

@@ -17,6 +17,8 @@ constexpr int QK = 32;            // values per block
 constexpr int Q8_0_BYTES = 34;    // binary16 scale + 32 int8 quants
 constexpr int GROUP_BLOCKS = 8;   // 8 blocks = 272 bytes = 17 x 16 B (lcm of 34 and 16)
 constexpr int GROUP_BYTES = GROUP_BLOCKS * Q8_0_BYTES;
+constexpr int Q4_0_BYTES = 18;    // binary16 scale + 16 bytes of 4-bit quants (GGUF Q4_0)
+constexpr int Q4_GROUP_BYTES = GROUP_BLOCKS * Q4_0_BYTES;   // 144 = 9 x 16 B
 constexpr int K_ALIGN = 256;      // k must be a multiple of this (row start 16 B aligned)
 
 // Device status word bits (read back by q8act_device_status).

@@ -1,17 +1,19 @@
-// dequant.cu -- Q8_0 -> row-major binary16 (memra-engine 0.81.0 f16_ffi.rs,
-// memra_q8_0_dequant_f16: w16[r][32b+i] = fp16(d_w * q)), and the load-time repack for the
-// tensor-core GEMM (the same stream; it stores the exact binary16 quants wq16[r][32b+i] = q
-// and the scale plane wdt[b][r] = f32(d_w) instead of their rounded product).
+// dequant.cu -- Q8_0 and Q4_0 -> row-major binary16 (memra-engine 0.81.0 f16_ffi.rs,
+// memra_q8_0_dequant_f16 and memra_q4_0_dequant_f16: w16[r][32b+i] = fp16(d_w * q)), and the
+// load-time repack of Q8_0 for the tensor-core GEMM (the same stream; it stores the exact
+// binary16 quants wq16[r][32b+i] = q and the scale plane wdt[b][r] = f32(d_w) instead of
+// their rounded product).
 //
-// HBM-bound: 34 bytes in and 64 bytes out per block.  Persistent CTAs stream chunks of
-// whole rows (contiguous, 16-byte aligned) into a shared-memory ring with cp.async.bulk.
-// A warp converts one 272-byte unit (8 blocks = 256 values) at a time: lane j builds the
-// 16-byte output piece j (8 values of block j/4) from shared memory and the warp stores the
-// unit's 512 output bytes with one fully coalesced 16-byte-per-lane store.
+// HBM-bound: 34 (Q8_0) or 18 (Q4_0) bytes in and 64 bytes out per block.  Persistent CTAs
+// stream chunks of whole rows (contiguous, 16-byte aligned) into a shared-memory ring with
+// cp.async.bulk.  A warp converts one unit of 8 blocks (256 values: 272 or 144 bytes, both
+// multiples of 16) at a time: lane j builds the 16-byte output piece j (8 values of block
+// j/4) from shared memory and the warp stores the unit's 512 output bytes with one fully
+// coalesced 16-byte-per-lane store.
 //
-// Arithmetic: the int8 quants become binary16 exactly (|q| <= 127), and the binary16
-// multiplier rounds the exact product d_w * q once, to nearest even -- the same value as
-// rounding the (exact) f32 product, which is how the format's dequant is defined.
+// Arithmetic: the quants become binary16 exactly (|q| <= 127), and the binary16 multiplier
+// rounds the exact product d_w * q once, to nearest even -- the same value as rounding the
+// (exact) f32 product, which is how the formats' dequant is defined.
 #include "common.cuh"
 #include "launch.h"
 
@@ -25,7 +27,7 @@ constexpr size_t TWO_PER_SM_SMEM = 113 * 1024;   // two CTAs per SM when 3 stage
 constexpr int TARGET_CHUNK = 17408;               // bytes of raw rows per stage (<= 64 units)
 
 struct Plan {
-    int G;               // units (272-byte groups) per row
+    int G;               // units (groups of 8 blocks) per row
     int R;               // rows per chunk
     int stages;
     uint32_t row_bytes;
@@ -34,11 +36,11 @@ struct Plan {
     size_t off_bar, smem;
 };
 
-Plan make_plan(int64_t n, int64_t k, size_t smem_cap)
+Plan make_plan(int64_t n, int64_t k, int block_bytes, size_t smem_cap)
 {
     Plan p{};
     p.G = (int)(k / 256);
-    p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
+    p.row_bytes = (uint32_t)(k / QK * block_bytes);
     p.R = (int)(TARGET_CHUNK / p.row_bytes);
     if (p.R < 1) p.R = 1;
     if ((int64_t)p.R > n) p.R = (int)n;
@@ -70,10 +72,65 @@ __device__ __forceinline__ void bytes_to_half2x2(uint32_t q4, __half2 &lo, __hal
     hi = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
 }
 
-template <bool REPACK>
+// Four 4-bit values (one per byte, 0..15) -> two half2 holding value - 8 exactly: the
+// binary16 pattern 0x6400 | v is 1024 + v, and subtracting 1032 leaves v - 8.
+__device__ __forceinline__ void nibbles_to_half2x2(uint32_t n4, __half2 &lo, __half2 &hi)
+{
+    const uint32_t a = __byte_perm(n4, 0x64646464u, 0x5140);
+    const uint32_t b = __byte_perm(n4, 0x64646464u, 0x5342);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6408));  // 1032
+    lo = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    hi = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+}
+
+// Block formats.  load(): the raw words of lane (jb, sub)'s piece -- values 8 sub .. 8 sub + 7
+// of block jb of a unit; convert(): those 8 values as exact binary16 integers.
+struct FmtQ8_0 {
+    static constexpr int BLOCK_BYTES = Q8_0_BYTES;
+    static constexpr int UNIT_BYTES = GROUP_BYTES;
+    __device__ static void load(const uint8_t *unit, int jb, int sub, uint32_t &dbits, uint32_t &w0, uint32_t &w1)
+    {
+        const uint8_t *blk = unit + jb * Q8_0_BYTES;
+        const uint8_t *qp = blk + 2 + 8 * sub;
+        dbits = lds_u16(blk);
+        w0 = lds_u16(qp) | (lds_u16(qp + 2) << 16);
+        w1 = lds_u16(qp + 4) | (lds_u16(qp + 6) << 16);
+    }
+    __device__ static void convert(uint32_t w0, uint32_t w1, int, __half2 (&h)[4])
+    {
+        bytes_to_half2x2(w0, h[0], h[1]);
+        bytes_to_half2x2(w1, h[2], h[3]);
+    }
+};
+
+// Q4_0 (the GGUF 18-byte block): element i < 16 in the low nibble of quant byte i, element
+// i + 16 in its high nibble, value d * (nibble - 8).  Pieces 0 and 1 are the low nibbles of
+// bytes 0-7 and 8-15, pieces 2 and 3 their high nibbles.
+struct FmtQ4_0 {
+    static constexpr int BLOCK_BYTES = Q4_0_BYTES;
+    static constexpr int UNIT_BYTES = Q4_GROUP_BYTES;
+    __device__ static void load(const uint8_t *unit, int jb, int sub, uint32_t &dbits, uint32_t &w0, uint32_t &w1)
+    {
+        const uint8_t *blk = unit + jb * Q4_0_BYTES;
+        const uint8_t *qp = blk + 2 + 8 * (sub & 1);
+        dbits = lds_u16(blk);
+        w0 = lds_u16(qp) | (lds_u16(qp + 2) << 16);
+        w1 = lds_u16(qp + 4) | (lds_u16(qp + 6) << 16);
+    }
+    __device__ static void convert(uint32_t w0, uint32_t w1, int sub, __half2 (&h)[4])
+    {
+        const int sh = (sub & 2) ? 4 : 0;
+        nibbles_to_half2x2((w0 >> sh) & 0x0F0F0F0Fu, h[0], h[1]);
+        nibbles_to_half2x2((w1 >> sh) & 0x0F0F0F0Fu, h[2], h[3]);
+    }
+};
+
+// REPACK (Q8_0 only): store the exact quants and the transposed f32 scale plane instead of
+// the rounded products.
+template <class F, bool REPACK>
 __global__ void __launch_bounds__(THREADS, 2)
-    dequant_q8_0_f16_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out,
-                            float *__restrict__ wdt, int64_t ldn, int n, int k, Plan p, int *status)
+    dequant_f16_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out,
+                       float *__restrict__ wdt, int64_t ldn, int n, int k, Plan p, int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
@@ -131,11 +188,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             for (int e = 0; e < UNR; ++e) {
                 const int u = u0 + e * CONV_WARPS;
                 const int uu = u < units ? u : u0;   // an in-range unit; its result is not stored
-                const uint8_t *blk = sbase + (size_t)uu * GROUP_BYTES + jb * Q8_0_BYTES;
-                const uint8_t *qp = blk + 2 + 8 * sub;
-                dbits[e] = lds_u16(blk);
-                q01[e] = lds_u16(qp) | (lds_u16(qp + 2) << 16);
-                q23[e] = lds_u16(qp + 4) | (lds_u16(qp + 6) << 16);
+                F::load(sbase + (size_t)uu * F::UNIT_BYTES, jb, sub, dbits[e], q01[e], q23[e]);
             }
 #pragma unroll
             for (int e = 0; e < UNR; ++e) {
@@ -143,8 +196,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                 if (u >= units) break;
                 const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits[e]));
                 __half2 h[4];
-                bytes_to_half2x2(q01[e], h[0], h[1]);
-                bytes_to_half2x2(q23[e], h[2], h[3]);
+                F::convert(q01[e], q23[e], sub, h);
                 uint4 o;
                 uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
@@ -164,19 +216,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
 }
 
-template <bool REPACK>
+template <class F, bool REPACK>
 cudaError_t launch_stream(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16, float *wdt,
                           int64_t ldn, int64_t n, int64_t k, cudaStream_t stream)
 {
-    Plan p = make_plan(n, k, TWO_PER_SM_SMEM < dev.max_smem_optin ? TWO_PER_SM_SMEM : dev.max_smem_optin);
+    Plan p = make_plan(n, k, F::BLOCK_BYTES,
+                       TWO_PER_SM_SMEM < dev.max_smem_optin ? TWO_PER_SM_SMEM : dev.max_smem_optin);
     int per_sm = 2;
     if (p.stages < 3) {
-        p = make_plan(n, k, dev.max_smem_optin);
+        p = make_plan(n, k, F::BLOCK_BYTES, dev.max_smem_optin);
         per_sm = 1;
     }
     if (p.stages < 2) return cudaErrorInvalidValue;
-    auto kern = dequant_q8_0_f16_kernel<REPACK>;
-    cudaError_t e = set_kernel_smem<dequant_q8_0_f16_kernel<REPACK>>(dev.device, p.smem);
+    auto kern = dequant_f16_kernel<F, REPACK>;
+    cudaError_t e = set_kernel_smem<dequant_f16_kernel<F, REPACK>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
@@ -190,13 +243,19 @@ cudaError_t launch_stream(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16
 cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
                                     int64_t n, int64_t k, cudaStream_t stream)
 {
-    return launch_stream<false>(dev, w, w16, nullptr, 0, n, k, stream);
+    return launch_stream<FmtQ8_0, false>(dev, w, w16, nullptr, 0, n, k, stream);
+}
+
+cudaError_t launch_dequant_q4_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
+                                    int64_t n, int64_t k, cudaStream_t stream)
+{
+    return launch_stream<FmtQ4_0, false>(dev, w, w16, nullptr, 0, n, k, stream);
 }
 
 cudaError_t launch_repack_q8_0(const DeviceInfo &dev, const uint8_t *w, uint16_t *wq16, float *wdt,
                                int64_t ldn, int64_t n, int64_t k, cudaStream_t stream)
 {
-    return launch_stream<true>(dev, w, wq16, wdt, ldn, n, k, stream);
+    return launch_stream<FmtQ8_0, true>(dev, w, wq16, wdt, ldn, n, k, stream);
 }
 
 }  // namespace q8

@@ -27,7 +27,66 @@ constexpr int THREADS = CONSUMERS + 32;
 constexpr int MAX_STAGES = 6;
 constexpr int XG_WORDS = 68;   // per (token, group): 64 quant words + 4 pad
 constexpr int XDG_WORDS = 12;  // per (token, group): 8 scales + 4 pad
-constexpr int UNIT_WORDS = GROUP_BYTES / 4;  // 68
+
+// Block formats.  A unit is 8 blocks (272 bytes of Q8_0, 144 of Q4_0: multiples of 16).
+// block(): the scale bits of block j of a unit and its 32 quants as signed bytes scaled by
+// 2^SHIFT, ready for dp4a with the activation (the exact dot is the dp4a sum >> SHIFT).
+struct GQ8_0 {
+    static constexpr int BLOCK_BYTES = Q8_0_BYTES;
+    static constexpr int UNIT_BYTES = GROUP_BYTES;
+    static constexpr int UNIT_WORDS = UNIT_BYTES / 4;   // 68
+    static constexpr int SHIFT = 0;
+    __device__ static void block(const uint32_t (&wv)[UNIT_WORDS], int j, uint32_t (&q)[8], uint32_t &dbits)
+    {
+        // Block j starts at byte 34j: even j at word 17(j/2) (scale in the low half, quants
+        // straddle words), odd j with its scale in the high half of word 17(j/2)+8 and
+        // word-aligned quants after it.
+        if ((j & 1) == 0) {
+            const int w0 = 17 * (j >> 1);
+            dbits = wv[w0] & 0xffffu;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = __byte_perm(wv[w0 + e], wv[w0 + e + 1], 0x5432);
+        } else {
+            const int w1 = 17 * (j >> 1) + 8;
+            dbits = wv[w1] >> 16;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = wv[w1 + 1 + e];
+        }
+    }
+};
+
+// Q4_0 (the GGUF 18-byte block): element i < 16 in the low nibble of quant byte i, element
+// i + 16 in its high nibble, value nibble - 8.  Moving a nibble n to the top of its byte and
+// flipping the sign bit gives the signed byte 16 (n - 8), so dp4a sums 16 D exactly.
+struct GQ4_0 {
+    static constexpr int BLOCK_BYTES = Q4_0_BYTES;
+    static constexpr int UNIT_BYTES = Q4_GROUP_BYTES;
+    static constexpr int UNIT_WORDS = UNIT_BYTES / 4;   // 36
+    static constexpr int SHIFT = 4;
+    __device__ static void block(const uint32_t (&wv)[UNIT_WORDS], int j, uint32_t (&q)[8], uint32_t &dbits)
+    {
+        // Block j starts at byte 18j: even j at word 9(j/2) (scale in the low half, the 16
+        // quant bytes straddle words), odd j with its scale in the high half of word
+        // 9(j/2)+4 and word-aligned quant bytes after it.
+        uint32_t b[4];
+        if ((j & 1) == 0) {
+            const int w0 = 9 * (j >> 1);
+            dbits = wv[w0] & 0xffffu;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) b[e] = __byte_perm(wv[w0 + e], wv[w0 + e + 1], 0x5432);
+        } else {
+            const int w1 = 9 * (j >> 1) + 4;
+            dbits = wv[w1] >> 16;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) b[e] = wv[w1 + 1 + e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            q[e] = ((b[e] << 4) & 0xF0F0F0F0u) ^ 0x80808080u;   // elements 4e .. 4e+3
+            q[4 + e] = (b[e] & 0xF0F0F0F0u) ^ 0x80808080u;      // elements 16+4e .. 16+4e+3
+        }
+    }
+};
 
 struct Plan {
     int G;              // groups of 8 blocks per row (k / 256)
@@ -42,7 +101,7 @@ struct Plan {
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap)
+Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap, int block_bytes)
 {
     Plan p{};
     p.G = (int)(k / 256);
@@ -50,7 +109,7 @@ Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap)
     if (p.R > r_cap) p.R = r_cap;
     if ((int64_t)p.R > n) p.R = (int)n;
     p.U = p.R * p.G;
-    p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
+    p.row_bytes = (uint32_t)(k / QK * block_bytes);
     p.chunk_bytes = (uint32_t)p.R * p.row_bytes;
     p.nchunks = (n + p.R - 1) / p.R;
     const size_t x_bytes = (size_t)m * p.G * XG_WORDS * 4;
@@ -74,17 +133,17 @@ Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap)
 // Two CTAs per SM when two rings of at least 3 stages fit, else one CTA with up to 6 stages.
 // When a large activation leaves room for fewer than 2 full-size stages, the chunk shrinks
 // (fewer rows per chunk) until two fit.
-Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
+Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin, int block_bytes)
 {
     const size_t half = 113 * 1024;
-    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin, CONSUMERS);
+    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin, CONSUMERS, block_bytes);
     if (p.stages >= 3) {
         p.ctas_per_sm = 2;
         return p;
     }
-    p = make_plan(m, n, k, smem_optin, CONSUMERS);
+    p = make_plan(m, n, k, smem_optin, CONSUMERS, block_bytes);
     for (int r_cap = p.R / 2; p.stages < 2 && r_cap >= 1; r_cap /= 2)
-        p = make_plan(m, n, k, smem_optin, r_cap);
+        p = make_plan(m, n, k, smem_optin, r_cap, block_bytes);
     return p;
 }
 
@@ -134,9 +193,9 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
     return r != 0;
 }
 
-template <int M, bool DOTS>
+template <class F, int M, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 2)
-    gemv_q8_0_kernel(const __grid_constant__ Group grp, const int8_t *__restrict__ xq,
+    gemv_kernel(const __grid_constant__ Group grp, const int8_t *__restrict__ xq,
                      const float *__restrict__ xd, int32_t *__restrict__ dots, int k, Plan p,
                      int *status)
 {
@@ -230,10 +289,10 @@ __global__ void __launch_bounds__(THREADS, 2)
             for (int t = 0; t < M; ++t) acc[t] = 0.0f;
             if (row < rows) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(sbase + (size_t)row * p.row_bytes +
-                                                                   g * GROUP_BYTES);
-                uint32_t wv[UNIT_WORDS];
+                                                                   g * F::UNIT_BYTES);
+                uint32_t wv[F::UNIT_WORDS];
 #pragma unroll
-                for (int c = 0; c < UNIT_WORDS / 4; ++c) {
+                for (int c = 0; c < F::UNIT_WORDS / 4; ++c) {
                     const uint4 v = src[c];
                     wv[4 * c + 0] = v.x;
                     wv[4 * c + 1] = v.y;
@@ -244,22 +303,9 @@ __global__ void __launch_bounds__(THREADS, 2)
                 const float *xdg = xds + g * XDG_WORDS;
 #pragma unroll
                 for (int j = 0; j < GROUP_BLOCKS; ++j) {
-                    // Block j of the unit starts at byte 34j: even j at word 17(j/2) (scale in
-                    // the low half, quants straddle words), odd j with its scale in the high
-                    // half of word 17(j/2)+8 and word-aligned quants after it.
                     uint32_t q[8];
                     uint32_t dbits;
-                    if ((j & 1) == 0) {
-                        const int w0 = 17 * (j >> 1);
-                        dbits = wv[w0] & 0xffffu;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) q[e] = __byte_perm(wv[w0 + e], wv[w0 + e + 1], 0x5432);
-                    } else {
-                        const int w1 = 17 * (j >> 1) + 8;
-                        dbits = wv[w1] >> 16;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) q[e] = wv[w1 + 1 + e];
-                    }
+                    F::block(wv, j, q, dbits);
                     const float dw = half_bits_to_float(dbits);
 #pragma unroll
                     for (int t = 0; t < M; ++t) {
@@ -273,6 +319,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                         D = dp4a(q[5], b.y, D);
                         D = dp4a(q[6], b.z, D);
                         D = dp4a(q[7], b.w, D);
+                        D >>= F::SHIFT;   // exact: the sum is a multiple of 2^SHIFT
                         if (DOTS) {
                             dots[((int64_t)t * n + row0 + row) * nb + g * GROUP_BLOCKS + j] = D;
                         } else {
@@ -314,19 +361,19 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
 }
 
-template <int M, bool DOTS>
+template <class F, int M, bool DOTS>
 cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const float *xd,
                      int32_t *dots, int64_t k, cudaStream_t stream)
 {
     int64_t nmax = 0;
     for (int i = 0; i < grp.count; ++i) nmax = grp.n[i] > nmax ? grp.n[i] : nmax;
-    Plan p = choose_plan(M, nmax, k, dev.max_smem_optin);
+    Plan p = choose_plan(M, nmax, k, dev.max_smem_optin, F::BLOCK_BYTES);
     if (p.stages < 2) return cudaErrorInvalidValue;
     grp.first_chunk[0] = 0;
     for (int i = 0; i < grp.count; ++i) grp.first_chunk[i + 1] = grp.first_chunk[i] + (grp.n[i] + p.R - 1) / p.R;
     p.nchunks = grp.first_chunk[grp.count];
-    auto kern = gemv_q8_0_kernel<M, DOTS>;
-    cudaError_t e = set_kernel_smem<gemv_q8_0_kernel<M, DOTS>>(dev.device, p.smem);
+    auto kern = gemv_kernel<F, M, DOTS>;
+    cudaError_t e = set_kernel_smem<gemv_kernel<F, M, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
@@ -334,26 +381,26 @@ cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const f
     return cudaGetLastError();
 }
 
-template <bool DOTS>
+template <class F, bool DOTS>
 cudaError_t dispatch(const DeviceInfo &dev, const Group &grp, const int8_t *xq, const float *xd,
                      int32_t *dots, int64_t m, int64_t k, cudaStream_t stream)
 {
     switch (m) {
-    case 1: return launch_m<1, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 2: return launch_m<2, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 3: return launch_m<3, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 4: return launch_m<4, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 5: return launch_m<5, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 6: return launch_m<6, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 7: return launch_m<7, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 8: return launch_m<8, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 9: return launch_m<9, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 10: return launch_m<10, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 11: return launch_m<11, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 12: return launch_m<12, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 13: return launch_m<13, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 14: return launch_m<14, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 15: return launch_m<15, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 1: return launch_m<F, 1, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 2: return launch_m<F, 2, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 3: return launch_m<F, 3, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 4: return launch_m<F, 4, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 5: return launch_m<F, 5, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 6: return launch_m<F, 6, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 7: return launch_m<F, 7, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 8: return launch_m<F, 8, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 9: return launch_m<F, 9, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 10: return launch_m<F, 10, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 11: return launch_m<F, 11, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 12: return launch_m<F, 12, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 13: return launch_m<F, 13, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 14: return launch_m<F, 14, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 15: return launch_m<F, 15, DOTS>(dev, grp, xq, xd, dots, k, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -363,7 +410,7 @@ cudaError_t dispatch(const DeviceInfo &dev, const Group &grp, const int8_t *xq, 
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 {
     if (m < 1 || m > Q8ACT_GEMV_MAX_M) return false;
-    return choose_plan(m, 1 << 20, k, dev.max_smem_optin).stages >= 2;
+    return choose_plan(m, 1 << 20, k, dev.max_smem_optin, Q8_0_BYTES).stages >= 2;
 }
 
 cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
@@ -375,8 +422,27 @@ cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8
     grp.w[0] = w;
     grp.y[0] = y;
     grp.n[0] = (int)n;
-    if (dots) return dispatch<true>(dev, grp, xq, xd, dots, m, k, stream);
-    return dispatch<false>(dev, grp, xq, xd, dots, m, k, stream);
+    if (dots) return dispatch<GQ8_0, true>(dev, grp, xq, xd, dots, m, k, stream);
+    return dispatch<GQ8_0, false>(dev, grp, xq, xd, dots, m, k, stream);
+}
+
+bool gemv_q4_0_supported(const DeviceInfo &dev, int64_t m, int64_t k)
+{
+    if (m < 1 || m > Q8ACT_GEMV_MAX_M) return false;
+    return choose_plan(m, 1 << 20, k, dev.max_smem_optin, Q4_0_BYTES).stages >= 2;
+}
+
+cudaError_t launch_gemv_q4_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
+                             const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream)
+{
+    Group grp{};
+    grp.count = 1;
+    grp.w[0] = w;
+    grp.y[0] = y;
+    grp.n[0] = (int)n;
+    if (dots) return dispatch<GQ4_0, true>(dev, grp, xq, xd, dots, m, k, stream);
+    return dispatch<GQ4_0, false>(dev, grp, xq, xd, dots, m, k, stream);
 }
 
 cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,
@@ -391,7 +457,7 @@ cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *
         grp.y[i] = y[i];
         grp.n[i] = (int)n[i];
     }
-    return dispatch<false>(dev, grp, xq, xd, nullptr, m, k, stream);
+    return dispatch<GQ8_0, false>(dev, grp, xq, xd, nullptr, m, k, stream);
 }
 
 }  // namespace q8

@@ -25,6 +25,15 @@ cudaError_t launch_dequant_q8_0_f16(const DeviceInfo &dev, const uint8_t *w, uin
                                     int64_t n, int64_t k, cudaStream_t stream);
 cudaError_t launch_repack_q8_0(const DeviceInfo &dev, const uint8_t *w, uint16_t *wq16, float *wdt,
                                int64_t ldn, int64_t n, int64_t k, cudaStream_t stream);
+// Q4_0 (GGUF 18-byte blocks): the writer (data preparation), the fp16 dequant, the GEMV.
+cudaError_t launch_quantize_q4_0(const DeviceInfo &dev, const float *w, uint8_t *wq, int64_t n,
+                                 int64_t k, cudaStream_t stream);
+cudaError_t launch_dequant_q4_0_f16(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16,
+                                    int64_t n, int64_t k, cudaStream_t stream);
+bool gemv_q4_0_supported(const DeviceInfo &dev, int64_t m, int64_t k);
+cudaError_t launch_gemv_q4_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
+                             const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream);
 
 // GEMV: returns cudaErrorInvalidValue when m*k is too large for the shared-memory plan.
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);

@@ -1,5 +1,5 @@
-// quantize.cu -- the per-32-block quantizers: q8_1 activations (int8 and MMQ layouts) and
-// Q8_0 weights.  All three are HBM-bound elementwise passes: one thread owns 4 consecutive
+// quantize.cu -- the per-32-block quantizers: q8_1 activations (int8 and MMQ layouts), and
+// Q8_0 and Q4_0 weights (data preparation).  All three are HBM-bound elementwise passes: one thread owns 4 consecutive
 // values (one 16-byte load), 8 consecutive lanes own one block and find its amax with three
 // shuffles.
 //
@@ -128,6 +128,49 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__rest
     }
 }
 
+// w [n][k] f32 -> Q4_0 blocks (18 B: binary16 scale of the f32 d = amax / 7, then 16 bytes,
+// element i < 16 in the low nibble of byte i and element i + 16 in its high nibble, each
+// stored as q + 8 with q = clamp(round(v / d), -8, 7)).  Data preparation for the Q4_0 path.
+// nchunks is a multiple of 64 and the stride of 32, so the loop and its shuffles are
+// warp-uniform; lanes 0-3 of a block's 8 write its bytes, merging lane j + 4's nibbles.
+__global__ void __launch_bounds__(256) quantize_q4_0_kernel(const float4 *__restrict__ w,
+                                                            uint8_t *__restrict__ out,
+                                                            int64_t nchunks)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
+        const float4 v = load_stream(w + i);
+        float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
+        const float d = __fdiv_rn(a, 7.0f);
+        const float vals[4] = {v.x, v.y, v.z, v.w};
+        uint32_t nib4 = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int q = 0;
+            if (d != 0.0f) {
+                float t = roundf(__fdiv_rn(vals[e], d));
+                if (t > 7.0f) t = 7.0f;
+                if (t < -8.0f) t = -8.0f;
+                q = __float2int_rz(t);   // NaN converts to 0
+            }
+            nib4 |= (uint32_t)(q + 8) << (8 * e);
+        }
+        const uint32_t hi = __shfl_down_sync(FULL, nib4, 4);
+        const int j = (int)(i & 7);
+        if (j < 4) {
+            uint8_t *blk = out + (i >> 3) * Q4_0_BYTES;
+            const uint32_t bytes = nib4 | (hi << 4);
+            uint16_t *q16 = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);   // 2-byte aligned
+            q16[0] = (uint16_t)(bytes & 0xffffu);
+            q16[1] = (uint16_t)(bytes >> 16);
+            if (j == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__float2half_rn(d));
+        }
+    }
+}
+
 // Every kernel of the library asks for the largest shared-memory carveout, so that moving
 // between these smem-free passes and the shared-memory-heavy GEMV/GEMM/dequant never forces
 // the SM to re-partition its L1/shared memory between launches.
@@ -179,6 +222,16 @@ cudaError_t launch_quantize_q8_0(const DeviceInfo &dev, const float *w, uint8_t 
     const int64_t nchunks = n * k / 4;
     set_max_carveout(quantize_q8_0_kernel);
     quantize_q8_0_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
+        reinterpret_cast<const float4 *>(w), wq, nchunks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q4_0(const DeviceInfo &dev, const float *w, uint8_t *wq, int64_t n,
+                                 int64_t k, cudaStream_t stream)
+{
+    const int64_t nchunks = n * k / 4;
+    set_max_carveout(quantize_q4_0_kernel);
+    quantize_q4_0_kernel<<<grid_for(dev, nchunks, 256), 256, 0, stream>>>(
         reinterpret_cast<const float4 *>(w), wq, nchunks);
     return cudaGetLastError();
 }

@@ -92,6 +92,17 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_gemv_q8_0_group([A, A], [A, A], [8, 0], A, A, 1, 256, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemv_q8_0_group([A, MIS], [A, A], [8, 8], A, A, 1, 256, S0), q8.Q8ACT_ERR_ALIGN),
     (lambda: q8.q8act_gemv_q8_0_group([A], [A], [8], A, A, q8.Q8ACT_GEMV_MAX_M + 1, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_quantize_q4_0(None, A, 4, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_quantize_q4_0(A, A, 4, 288, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_quantize_q4_0(A, MIS, 4, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_dequant_q4_0_f16(A, None, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_dequant_q4_0_f16(A, A, 0, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_dequant_q4_0_f16(MIS, A, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_gemv_q4_0(A, A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemv_q4_0(A, A, A, A, q8.Q8ACT_GEMV_MAX_M + 1, 8, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q4_0(A, A, A, A, 1, 8, 1280 + 32, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q4_0(A, A, MIS, A, 1, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_debug_gemv_q4_0_block_dots(A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
 ])
 def test_host_side_refusals(L, call, want):
     assert call() == want
