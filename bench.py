@@ -58,6 +58,19 @@ def gemv_bytes(m, n, k):
     return n * row_bytes(k) + m * k + m * (k // 32) * 4 + m * n * 4
 
 
+def row_bytes_q4_0(k):
+    return k // 32 * 18
+
+
+def gemv_q4_0_bytes(m, n, k):
+    """Algorithmic bytes of one Q4_0 GEMV: Q4_0 weights + int8 quants + f32 scales + output."""
+    return n * row_bytes_q4_0(k) + m * k + m * (k // 32) * 4 + m * n * 4
+
+
+def dequant_q4_0_bytes(n, k):
+    return n * row_bytes_q4_0(k) + 2 * n * k
+
+
 def gemm_flops(m, n, k):
     return 2.0 * m * n * k
 
@@ -165,13 +178,15 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- inputs: seeded host f32, quantized to Q8_0 on the device by the library ----
     def weights_q8(n, k):
+        """Q8_0 and Q4_0 encodings of the same seeded f32 weights."""
         w32 = torch.from_numpy(inputs.weights_f32(n, k)).to(dev)
         wq = q8.quantize_q8_0(w32)
+        w4 = q8.quantize_q4_0(w32)
         del w32
-        return wq
+        return wq, w4
 
-    w_gemv = weights_q8(GEMV["n"], GEMV["k"])
-    w_gemm = weights_q8(GEMM["n"], GEMM["k"])
+    w_gemv, w4_gemv = weights_q8(GEMV["n"], GEMV["k"])
+    w_gemm, w4_gemm = weights_q8(GEMM["n"], GEMM["k"])
     x_gemv = torch.from_numpy(inputs.activations_f32(GEMV["m"], GEMV["k"])).to(dev)
     x_gemm = torch.from_numpy(inputs.activations_f32(GEMM["m"], GEMM["k"])).to(dev)
     xq = torch.empty((GEMV["m"], GEMV["k"]), dtype=torch.int8, device=dev)
@@ -262,6 +277,38 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         step_ms, mean_ms = max_over_ranks(step_ms, mean_ms, [nm for nm, _ in parts], dev)
 
+    # ---- the next rows (Q4_0 GEMV and dequant): timed in a loop of their own, after the
+    # step, with the same warm-up and flush rules; they are not part of the step ----
+    y4 = torch.empty((GEMV["m"], GEMV["n"]), dtype=torch.float32, device=dev)
+
+    def k_gemv4():
+        q8.check(q8.q8act_gemv_q4_0(w4_gemv, xq, xd, y4, GEMV["m"], GEMV["n"], GEMV["k"], stream))
+
+    def k_deq4():
+        q8.check(q8.q8act_dequant_q4_0_f16(w4_gemm, w16, DEQ["n"], DEQ["k"], stream))
+
+    nxt = [("dequant_q4_0_f16", k_deq4, True), ("gemv_q4_0", k_gemv4, False)]
+    k_quant()
+    for _ in range(args.warmup):
+        for _, fn, fl in nxt:
+            if fl:
+                flush_l2()
+            fn()
+    nsteps = min(args.steps, 100)
+    ev4 = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in nxt]
+           for _ in range(nsteps)]
+    for s_ in range(nsteps):
+        for i, (_, fn, fl) in enumerate(nxt):
+            if fl:
+                flush_l2()
+            ev4[s_][i][0].record(stream)
+            fn()
+            ev4[s_][i][1].record(stream)
+    torch.cuda.synchronize()
+    q8.device_status(stream)
+    mean4 = {nm: float(np.mean([ev4[s_][i][0].elapsed_time(ev4[s_][i][1]) for s_ in range(nsteps)]))
+             for i, (nm, _, _) in enumerate(nxt)}
+
     # ---- end to end through the public API: host f32 in (pinned), host f32 out ----
     e2e = run_e2e(args, q8, torch, dev, stream)
 
@@ -284,6 +331,16 @@ def run_ours(args, rank, world, local_rank):
                                      "GB/s", mean_ms["dequant_q8_0_f16"], db)
     for nm in comps:
         comps[nm].update(spread[nm])
+    g4 = gemv_q4_0_bytes(**GEMV)
+    d4 = dequant_q4_0_bytes(**DEQ)
+    next_rows = {
+        "gemv_q4_0": roof("hbm", g4 / (mean4["gemv_q4_0"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                          mean4["gemv_q4_0"], g4),
+        "dequant_q4_0_f16": roof("hbm", d4 / (mean4["dequant_q4_0_f16"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                 mean4["dequant_q4_0_f16"], d4),
+        "steps": nsteps,
+        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096, same seeded weights; timed after the step in a loop of their own (dequant after an L2 flush)",
+    }
     dominant = max(mean_ms, key=lambda nm: mean_ms[nm])
     traffic = load_traffic(dominant)
     d = comps[dominant]
@@ -305,6 +362,7 @@ def run_ours(args, rank, world, local_rank):
         "gemm_tops": round(comps["gemm_q8_0"]["achieved"], 2),
         "gemm_repacked_tops": round(comps["gemm_q8_0_repacked"]["achieved"], 2),
         "components": comps,
+        "next_rows": next_rows,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

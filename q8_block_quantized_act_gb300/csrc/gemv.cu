@@ -1,15 +1,16 @@
 // gemv.cu -- Q8_0 x q8_1 GEMV for decode and speculative verify (m = 1..15): the "mmvq"
-// regime of memra-engine 0.113.0 decode_kernel_census.rs (fn q8 -> qmatvec_mmvq_into).
+// regime of memra-engine 0.113.0 decode_kernel_census.rs (fn q8 -> qmatvec_mmvq_into); and
+// the same kernel over Q4_0 weights (the GGUF 18-byte block of f16_ffi.rs).
 //
-// The weight stream (34 bytes per 32 weights) is read exactly once, so the kernel is bound
-// by HBM bandwidth.  Design (one persistent CTA per SM):
-//   * a producer warp streams "chunks" of R consecutive rows (R * row_bytes <= 34.8 KB,
-//     contiguous in memory) into a ring of shared-memory stages with cp.async.bulk,
-//     completing on mbarriers -- coalesced, 16-byte aligned, no per-thread address math;
-//   * 128 consumer threads split each chunk into "units" of 8 blocks (272 bytes = 17 x 16 B,
-//     the period at which 34-byte blocks realign to 16 bytes); a unit is read with 17
-//     conflict-free 16-byte shared loads, its 8 blocks are dotted with the activation
-//     (4 x dp4a per block per token) and folded as acc += (d_w * d_a) * D;
+// The weight stream (34 or 18 bytes per 32 weights) is read exactly once, so the kernel is
+// bound by HBM bandwidth.  Design (persistent CTAs, two per SM):
+//   * a producer warp streams "chunks" of R consecutive rows (contiguous in memory) into a
+//     ring of shared-memory stages with cp.async.bulk, completing on mbarriers -- coalesced,
+//     16-byte aligned, no per-thread address math;
+//   * 128 consumer threads split each chunk into "units" of 8 blocks (272 = 17 x 16 or 144 = 9 x 16 bytes,
+//     the period at which the blocks realign to 16 bytes); a unit is read with conflict-free
+//     16-byte shared loads, its 8 blocks are dotted with the activation (8 dp4a per block
+//     per token) and folded as acc += (d_w * d_a) * D;
 //   * the activation (m x k int8 + scales) sits in shared memory for the whole kernel, padded
 //     so that neighbouring units hit different banks;
 //   * the per-row sum over units uses a fixed order -- a butterfly of warp shuffles when a
@@ -22,8 +23,6 @@
 namespace q8 {
 namespace {
 
-constexpr int CONSUMERS = 128;
-constexpr int THREADS = CONSUMERS + 32;
 constexpr int MAX_STAGES = 6;
 constexpr int XG_WORDS = 68;   // per (token, group): 64 quant words + 4 pad
 constexpr int XDG_WORDS = 12;  // per (token, group): 8 scales + 4 pad
@@ -36,6 +35,8 @@ struct GQ8_0 {
     static constexpr int UNIT_BYTES = GROUP_BYTES;
     static constexpr int UNIT_WORDS = UNIT_BYTES / 4;   // 68
     static constexpr int SHIFT = 0;
+    static constexpr int CONSUMERS = 128;    // consumer threads per CTA
+    static constexpr int CHUNK_UNITS = 128;  // units per chunk: one per consumer
     __device__ static void block(const uint32_t (&wv)[UNIT_WORDS], int j, uint32_t (&q)[8], uint32_t &dbits)
     {
         // Block j starts at byte 34j: even j at word 17(j/2) (scale in the low half, quants
@@ -63,6 +64,8 @@ struct GQ4_0 {
     static constexpr int UNIT_BYTES = Q4_GROUP_BYTES;
     static constexpr int UNIT_WORDS = UNIT_BYTES / 4;   // 36
     static constexpr int SHIFT = 4;
+    static constexpr int CONSUMERS = 128;
+    static constexpr int CHUNK_UNITS = 128;
     __device__ static void block(const uint32_t (&wv)[UNIT_WORDS], int j, uint32_t (&q)[8], uint32_t &dbits)
     {
         // Block j starts at byte 18j: even j at word 9(j/2) (scale in the low half, the 16
@@ -101,11 +104,11 @@ struct Plan {
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap, int block_bytes)
+Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap, int block_bytes, int chunk_units)
 {
     Plan p{};
     p.G = (int)(k / 256);
-    p.R = p.G <= CONSUMERS ? CONSUMERS / p.G : 1;
+    p.R = p.G <= chunk_units ? chunk_units / p.G : 1;
     if (p.R > r_cap) p.R = r_cap;
     if ((int64_t)p.R > n) p.R = (int)n;
     p.U = p.R * p.G;
@@ -133,17 +136,18 @@ Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap, int 
 // Two CTAs per SM when two rings of at least 3 stages fit, else one CTA with up to 6 stages.
 // When a large activation leaves room for fewer than 2 full-size stages, the chunk shrinks
 // (fewer rows per chunk) until two fit.
-Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin, int block_bytes)
+template <class F>
+Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
 {
     const size_t half = 113 * 1024;
-    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin, CONSUMERS, block_bytes);
+    Plan p = make_plan(m, n, k, half < smem_optin ? half : smem_optin, F::CHUNK_UNITS, F::BLOCK_BYTES, F::CHUNK_UNITS);
     if (p.stages >= 3) {
         p.ctas_per_sm = 2;
         return p;
     }
-    p = make_plan(m, n, k, smem_optin, CONSUMERS, block_bytes);
+    p = make_plan(m, n, k, smem_optin, F::CHUNK_UNITS, F::BLOCK_BYTES, F::CHUNK_UNITS);
     for (int r_cap = p.R / 2; p.stages < 2 && r_cap >= 1; r_cap /= 2)
-        p = make_plan(m, n, k, smem_optin, r_cap, block_bytes);
+        p = make_plan(m, n, k, smem_optin, r_cap, F::BLOCK_BYTES, F::CHUNK_UNITS);
     return p;
 }
 
@@ -194,7 +198,7 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
 }
 
 template <class F, int M, bool DOTS>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
     gemv_kernel(const __grid_constant__ Group grp, const int8_t *__restrict__ xq,
                      const float *__restrict__ xd, int32_t *__restrict__ dots, int k, Plan p,
                      int *status)
@@ -206,6 +210,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + MAX_STAGES;
 
+    constexpr int CONSUMERS = F::CONSUMERS;
     const int tid = threadIdx.x;
     const int G = p.G;
     const int nb = k / QK;
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CONSUMERS);
+            mbar_init(&empty[s], CONSUMERS / 32);
         }
         fence_mbar_init();
     }
@@ -311,15 +316,16 @@ __global__ void __launch_bounds__(THREADS, 2)
                     for (int t = 0; t < M; ++t) {
                         const uint4 *xv = reinterpret_cast<const uint4 *>(xg + t * G * XG_WORDS + j * 8);
                         const uint4 a = xv[0], b = xv[1];
-                        int D = dp4a(q[0], a.x, 0);
-                        D = dp4a(q[1], a.y, D);
-                        D = dp4a(q[2], a.z, D);
-                        D = dp4a(q[3], a.w, D);
-                        D = dp4a(q[4], b.x, D);
-                        D = dp4a(q[5], b.y, D);
-                        D = dp4a(q[6], b.z, D);
-                        D = dp4a(q[7], b.w, D);
-                        D >>= F::SHIFT;   // exact: the sum is a multiple of 2^SHIFT
+                        // Two independent chains of 4 (integer sums: exact in any order).
+                        int D0 = dp4a(q[0], a.x, 0);
+                        int D1 = dp4a(q[4], b.x, 0);
+                        D0 = dp4a(q[1], a.y, D0);
+                        D1 = dp4a(q[5], b.y, D1);
+                        D0 = dp4a(q[2], a.z, D0);
+                        D1 = dp4a(q[6], b.z, D1);
+                        D0 = dp4a(q[3], a.w, D0);
+                        D1 = dp4a(q[7], b.w, D1);
+                        const int D = (D0 + D1) >> F::SHIFT;   // exact: a multiple of 2^SHIFT
                         if (DOTS) {
                             dots[((int64_t)t * n + row0 + row) * nb + g * GROUP_BLOCKS + j] = D;
                         } else {
@@ -348,7 +354,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                 for (int t = 0; t < M; ++t) pbuf[u * M + t] = acc[t];
             }
         }
-        mbar_arrive(&empty[s]);  // this stage's bytes are no longer needed
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage's bytes
         if (DOTS || p.warp_reduce) continue;
         named_bar_sync(1, CONSUMERS);
         for (int idx = tid; idx < rows * M; idx += CONSUMERS) {
@@ -367,7 +374,7 @@ cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const f
 {
     int64_t nmax = 0;
     for (int i = 0; i < grp.count; ++i) nmax = grp.n[i] > nmax ? grp.n[i] : nmax;
-    Plan p = choose_plan(M, nmax, k, dev.max_smem_optin, F::BLOCK_BYTES);
+    Plan p = choose_plan<F>(M, nmax, k, dev.max_smem_optin);
     if (p.stages < 2) return cudaErrorInvalidValue;
     grp.first_chunk[0] = 0;
     for (int i = 0; i < grp.count; ++i) grp.first_chunk[i + 1] = grp.first_chunk[i] + (grp.n[i] + p.R - 1) / p.R;
@@ -377,7 +384,7 @@ cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const f
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    kern<<<(int)grid, THREADS, p.smem, stream>>>(grp, xq, xd, dots, (int)k, p, dev.status);
+    kern<<<(int)grid, F::CONSUMERS + 32, p.smem, stream>>>(grp, xq, xd, dots, (int)k, p, dev.status);
     return cudaGetLastError();
 }
 
@@ -410,7 +417,7 @@ cudaError_t dispatch(const DeviceInfo &dev, const Group &grp, const int8_t *xq, 
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 {
     if (m < 1 || m > Q8ACT_GEMV_MAX_M) return false;
-    return choose_plan(m, 1 << 20, k, dev.max_smem_optin, Q8_0_BYTES).stages >= 2;
+    return choose_plan<GQ8_0>(m, 1 << 20, k, dev.max_smem_optin).stages >= 2;
 }
 
 cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
@@ -429,7 +436,7 @@ cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8
 bool gemv_q4_0_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 {
     if (m < 1 || m > Q8ACT_GEMV_MAX_M) return false;
-    return choose_plan(m, 1 << 20, k, dev.max_smem_optin, Q4_0_BYTES).stages >= 2;
+    return choose_plan<GQ4_0>(m, 1 << 20, k, dev.max_smem_optin).stages >= 2;
 }
 
 cudaError_t launch_gemv_q4_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,

@@ -16,7 +16,8 @@ import argparse
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", choices=("quantize", "quantize_mmq", "quantize_q8_0", "gemv", "gemm",
-                                       "gemm_preq", "gemm_repacked", "repack", "dequant"))
+                                       "gemm_preq", "gemm_repacked", "repack", "dequant", "gemv_q4_0",
+                                       "dequant_q4_0"))
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=4096)
@@ -35,6 +36,8 @@ def main(argv=None):
     need_w = a.kernel in ("gemv", "gemm", "gemm_preq", "gemm_repacked", "repack", "dequant")
     w = q8.quantize_q8_0(torch.from_numpy(inputs.weights_f32(n, k)).to(dev)) if need_w else None
     w32 = torch.from_numpy(inputs.weights_f32(n, k)).to(dev) if a.kernel == "quantize_q8_0" else None
+    w4 = (q8.quantize_q4_0(torch.from_numpy(inputs.weights_f32(n, k)).to(dev))
+          if a.kernel in ("gemv_q4_0", "dequant_q4_0") else None)
     xq, xd = q8.quantize_q8_1(x)
     xqh, xdt = q8.quantize_q8_1_mmq(x)
     ws = q8.gemm_workspace(m, k, dev) if a.kernel in ("gemm", "gemm_repacked") else None
@@ -58,6 +61,10 @@ def main(argv=None):
             q8.gemm_q8_0_repacked(wq16, wdt, x, ws=ws)
         elif a.kernel == "repack":
             q8.check(q8.q8act_repack_q8_0(w, wq16, wdt, n, k))
+        elif a.kernel == "gemv_q4_0":
+            q8.gemv_q4_0(w4, xq, xd, n)
+        elif a.kernel == "dequant_q4_0":
+            q8.dequant_q4_0_f16(w4, n, k)
         else:
             q8.dequant_q8_0_f16(w, n, k)
 
