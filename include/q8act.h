@@ -130,19 +130,20 @@ int q8act_gemv_q8_0_group(const void *const *w, float *const *y, const int64_t *
                           const int8_t *xq, const float *xd, int64_t m, int64_t k, void *stream);
 
 /*
- * Bytes of the workspace region that lets a fused GEMM split its last wave: when the
- * 128 x 128 output tiles fill the GPU's SMs unevenly and the last wave would be less than
- * half full, those tiles are cut into k pieces on the idle SMs, the pieces park partial
- * tiles here and the last piece to finish adds them in piece order (a fixed order: the result
- * does not depend on timing).  160 partial tiles of 64 KiB plus 160 counters.
+ * Bytes of the workspace region that lets a fused GEMM balance its work: when the 128 x 128
+ * output tiles do not fill whole waves of the GPU's SMs, every CTA (one per SM) takes an
+ * equal contiguous run of (tile, 256-wide k group) units, so that tiles at the runs' ends are
+ * cut into k pieces; the pieces park partial tiles here, and the last piece to finish adds
+ * them in a fixed order (the result does not depend on timing).  Room for two partial tiles
+ * of 64 KiB per CTA for up to 160 CTAs, plus 160 x 16 counters.
  */
-#define Q8ACT_GEMM_SPLIT_BYTES ((size_t)160 * 65536 + 160 * 4)
+#define Q8ACT_GEMM_SPLIT_BYTES ((size_t)320 * 65536 + 160 * 64)
 
 /*
  * Workspace bytes for the fused GEMMs on an m x k activation: the MMQ-layout quants and
  * scales plus Q8ACT_GEMM_SPLIT_BYTES.  A workspace of at least
- * q8act_gemm_workspace_bytes(m, k) - Q8ACT_GEMM_SPLIT_BYTES is accepted (the last wave is
- * then never split).  Returns 0 when the dimensions are invalid (as
+ * q8act_gemm_workspace_bytes(m, k) - Q8ACT_GEMM_SPLIT_BYTES is accepted (every tile is
+ * then done by one CTA over the whole of k).  Returns 0 when the dimensions are invalid (as
  * memra_fp8_blk_q8_0_bytes in fp8_ffi.rs returns 0 on bad dims).
  */
 size_t q8act_gemm_workspace_bytes(int64_t m, int64_t k);

@@ -40,7 +40,7 @@ EXPORTED = (
     "q8act_quantize_q4_0", "q8act_dequant_q4_0_f16", "q8act_gemv_q4_0", "q8act_debug_gemv_q4_0_block_dots",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
-Q8ACT_GEMM_SPLIT_BYTES = 160 * 65536 + 160 * 4
+Q8ACT_GEMM_SPLIT_BYTES = 320 * 65536 + 160 * 64
 
 
 class Q8ActError(RuntimeError):

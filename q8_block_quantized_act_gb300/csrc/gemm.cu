@@ -200,19 +200,35 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
     }
 }
 
-// Work split of one launch.  Tiles (128 weight rows x 128 tokens, row tile fastest) below
-// tiles_full are done by one CTA each over the whole of k.  When the remaining tiles fill less
-// than half of a wave, each of them is cut into `pieces` k ranges (whole 256-wide groups) on
-// separate CTAs, which write partial tiles to `partial`; the piece that finishes last (counted
-// in `counters`) adds the partial tiles in piece order and stores the result, so the output
-// does not depend on which piece finishes first.
-struct Split {
+// Work schedule of one launch.  The work is the sequence of units (tile, 256-wide k group),
+// tile-major; tiles are 128 weight rows x BN tokens, row tile fastest.  Plain: CTA c does tile
+// c over the whole of k.  Balanced: CTA c does the contiguous units [c U / C, (c + 1) U / C),
+// whole tiles in the middle and pieces of at most one tile at each end, so every CTA has the
+// same work to within one group whatever the tile count.  A piece parks each fold warp's
+// 32 x 32 slice of its partial sums in slot 2c (the CTA's first tile) or 2c + 1 (its last);
+// for every slice, the warp that completes the count of the tile's pieces (counters[first CTA
+// of the tile][warp]) adds the pieces' slices in CTA order and stores them, so the output does
+// not depend on which piece finishes first, and no warp ever waits for another.
+struct Sched {
     int ntn;             // tiles along n
-    int tiles_full;
-    int pieces;          // 1: no split
-    float *partial;      // float4 [leftover tile][piece][8][512 fold threads]
-    unsigned *counters;  // [leftover tile], zero on entry, zero again on exit
+    int G;               // 256-wide k groups per tile
+    long long units;     // tiles * G
+    int ctas;            // C = gridDim.x in balanced mode
+    int balanced;
+    float *partial;      // float4 [2 C][8][512 fold threads]
+    unsigned *counters;  // [C][16 fold warps], zero on entry, zero again on exit
 };
+
+__host__ __device__ __forceinline__ long long sched_start(const Sched &s, long long c)
+{
+    return c * s.units / s.ctas;
+}
+
+// The CTA whose range holds unit u.
+__host__ __device__ __forceinline__ int sched_owner(const Sched &s, long long u)
+{
+    return (int)(((u + 1) * s.ctas - 1) / s.units);
+}
 
 // REPACKED: the weights come as the load-time repacked planes (binary16 quants [n][k] and
 // f32 scales [k/32][ldn]) and are loaded by TMA exactly like the activation; the converter
@@ -223,7 +239,7 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_xd,
                      const __grid_constant__ CUtensorMap tm_wd, float *__restrict__ y,
-                     int32_t *__restrict__ dots, int m, int n, int k, Split sp, int *status)
+                     int32_t *__restrict__ dots, int m, int n, int k, Sched sp, int *status)
 {
     using C = Cfg<BN_T, !REPACKED>;
     constexpr int BN = C::BN, TMEM_COLS = C::TMEM_COLS, ACT_TILE_BYTES = C::ACT_TILE_BYTES;
@@ -241,23 +257,18 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // This CTA's tile and k range; kc below counts the CTA's own chunks, kg0 + kc is the
-    // chunk's place in k.
-    const int ngroups_all = k / (KC * CHUNKS_PER_GROUP);
-    int tile, piece = -1, g0 = 0, g1 = ngroups_all;
-    if ((int)blockIdx.x < sp.tiles_full) {
-        tile = blockIdx.x;
+    // This CTA's units [u0, u1); kc below counts the CTA's own chunks (unit u0 + kc / 4).
+    const int G = sp.G;
+    long long u0, u1;
+    if (sp.balanced) {
+        u0 = sched_start(sp, blockIdx.x);
+        u1 = sched_start(sp, (long long)blockIdx.x + 1);
     } else {
-        const int j = blockIdx.x - sp.tiles_full;
-        tile = sp.tiles_full + j / sp.pieces;
-        piece = j % sp.pieces;
-        g0 = piece * ngroups_all / sp.pieces;
-        g1 = (piece + 1) * ngroups_all / sp.pieces;
+        u0 = (long long)blockIdx.x * G;
+        u1 = u0 + G;
     }
-    const int row0 = (tile % sp.ntn) * BM;
-    const int tok0 = (tile / sp.ntn) * BN;
-    const int kg0 = g0 * CHUNKS_PER_GROUP;
-    const int nkc = (g1 - g0) * CHUNKS_PER_GROUP;
+    const int nkc = (int)(u1 - u0) * CHUNKS_PER_GROUP;
+    const int tile_first = (int)(u0 / G), kg_first = (int)(u0 % G);   // the CTA's first unit
     const int nb = k / QK;
 
     if (threadIdx.x == 0) {
@@ -291,13 +302,27 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             int issued_raw = 0, issued_act = 0, issued_sc = 0;
+            // The chunk's k group and tile (row tile rt, token tile tt), advanced without
+            // divisions: this thread's issue latency paces the repacked kernel.
+            int kg = kg_first, rt = tile_first % sp.ntn, tt = tile_first / sp.ntn;
+            int row0 = rt * BM, tok0 = tt * BN;
             for (int kc = 0; kc < nkc; ++kc) {
+                if (kc > 0 && (kc & (CHUNKS_PER_GROUP - 1)) == 0 && ++kg == G) {
+                    kg = 0;
+                    if (++rt == sp.ntn) {
+                        rt = 0;
+                        ++tt;
+                    }
+                    row0 = rt * BM;
+                    tok0 = tt * BN;
+                }
+                const int kch = kg * CHUNKS_PER_GROUP + (kc & (CHUNKS_PER_GROUP - 1));
                 if (!REPACKED && (kc & (CHUNKS_PER_GROUP - 1)) == 0) {
                     const int g = kc / CHUNKS_PER_GROUP;       // local group (ring position)
                     const int rs = g % RAW_STAGES;
                     if (!wait_or_abort(&bars.raw_empty[rs], ((g / RAW_STAGES) & 1) ^ 1, status, abort_flag)) break;
                     mbar_arrive_expect_tx(&bars.raw_full[rs], RAW_TILE_BYTES);
-                    tma_load_2d(smem + OFF_RAW + rs * RAW_TILE_BYTES, &tm_w, (g0 + g) * (GROUP_BYTES / 2), row0,
+                    tma_load_2d(smem + OFF_RAW + rs * RAW_TILE_BYTES, &tm_w, kg * (GROUP_BYTES / 2), row0,
                                 &bars.raw_full[rs]);
                     ++issued_raw;
                 }
@@ -308,16 +333,16 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                 // the first raw weight group -- overlaps that kernel's tail.
                 if (kc == 0) griddep_wait();
                 mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES + (REPACKED ? A_TILE_BYTES : 0));
-                tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, (kg0 + kc) * KC, tok0, &bars.stage_full[st]);
+                tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, kch * KC, tok0, &bars.stage_full[st]);
                 if (REPACKED)
-                    tma_load_2d(smem + OFF_A + st * A_TILE_BYTES, &tm_w, (kg0 + kc) * KC, row0, &bars.stage_full[st]);
+                    tma_load_2d(smem + OFF_A + st * A_TILE_BYTES, &tm_w, kch * KC, row0, &bars.stage_full[st]);
                 ++issued_act;
                 const int ss = kc % SC_STAGES;
                 if (!wait_or_abort(&bars.sc_empty[ss], ((kc / SC_STAGES) & 1) ^ 1, status, abort_flag)) break;
                 mbar_arrive_expect_tx(&bars.sc_full[ss], 2 * BN * 4 + (REPACKED ? 2 * BM * 4 : 0));
-                tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES, &tm_xd, tok0, 2 * (kg0 + kc), &bars.sc_full[ss]);
+                tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES, &tm_xd, tok0, 2 * kch, &bars.sc_full[ss]);
                 if (REPACKED)
-                    tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4, &tm_wd, row0, 2 * (kg0 + kc), &bars.sc_full[ss]);
+                    tma_load_2d(smem + OFF_SC + ss * SC_SLOT_BYTES + 2 * BN * 4, &tm_wd, row0, 2 * kch, &bars.sc_full[ss]);
                 ++issued_sc;
             }
             // Drain: never leave with a copy into this CTA's shared memory in flight.
@@ -452,15 +477,28 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
 #pragma unroll
             for (int j = 0; j < NJ; ++j) { acc[hl][j][0] = make_float2(0.f, 0.f); acc[hl][j][1] = make_float2(0.f, 0.f); }
 
-        for (int kc = 0; kc < nkc; ++kc) {
+        constexpr int FT = NUM_FOLD_WARPS * 32;
+        // Segments: runs of this CTA's chunks within one tile.  The chunk loop inside is the
+        // hot loop; a segment's epilogue stores or parks its accumulators.
+        bool ok = true;
+        int kc = 0;
+        for (int tile = tile_first, seg_kg = kg_first; ok && kc < nkc; ++tile, seg_kg = 0) {
+            const int seg_groups = (G - seg_kg) < (nkc - kc) / CHUNKS_PER_GROUP ? (G - seg_kg) : (nkc - kc) / CHUNKS_PER_GROUP;
+            const int seg_end = kc + seg_groups * CHUNKS_PER_GROUP;
+            const int kch0 = seg_kg * CHUNKS_PER_GROUP - kc;    // + kc: the chunk's place in k
+            const int row0 = (tile % sp.ntn) * BM, tok0 = (tile / sp.ntn) * BN;
+        for (; kc < seg_end; ++kc) {
             const int ss = kc % SC_STAGES;
             const int pr = kc & 1;
-            if (!wait_or_abort(&bars.pair_full[pr], (kc >> 1) & 1, status, abort_flag)) break;
-            if (!wait_or_abort(&bars.sc_full[ss], (kc / SC_STAGES) & 1, status, abort_flag)) break;
+            if (!wait_or_abort(&bars.pair_full[pr], (kc >> 1) & 1, status, abort_flag) ||
+                !wait_or_abort(&bars.sc_full[ss], (kc / SC_STAGES) & 1, status, abort_flag)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {
-                const int b = 2 * (kg0 + kc) + blk;
+                const int b = 2 * (kch0 + kc) + blk;
                 // Both 16-lane halves of this warp's 32 x 32 slice of the block's accumulator.
                 uint32_t d0[16], d1[16];
                 const uint32_t tcol = (uint32_t)((2 * pr + blk) * BN + FOLD_COLS * cq);
@@ -511,33 +549,77 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.sc_empty[ss]);
         }
-        if (!DOTS && !*abort_flag) {
-            if (piece >= 0) {
-                // A piece of a split tile: park the partial sums, thread index fastest, so that
-                // every warp store is one contiguous 512-byte run.
-                float4 *dst = reinterpret_cast<float4 *>(sp.partial) +
-                              ((int64_t)(tile - sp.tiles_full) * sp.pieces + piece) * (2 * NJ * NUM_FOLD_WARPS * 32) +
-                              fw * 32 + lane;
+            // ---- end of the segment ----
+            if (!ok) break;
+            if (!DOTS && !*abort_flag) {
+                bool store = seg_kg == 0 && seg_groups == G;   // the whole tile
+                if (!store) {
+                    // A piece: park this warp's slice, thread index fastest (every warp store is
+                    // one contiguous 512-byte run), then count it.
+                    const int slot = 2 * (int)blockIdx.x + (tile == tile_first ? 0 : 1);
+                    float4 *dst = reinterpret_cast<float4 *>(sp.partial) + (int64_t)slot * (2 * NJ * FT) + fw * 32 + lane;
 #pragma unroll
-                for (int hl = 0; hl < 2; ++hl)
+                    for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                    for (int j = 0; j < NJ; ++j)
-                        __stcg(dst + (hl * NJ + j) * (NUM_FOLD_WARPS * 32),
-                               make_float4(acc[hl][j][0].x, acc[hl][j][0].y, acc[hl][j][1].x, acc[hl][j][1].y));
-                __threadfence();
-            } else {
+                        for (int j = 0; j < NJ; ++j)
+                            __stcg(dst + (hl * NJ + j) * FT,
+                                   make_float4(acc[hl][j][0].x, acc[hl][j][0].y, acc[hl][j][1].x, acc[hl][j][1].y));
+                    __threadfence();
+                    __syncwarp();
+                    const int c0 = sched_owner(sp, (long long)tile * G);
+                    const int cl = sched_owner(sp, (long long)tile * G + G - 1);
+                    uint32_t last = 0;
+                    if (lane == 0) {
+                        unsigned *ctr = sp.counters + (size_t)c0 * NUM_FOLD_WARPS + fw;
+                        const unsigned before = atomicAdd(ctr, 1u);
+                        last = before == (unsigned)(cl - c0) ? 1u : 0u;
+                        if (last) *ctr = 0;   // ready for the next launch
+                        __threadfence();
+                    }
+                    store = __shfl_sync(0xffffffffu, last, 0) != 0;
+                    if (store) {
+                        // This warp's slice is complete: the pieces' sum, in CTA order.
+                        __threadfence();
+                        for (int cc = c0; cc <= cl; ++cc) {
+                            const int sl = 2 * cc + (tile == (int)(sched_start(sp, cc) / G) ? 0 : 1);
+                            const float4 *src = reinterpret_cast<const float4 *>(sp.partial) + (int64_t)sl * (2 * NJ * FT) +
+                                                fw * 32 + lane;
 #pragma unroll
-                for (int hl = 0; hl < 2; ++hl)
+                            for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                    for (int j = 0; j < NJ; ++j)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
-                            const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
-                            const float2 v = acc[hl][j][e >> 1];
-                            if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = (e & 1) ? v.y : v.x;
+                                for (int j = 0; j < NJ; ++j) {
+                                    const float4 v = __ldcg(src + (hl * NJ + j) * FT);
+                                    if (cc == c0) {
+                                        acc[hl][j][0] = make_float2(v.x, v.y);
+                                        acc[hl][j][1] = make_float2(v.z, v.w);
+                                    } else {
+                                        acc[hl][j][0].x = __fadd_rn(acc[hl][j][0].x, v.x);
+                                        acc[hl][j][0].y = __fadd_rn(acc[hl][j][0].y, v.y);
+                                        acc[hl][j][1].x = __fadd_rn(acc[hl][j][1].x, v.z);
+                                        acc[hl][j][1].y = __fadd_rn(acc[hl][j][1].y, v.w);
+                                    }
+                                }
                         }
+                    }
+                }
+                if (store) {
+#pragma unroll
+                    for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
+                                const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
+                                const float2 v = acc[hl][j][e >> 1];
+                                if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = (e & 1) ? v.y : v.x;
+                            }
+                }
             }
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) { acc[hl][j][0] = make_float2(0.f, 0.f); acc[hl][j][1] = make_float2(0.f, 0.f); }
         }
     }
 
@@ -547,57 +629,6 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS) : "memory");
-    }
-    if (DOTS || piece < 0) return;
-
-    // ---- split tile: the last piece to finish adds the partial tiles in piece order ----
-    volatile int *last = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
-    if (threadIdx.x == 0) {
-        const int lt = tile - sp.tiles_full;
-        const unsigned before = atomicAdd(&sp.counters[lt], 1u);
-        const bool is_last = before == (unsigned)sp.pieces - 1;
-        if (is_last) sp.counters[lt] = 0;   // ready for the next launch
-        __threadfence();
-        *last = is_last ? 1 : 0;
-    }
-    __syncthreads();
-    if (!*last || *abort_flag || warp < NUM_CONV_WARPS || warp >= NUM_CONV_WARPS + NUM_FOLD_WARPS) return;
-    {
-        const int fw = warp - NUM_CONV_WARPS;
-        const int quarter = warp & 3;
-        const int cq = fw >> 2;
-        const int tr = lane >> 2;
-        const int tc = 2 * (lane & 3);
-        constexpr int NJ = FOLD_COLS / 8;
-        constexpr int FT = NUM_FOLD_WARPS * 32;
-        const float4 *src = reinterpret_cast<const float4 *>(sp.partial) +
-                            (int64_t)(tile - sp.tiles_full) * sp.pieces * (2 * NJ * FT) + fw * 32 + lane;
-        const int64_t piece_stride = 2 * NJ * FT;   // in float4
-        float4 sum[2 * NJ];
-#pragma unroll
-        for (int i = 0; i < 2 * NJ; ++i) sum[i] = __ldcg(src + i * FT);
-        for (int pc = 1; pc < sp.pieces; ++pc) {
-#pragma unroll
-            for (int i = 0; i < 2 * NJ; ++i) {
-                const float4 v = __ldcg(src + pc * piece_stride + i * FT);
-                sum[i].x = __fadd_rn(sum[i].x, v.x);
-                sum[i].y = __fadd_rn(sum[i].y, v.y);
-                sum[i].z = __fadd_rn(sum[i].z, v.z);
-                sum[i].w = __fadd_rn(sum[i].w, v.w);
-            }
-        }
-#pragma unroll
-        for (int hl = 0; hl < 2; ++hl)
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r_e = row0 + 32 * quarter + 16 * hl + tr + 8 * (e >> 1);
-                    const int t_e = tok0 + FOLD_COLS * cq + 8 * j + tc + (e & 1);
-                    const float4 v = sum[hl * NJ + j];
-                    const float val = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-                    if (r_e < n && t_e < m) y[(int64_t)t_e * n + r_e] = val;
-                }
     }
 }
 
@@ -648,35 +679,46 @@ size_t gemm_split_bytes();
 
 namespace {
 
-constexpr int kMaxSplitUnits = 160;   // CTAs of a split last wave (>= the SM count)
-constexpr size_t kPartialBytes = (size_t)kMaxSplitUnits * BM * 128 * 4;   // a 128 x 128 f32 tile each
+constexpr int kMaxCtas = 160;   // CTAs of a balanced launch (>= the SM count)
+constexpr int kFoldWarps = 16;
+constexpr size_t kPartialBytes = (size_t)2 * kMaxCtas * BM * 128 * 4;   // two 128 x 128 f32 tiles per CTA
+constexpr size_t kCounterBytes = (size_t)kMaxCtas * kFoldWarps * sizeof(unsigned);
 
-// One CTA per tile; if the last wave would be less than half full, its tiles are cut into
-// k pieces that fill it (needs the split region of the workspace).
-Split plan_split(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, int BN, int ctas_per_sm, void *split_ws,
+// Plain (one CTA per tile over the whole of k) or balanced, whichever a simple cost model in
+// k groups on the longest-running SM favours: plain takes waves * G plus one group of set-up
+// per extra wave; balanced takes ceil(U / C) groups plus two for parking and counting pieces
+// plus one per piece of the most-cut tile (the completing warp reads every piece).  Measured
+// on GB300: at m = 512, 4096 x 4096 (128 tiles on 152 SMs, every tile cut) plain wins, 54 vs
+// 62 us per call; at 164, 640, 2016 and 2560 tiles balanced wins by 3-30 %.  The block-dot
+// export and calls without the split region are always plain.
+Sched plan_sched(const DeviceInfo &dev, int64_t m, int64_t n, int64_t k, int BN, int ctas_per_sm, void *split_ws,
                  size_t split_bytes, bool zero_counters, int64_t *grid, cudaStream_t stream, cudaError_t *err)
 {
-    Split sp{};
+    Sched sp{};
     const int64_t ntn = (n + BM - 1) / BM, ntm = (m + BN - 1) / BN, tiles = ntn * ntm;
     sp.ntn = (int)ntn;
-    sp.tiles_full = (int)tiles;
-    sp.pieces = 1;
+    sp.G = (int)(k / (KC * CHUNKS_PER_GROUP));
+    sp.units = tiles * sp.G;
+    sp.ctas = (int)tiles;
+    sp.balanced = 0;
     *grid = tiles;
     *err = cudaSuccess;
     const int64_t cap = (int64_t)dev.num_sms * ctas_per_sm;
-    const int64_t slots = cap < kMaxSplitUnits ? cap : kMaxSplitUnits;
-    const int64_t rem = tiles % slots;
-    const int64_t ngroups = k / (KC * CHUNKS_PER_GROUP);
-    if (!split_ws || split_bytes < gemm_split_bytes() || rem == 0 || 2 * rem > slots) return sp;
-    int64_t pieces = slots / rem;
-    if (pieces > ngroups) pieces = ngroups;
-    if (pieces < 2) return sp;
-    sp.tiles_full = (int)(tiles - rem);
-    sp.pieces = (int)pieces;
+    const int64_t slots = cap < kMaxCtas ? cap : kMaxCtas;
+    if (!split_ws || split_bytes < gemm_split_bytes() || tiles % slots == 0) return sp;
+    const int64_t C = slots < sp.units ? slots : sp.units;
+    const int64_t waves = (tiles + slots - 1) / slots;
+    const int64_t plain_cost = waves * sp.G + (waves - 1);
+    const int64_t per = sp.units / C;
+    const int64_t most_pieces = (sp.G + per - 1) / per + 1;
+    const int64_t balanced_cost = (sp.units + C - 1) / C + 2 + most_pieces;
+    if (balanced_cost >= plain_cost) return sp;
+    sp.balanced = 1;
+    sp.ctas = (int)C;
     sp.partial = static_cast<float *>(split_ws);
     sp.counters = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(split_ws) + kPartialBytes);
-    *grid = sp.tiles_full + rem * pieces;
-    if (zero_counters) *err = cudaMemsetAsync(sp.counters, 0, (size_t)rem * sizeof(unsigned), stream);
+    *grid = C;
+    if (zero_counters) *err = cudaMemsetAsync(sp.counters, 0, (size_t)C * kFoldWarps * sizeof(unsigned), stream);
     return sp;
 }
 
@@ -693,7 +735,8 @@ cudaError_t launch_kernel(const DeviceInfo &dev, const CUtensorMap &tm_w, const 
     cudaError_t e = set_kernel_smem<gemm_q8_0_kernel<DOTS, REPACKED, BN_T>>(dev.device, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int64_t grid = 0;
-    const Split sp = plan_split(dev, m, n, k, BN_T, C::CTAS_PER_SM, DOTS ? nullptr : split_ws, split_bytes, !pdl,
+    static_assert(C::NUM_FOLD_WARPS == kFoldWarps, "counter layout");
+    const Sched sp = plan_sched(dev, m, n, k, BN_T, C::CTAS_PER_SM, DOTS ? nullptr : split_ws, split_bytes, !pdl,
                                 &grid, stream, &e);
     if (e != cudaSuccess) return e;
     if (!pdl) {
@@ -727,7 +770,7 @@ bool encode_activation(CUtensorMap *tm_x, CUtensorMap *tm_xd, const uint16_t *xq
 
 size_t gemm_split_bytes()
 {
-    static_assert(kPartialBytes + (size_t)kMaxSplitUnits * sizeof(unsigned) == Q8ACT_GEMM_SPLIT_BYTES,
+    static_assert(kPartialBytes + kCounterBytes == Q8ACT_GEMM_SPLIT_BYTES,
                   "split region size");
     return Q8ACT_GEMM_SPLIT_BYTES;
 }
@@ -738,7 +781,7 @@ cudaError_t gemm_prepare_split(const DeviceInfo &dev, int64_t m, int64_t n, int6
     int64_t grid = 0;
     cudaError_t e = cudaSuccess;
     const int ctas = repacked ? Cfg<RP_BN, false>::CTAS_PER_SM : Cfg<128, true>::CTAS_PER_SM;
-    plan_split(dev, m, n, k, repacked ? RP_BN : 128, ctas, split_ws, split_bytes, true, &grid, stream, &e);
+    plan_sched(dev, m, n, k, repacked ? RP_BN : 128, ctas, split_ws, split_bytes, true, &grid, stream, &e);
     return e;
 }
 

@@ -60,27 +60,50 @@ def test_gemm_preq_equals_fused():
     assert np.array_equal(y_fused.view(np.uint32), y_pre.view(np.uint32))
 
 
+def _balanced(m, n, k):
+    """The fused GEMM's schedule choice (mirrors the library's plan): True when its cost model
+    prefers equal contiguous runs of (tile, k group) units per CTA over one CTA per tile."""
+    slots = min(torch.cuda.get_device_properties(0).multi_processor_count, 160)
+    tiles = -(-n // 128) * -(-m // 128)
+    G = k // 256
+    U = tiles * G
+    if tiles % slots == 0:
+        return False
+    C = min(slots, U)
+    waves = -(-tiles // slots)
+    per = U // C
+    balanced_cost = -(-U // C) + 2 + (-(-G // per) + 1)
+    return balanced_cost < waves * G + waves - 1
+
+
 @pytest.mark.parametrize("m,n,k", [
-    (200, 260, 1024),     # 6 tiles: every tile cut into the 4 groups of k
-    (1, 64, 4096),        # one tile cut into 16 pieces
-    (512, 5152, 4096),    # 164 tiles on 152 SMs: the 12 leftover tiles cut into 12 pieces
-    (130, 1200, 2048),    # 20 tiles, 8 pieces each, ragged in m and n
+    (512, 5152, 4096),    # 164 tiles on 152 SMs
+    (256, 20480, 1024),   # 320 tiles, 4 groups each
+    (64, 9000, 4096),     # ragged in m and n; tiles cut into up to 3 pieces
+    (512, 2048, 4096),    # 64 tiles, every one cut
 ])
-def test_gemm_last_wave_split(m, n, k):
-    """The split last wave: within 1e-5 * S of the oracle, deterministic, and within the same
-    bound of the unsplit result (only the order of the fold's f32 additions differs)."""
+def test_gemm_balanced_schedule(m, n, k):
+    """The balanced schedule: within 1e-5 * S of the oracle, deterministic, and within the same
+    bound of the one-CTA-per-tile schedule (only the order of the fold's f32 additions
+    differs); on the repacked weights too."""
     ensure_built()
+    assert _balanced(m, n, k), "shape does not take the balanced schedule"
     _, x, wb, xq, xd = problem(m, n, k, "token_scales")
     w_d, x_d = cuda(wb), cuda(x)
-    y_split = host(q8.gemm_q8_0(w_d, x_d, n))
+    y_bal = host(q8.gemm_q8_0(w_d, x_d, n))
     y_again = host(q8.gemm_q8_0(w_d, x_d, n))
-    y_whole = host(q8.gemm_q8_0(w_d, x_d, n, ws=_min_workspace(m, k)))
+    y_plain = host(q8.gemm_q8_0(w_d, x_d, n, ws=_min_workspace(m, k)))
+    wq16, wdt = q8.repack_q8_0(w_d, n, k)
+    y_rp = host(q8.gemm_q8_0_repacked(wq16, wdt, x_d))
     device_ok()
     rows = sample_rows(n, 256)
     _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
-    assert_within_tolerance(y_split[:, rows], y64, S)
-    assert_within_tolerance(y_whole[:, rows], y64, S)
-    assert np.array_equal(y_split.view(np.uint32), y_again.view(np.uint32)), "not deterministic"
+    assert_within_tolerance(y_bal[:, rows], y64, S)
+    assert_within_tolerance(y_plain[:, rows], y64, S)
+    assert_within_tolerance(y_rp[:, rows], y64, S)
+    assert np.array_equal(y_bal.view(np.uint32), y_again.view(np.uint32)), "not deterministic"
+    # the raw and the repacked kernels share the schedule and the fold: bitwise equal
+    assert np.array_equal(y_bal.view(np.uint32), y_rp.view(np.uint32))
 
 
 @pytest.mark.parametrize("m,n", [(512, 4096), (512, 5152), (2048, 20480), (512, 64448)])
