@@ -287,7 +287,14 @@ def run_ours(args, rank, world, local_rank):
     def k_deq4():
         q8.check(q8.q8act_dequant_q4_0_f16(w4_gemm, w16, DEQ["n"], DEQ["k"], stream))
 
-    nxt = [("dequant_q4_0_f16", k_deq4, True), ("gemv_q4_0", k_gemv4, False)]
+    ws_gemv = q8.gemv_workspace(GEMV["m"], GEMV["k"], dev)
+
+    def k_gemv_f32():
+        q8.check(q8.q8act_gemv_q8_0_f32(w_gemv, x_gemv, y4, GEMV["m"], GEMV["n"], GEMV["k"], ws_gemv,
+                                        ws_gemv.numel(), stream))
+
+    nxt = [("dequant_q4_0_f16", k_deq4, True), ("gemv_q4_0", k_gemv4, False),
+           ("gemv_q8_0_f32", k_gemv_f32, True)]
     k_quant()
     for _ in range(args.warmup):
         for _, fn, fl in nxt:
@@ -332,14 +339,17 @@ def run_ours(args, rank, world, local_rank):
     for nm in comps:
         comps[nm].update(spread[nm])
     g4 = gemv_q4_0_bytes(**GEMV)
+    gf = gemv_bytes(**GEMV) + 4 * GEMV["m"] * GEMV["k"]
     d4 = dequant_q4_0_bytes(**DEQ)
     next_rows = {
         "gemv_q4_0": roof("hbm", g4 / (mean4["gemv_q4_0"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
                           mean4["gemv_q4_0"], g4),
         "dequant_q4_0_f16": roof("hbm", d4 / (mean4["dequant_q4_0_f16"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
                                  mean4["dequant_q4_0_f16"], d4),
+        "gemv_q8_0_f32": roof("hbm", gf / (mean4["gemv_q8_0_f32"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                              mean4["gemv_q8_0_f32"], gf),
         "steps": nsteps,
-        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096, same seeded weights; timed after the step in a loop of their own (dequant after an L2 flush)",
+        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096 on the same seeded weights, and the fused decode call (q8_1 quantization + the Q8_0 GEMV in one call, f32 activation in; bytes = the GEMV's + the f32 activation); timed after the step in a loop of their own (the dequant and the fused call after an L2 flush)",
     }
     dominant = max(mean_ms, key=lambda nm: mean_ms[nm])
     traffic = load_traffic(dominant)

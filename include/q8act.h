@@ -247,6 +247,21 @@ int q8act_debug_gemm_repacked_block_dots(const uint16_t *wq16, const float *wdt,
                                          int64_t k, void *stream);
 
 /*
+ * The decode GEMV with the q8_1 quantization fused into the call (f32 activation in), like the
+ * fused GEMM: the quantizer writes xq and xd into `ws`, then the GEMV of q8act_gemv_q8_0 runs
+ * as a programmatic dependent of the quantizer, streaming its weights while the quantizer
+ * finishes and waiting for it before reading the activation.  Bitwise the same y as
+ * q8act_quantize_q8_1 followed by q8act_gemv_q8_0.  No counterpart in the pages (their decode
+ * census passes a pre-quantized activation): an addition of this library for the decode path.
+ *   w, y, m, n, k, stream: as for q8act_gemv_q8_0 (1 <= m <= 15); x [m][k] f32;
+ *   ws: device workspace of at least q8act_gemv_workspace_bytes(m, k) bytes (16-byte aligned).
+ * q8act_gemv_workspace_bytes returns 0 for invalid m or k.
+ */
+size_t q8act_gemv_workspace_bytes(int64_t m, int64_t k);
+int q8act_gemv_q8_0_f32(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Q4_0 weights -- the GGUF Q4_0 block named by memra-engine 0.81.0 f16_ffi.rs
  * (memra_q4_0_dequant_f16: "GGUF Q4_0 18B blocks -> row-major fp16 mirror").  A row of k
  * weights is k/32 blocks of 18 bytes: the binary16 scale d (little endian), then 16 bytes

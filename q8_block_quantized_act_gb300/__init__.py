@@ -22,7 +22,7 @@ from ._lib import (  # noqa: F401  (re-exported ABI)
     q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror,
     q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots,
     q8act_gemv_q8_0_group, Q8ACT_GEMV_MAX_GROUP, q8act_quantize_q4_0, q8act_dequant_q4_0_f16,
-    q8act_gemv_q4_0, q8act_debug_gemv_q4_0_block_dots)
+    q8act_gemv_q4_0, q8act_debug_gemv_q4_0_block_dots, q8act_gemv_workspace_bytes, q8act_gemv_q8_0_f32)
 
 QK = 32
 Q8_0_BYTES = 34
@@ -173,4 +173,24 @@ def gemv_q4_0(w, xq, xd, n: int, out=None):
     m, k = xq.shape
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
     check(q8act_gemv_q4_0(w, xq, xd, y, m, n, k), "q8act_gemv_q4_0")
+    return y
+
+
+def gemv_workspace(m: int, k: int, device):
+    """A workspace for the fused GEMV (q8act_gemv_q8_0_f32)."""
+    import torch
+    nbytes = q8act_gemv_workspace_bytes(m, k)
+    if nbytes == 0:
+        raise Q8ActError(Q8ACT_ERR_DIMS, "q8act_gemv_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def gemv_q8_0_f32(w, x, n: int, ws=None, out=None):
+    """Decode GEMV with the q8_1 quantization fused: f32 x [m, k] -> y f32 [m, n]."""
+    import torch
+    m, k = x.shape
+    if ws is None:
+        ws = gemv_workspace(m, k, x.device)
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
+    check(q8act_gemv_q8_0_f32(w, x, y, m, n, k, ws, ws.numel()), "q8act_gemv_q8_0_f32")
     return y

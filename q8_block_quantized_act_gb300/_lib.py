@@ -38,6 +38,7 @@ EXPORTED = (
     "q8act_gemm_q8_0_noalloc", "q8act_repack_q8_0", "q8act_repack_ldn",
     "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots", "q8act_gemv_q8_0_group",
     "q8act_quantize_q4_0", "q8act_dequant_q4_0_f16", "q8act_gemv_q4_0", "q8act_debug_gemv_q4_0_block_dots",
+    "q8act_gemv_workspace_bytes", "q8act_gemv_q8_0_f32",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 Q8ACT_GEMM_SPLIT_BYTES = 320 * 65536 + 160 * 64
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
                 "q8act_dequant_q4_0_f16": ([P, P, I64, I64, P], I32),
                 "q8act_gemv_q4_0": ([P, P, P, P, I64, I64, I64, P], I32),
                 "q8act_debug_gemv_q4_0_block_dots": ([P, P, P, I64, I64, I64, P], I32),
+                "q8act_gemv_workspace_bytes": ([I64, I64], SZ),
+                "q8act_gemv_q8_0_f32": ([P, P, P, I64, I64, I64, P, SZ, P], I32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -232,3 +235,11 @@ def q8act_gemv_q4_0(w, xq, xd, y, m, n, k, stream=None) -> int:
 
 def q8act_debug_gemv_q4_0_block_dots(w, xq, D, m, n, k, stream=None) -> int:
     return lib().q8act_debug_gemv_q4_0_block_dots(_p(w), _p(xq), _p(D), m, n, k, _s(stream))
+
+
+def q8act_gemv_workspace_bytes(m, k) -> int:
+    return lib().q8act_gemv_workspace_bytes(m, k)
+
+
+def q8act_gemv_q8_0_f32(w, x, y, m, n, k, ws, ws_bytes, stream=None) -> int:
+    return lib().q8act_gemv_q8_0_f32(_p(w), _p(x), _p(y), m, n, k, _p(ws), ws_bytes, _s(stream))

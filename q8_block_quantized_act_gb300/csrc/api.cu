@@ -159,8 +159,10 @@ int q8act_repack_q8_0(const void *w, uint16_t *wq16, float *wdt, int64_t n, int6
                                           n, k, (cudaStream_t)stream));
 }
 
+// pdl: the stream's previous operation is the q8_1 quantizer of the same call; the GEMV is
+// then launched as its programmatic dependent.
 static int gemv_common(const void *w, const int8_t *xq, const float *xd, float *y, int32_t *dots, int64_t m,
-                       int64_t n, int64_t k, void *stream)
+                       int64_t n, int64_t k, void *stream, bool pdl = false)
 {
     if (!w || !xq || !xd || (!y && !dots)) return Q8ACT_ERR_NULL;
     if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_MAX_M || n < 1 || n > INT32_MAX / 2 ||
@@ -173,10 +175,10 @@ static int gemv_common(const void *w, const int8_t *xq, const float *xd, float *
     if (rc) return rc;
     if (q8::gemv_mma_supported(*dev, m, k))
         return cuda_rc(q8::launch_gemv_q8_0_mma(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
-                                                (cudaStream_t)stream));
+                                                (cudaStream_t)stream, pdl));
     if (!q8::gemv_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
     return cuda_rc(q8::launch_gemv_q8_0(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
-                                        (cudaStream_t)stream));
+                                        (cudaStream_t)stream, pdl));
 }
 
 int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m, int64_t n, int64_t k,
@@ -184,6 +186,37 @@ int q8act_gemv_q8_0(const void *w, const int8_t *xq, const float *xd, float *y, 
 {
     if (!y) return Q8ACT_ERR_NULL;
     return gemv_common(w, xq, xd, y, nullptr, m, n, k, stream);
+}
+
+// Workspace of the fused GEMV: [int8 quants, m * k][f32 scales, m * k / 32], each part
+// rounded up to 256 bytes.
+size_t q8act_gemv_workspace_bytes(int64_t m, int64_t k)
+{
+    if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_MAX_M) return 0;
+    const size_t quants = (size_t)m * (size_t)k;
+    const size_t scales = (size_t)m * (size_t)(k / q8::QK) * 4;
+    return ((quants + 255) / 256 * 256) + ((scales + 255) / 256 * 256);
+}
+
+int q8act_gemv_q8_0_f32(const void *w, const float *x, float *y, int64_t m, int64_t n, int64_t k, void *ws,
+                        size_t ws_bytes, void *stream)
+{
+    if (!w || !x || !y) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_MAX_M || n < 1 || n > INT32_MAX / 2 ||
+        n * k > ((int64_t)1 << 36))
+        return Q8ACT_ERR_DIMS;
+    const size_t need = q8act_gemv_workspace_bytes(m, k);
+    if (!ws || ws_bytes < need) return Q8ACT_ERR_WORKSPACE;
+    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(ws)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if (!q8::gemv_mma_supported(*dev, m, k) && !q8::gemv_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
+    int8_t *xq = static_cast<int8_t *>(ws);
+    float *xd = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)m * k + 255) / 256 * 256);
+    rc = q8act_quantize_q8_1(x, xq, xd, m, k, stream);
+    if (rc) return rc;
+    return gemv_common(w, xq, xd, y, nullptr, m, n, k, stream, true);
 }
 
 int q8act_gemv_q8_0_group(const void *const *w, float *const *y, const int64_t *n, int count, const int8_t *xq,

@@ -227,6 +227,9 @@ __global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
     // activation cache -- quants [token][group][68 words], scales [token][group][12 words] --
     // and meet at a named barrier before their first chunk.
     if (tid < CONSUMERS) {
+        // The activation may come from the kernel just before this one in the stream (launched
+        // as its programmatic dependent); the weight stream above does not depend on it.
+        griddep_wait();
         for (int idx = tid; idx < M * G * 16; idx += CONSUMERS) {
             const int t = idx / (G * 16), rem = idx - t * G * 16, g = rem >> 4, c = rem & 15;
             const uint4 v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + g * 256 + c * 16);
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
 
 template <class F, int M, bool DOTS>
 cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const float *xd,
-                     int32_t *dots, int64_t k, cudaStream_t stream)
+                     int32_t *dots, int64_t k, bool pdl, cudaStream_t stream)
 {
     int64_t nmax = 0;
     for (int i = 0; i < grp.count; ++i) nmax = grp.n[i] > nmax ? grp.n[i] : nmax;
@@ -384,30 +387,34 @@ cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const f
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    kern<<<(int)grid, F::CONSUMERS + 32, p.smem, stream>>>(grp, xq, xd, dots, (int)k, p, dev.status);
-    return cudaGetLastError();
+    if (!pdl) {
+        kern<<<(int)grid, F::CONSUMERS + 32, p.smem, stream>>>(grp, xq, xd, dots, (int)k, p, dev.status);
+        return cudaGetLastError();
+    }
+    return launch_dependent(kern, (unsigned)grid, F::CONSUMERS + 32, p.smem, stream, grp, xq, xd, dots, (int)k, p,
+                            dev.status);
 }
 
 template <class F, bool DOTS>
 cudaError_t dispatch(const DeviceInfo &dev, const Group &grp, const int8_t *xq, const float *xd,
-                     int32_t *dots, int64_t m, int64_t k, cudaStream_t stream)
+                     int32_t *dots, int64_t m, int64_t k, cudaStream_t stream, bool pdl = false)
 {
     switch (m) {
-    case 1: return launch_m<F, 1, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 2: return launch_m<F, 2, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 3: return launch_m<F, 3, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 4: return launch_m<F, 4, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 5: return launch_m<F, 5, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 6: return launch_m<F, 6, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 7: return launch_m<F, 7, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 8: return launch_m<F, 8, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 9: return launch_m<F, 9, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 10: return launch_m<F, 10, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 11: return launch_m<F, 11, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 12: return launch_m<F, 12, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 13: return launch_m<F, 13, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 14: return launch_m<F, 14, DOTS>(dev, grp, xq, xd, dots, k, stream);
-    case 15: return launch_m<F, 15, DOTS>(dev, grp, xq, xd, dots, k, stream);
+    case 1: return launch_m<F, 1, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 2: return launch_m<F, 2, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 3: return launch_m<F, 3, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 4: return launch_m<F, 4, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 5: return launch_m<F, 5, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 6: return launch_m<F, 6, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 7: return launch_m<F, 7, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 8: return launch_m<F, 8, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 9: return launch_m<F, 9, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 10: return launch_m<F, 10, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 11: return launch_m<F, 11, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 12: return launch_m<F, 12, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 13: return launch_m<F, 13, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 14: return launch_m<F, 14, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
+    case 15: return launch_m<F, 15, DOTS>(dev, grp, xq, xd, dots, k, pdl, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -422,15 +429,15 @@ bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 
 cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
                              const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
-                             int64_t k, cudaStream_t stream)
+                             int64_t k, cudaStream_t stream, bool pdl)
 {
     Group grp{};
     grp.count = 1;
     grp.w[0] = w;
     grp.y[0] = y;
     grp.n[0] = (int)n;
-    if (dots) return dispatch<GQ8_0, true>(dev, grp, xq, xd, dots, m, k, stream);
-    return dispatch<GQ8_0, false>(dev, grp, xq, xd, dots, m, k, stream);
+    if (dots) return dispatch<GQ8_0, true>(dev, grp, xq, xd, dots, m, k, stream, pdl);
+    return dispatch<GQ8_0, false>(dev, grp, xq, xd, dots, m, k, stream, pdl);
 }
 
 bool gemv_q4_0_supported(const DeviceInfo &dev, int64_t m, int64_t k)

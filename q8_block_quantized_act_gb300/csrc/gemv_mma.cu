@@ -247,6 +247,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------- MMA warps: the activation cache (tokens >= m read as zero) -------------
+    // (after the kernel that produced the activation, when launched as its programmatic
+    // dependent; the weight stream does not depend on it)
+    griddep_wait();
     for (int idx = tid; idx < TOK * (k / 16); idx += NW * 32) {
         const int t = idx / (k / 16), c16 = idx - t * (k / 16);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int MT, bool DOTS>
 cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
-                      int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+                      int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream, bool pdl)
 {
     const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
@@ -391,8 +394,12 @@ cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
     cudaError_t e = set_kernel_smem<gemv_mma_kernel<MT, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
-    kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n, (int)k, p, dev.status);
-    return cudaGetLastError();
+    if (!pdl) {
+        kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n, (int)k, p, dev.status);
+        return cudaGetLastError();
+    }
+    return launch_dependent(kern, (unsigned)grid, THREADS, p.smem, stream, w, xq, xd, y, dots, (int)m, (int)n, (int)k, p,
+                            dev.status);
 }
 
 }  // namespace
@@ -406,13 +413,14 @@ bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 }
 
 cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
-                                 float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+                                 float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream,
+                                 bool pdl)
 {
     if (m > 8)
-        return dots ? launch_mt<2, true>(dev, w, xq, xd, y, dots, m, n, k, stream)
-                    : launch_mt<2, false>(dev, w, xq, xd, y, dots, m, n, k, stream);
-    return dots ? launch_mt<1, true>(dev, w, xq, xd, y, dots, m, n, k, stream)
-                : launch_mt<1, false>(dev, w, xq, xd, y, dots, m, n, k, stream);
+        return dots ? launch_mt<2, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
+                    : launch_mt<2, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+    return dots ? launch_mt<1, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
+                : launch_mt<1, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
 }
 
 }  // namespace q8

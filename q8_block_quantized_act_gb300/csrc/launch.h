@@ -42,11 +42,14 @@ cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *
                                    int64_t m, int64_t k, cudaStream_t stream);
 // The tensor-core GEMV for 3 <= m <= 16 (bitwise the same results as launch_gemv_q8_0).
 bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k);
+// pdl: launch as a programmatic dependent of the stream's previous kernel, which must be the
+// q8_1 quantizer producing xq / xd (the GEMV streams weights while it finishes).
 cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
-                                 float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+                                 float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream,
+                                 bool pdl = false);
 cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
                              const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
-                             int64_t k, cudaStream_t stream);
+                             int64_t k, cudaStream_t stream, bool pdl = false);
 
 // GEMM on MMQ-layout activations (xqh binary16 quants [m][k], xdt f32 scales [k/32][ldm]).
 // With dots != nullptr the fold is replaced by a store of the block dots D[m][n][k/32].

@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__rest
                                                             float *__restrict__ xd,
                                                             int64_t nchunks)
 {
+    // The GEMV that consumes this activation may be launched as a programmatic dependent: let
+    // it start streaming its weights (it waits for this grid before reading the activation).
+    griddep_launch_dependents();
     // Two independent chunks per step (more loads in flight).  nchunks is a multiple of 64
     // and the stride of 32, so both halves are warp-uniform, as the shuffles need.
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;

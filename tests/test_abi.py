@@ -38,6 +38,15 @@ def test_version_and_strerror(L):
         assert isinstance(q8.strerror(rc), str) and q8.strerror(rc)
 
 
+def test_gemv_workspace_query(L):
+    # int8 quants then f32 scales, each rounded up to 256 bytes; 0 for invalid m or k
+    assert q8.q8act_gemv_workspace_bytes(1, 4096) == 4096 + 512
+    assert q8.q8act_gemv_workspace_bytes(3, 256) == 768 + 256
+    assert q8.q8act_gemv_workspace_bytes(0, 4096) == 0
+    assert q8.q8act_gemv_workspace_bytes(q8.Q8ACT_GEMV_MAX_M + 1, 4096) == 0
+    assert q8.q8act_gemv_workspace_bytes(1, 100) == 0
+
+
 def test_workspace_query(L):
     assert q8.q8act_gemm_workspace_bytes(512, 4096) >= 512 * 4096 * 2 + 4096 // 32 * 512 * 4
     assert q8.q8act_gemm_workspace_bytes(0, 4096) == 0
@@ -103,6 +112,13 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_gemv_q4_0(A, A, A, A, 1, 8, 1280 + 32, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemv_q4_0(A, A, MIS, A, 1, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
     (lambda: q8.q8act_debug_gemv_q4_0_block_dots(A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, None, A, 1, 8, 256, A, 1 << 20, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, 0, 8, 256, A, 1 << 20, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, q8.Q8ACT_GEMV_MAX_M + 1, 8, 256, A, 1 << 20, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, 1, 8, 300, A, 1 << 20, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, 1, 8, 256, None, 1 << 20, S0), q8.Q8ACT_ERR_WORKSPACE),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, 1, 8, 256, A, 16, S0), q8.Q8ACT_ERR_WORKSPACE),
+    (lambda: q8.q8act_gemv_q8_0_f32(A, MIS, A, 1, 8, 256, A, 1 << 20, S0), q8.Q8ACT_ERR_ALIGN),
 ])
 def test_host_side_refusals(L, call, want):
     assert call() == want

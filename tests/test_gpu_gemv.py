@@ -6,6 +6,7 @@ import torch
 
 import oracle
 import q8_block_quantized_act_gb300 as q8
+from q8_block_quantized_act_gb300 import inputs
 from gpu_util import (assert_within_tolerance, cuda, device_ok, ensure_built, host, problem,
                       sample_rows)
 
@@ -105,3 +106,29 @@ def test_gemv_group_equals_single_calls(m, k, ns):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), f"matrix {i}"
     _, y64, S = oracle.matmul(ws[-1], xq, xd, k)
     assert_within_tolerance(ys[-1], y64, S)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 64448, 4096), (2, 5152, 4096), (3, 4096, 1280), (8, 20480, 4096),
+                                   (15, 777, 2048)])
+def test_gemv_f32_equals_two_calls(m, n, k):
+    """The fused decode call (q8_1 quantization, then the GEMV as its programmatic dependent)
+    gives bitwise the y of the two separate calls, also when two fused calls run back to back
+    on different activations; and it is within 1e-5 * S of the oracle."""
+    ensure_built()
+    w, x, wb, xq, xd = problem(m, n, k, "outliers")
+    x2 = inputs.activations_f32(m, k, kind="token_scales", seed=7)
+    w_d = cuda(wb)
+    ws = q8.gemv_workspace(m, k, w_d.device)
+    y1 = q8.gemv_q8_0_f32(w_d, cuda(x), n, ws=ws)
+    y2 = q8.gemv_q8_0_f32(w_d, cuda(x2), n, ws=ws)       # reuses the workspace right away
+    y1h, y2h = host(y1), host(y2)
+    xq1, xd1 = q8.quantize_q8_1(cuda(x))
+    ref1 = host(q8.gemv_q8_0(w_d, xq1, xd1, n))
+    xq2, xd2 = q8.quantize_q8_1(cuda(x2))
+    ref2 = host(q8.gemv_q8_0(w_d, xq2, xd2, n))
+    device_ok()
+    assert np.array_equal(y1h.view(np.uint32), ref1.view(np.uint32))
+    assert np.array_equal(y2h.view(np.uint32), ref2.view(np.uint32))
+    rows = sample_rows(n, 256)
+    _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
+    assert_within_tolerance(y1h[:, rows], y64, S)
