@@ -429,7 +429,8 @@ def load_traffic(kernel):
 
 def run_e2e(args, q8, torch, dev, stream):
     """The decode GEMV through the public API with host buffers: pinned host weights and
-    activation are copied in, the activation is quantized, the GEMV runs, y is copied out."""
+    activation are copied in, the fused decode call quantizes the activation and runs the GEMV,
+    y is copied out."""
     from q8_block_quantized_act_gb300 import inputs
     m, n, k = GEMV["m"], GEMV["n"], GEMV["k"]
     w_host = torch.empty((n, row_bytes(k)), dtype=torch.uint8).pin_memory()
@@ -440,15 +441,13 @@ def run_e2e(args, q8, torch, dev, stream):
     y_host = torch.empty((m, n), dtype=torch.float32).pin_memory()
     w_dev = torch.empty_like(w_host, device=dev)
     x_dev = torch.empty_like(x_host, device=dev)
-    xq = torch.empty((m, k), dtype=torch.int8, device=dev)
-    xd = torch.empty((m, k // 32), dtype=torch.float32, device=dev)
+    ws = q8.gemv_workspace(m, k, dev)
     y_dev = torch.empty((m, n), dtype=torch.float32, device=dev)
 
     def one():
         w_dev.copy_(w_host, non_blocking=True)
         x_dev.copy_(x_host, non_blocking=True)
-        q8.check(q8.q8act_quantize_q8_1(x_dev, xq, xd, m, k, stream))
-        q8.check(q8.q8act_gemv_q8_0(w_dev, xq, xd, y_dev, m, n, k, stream))
+        q8.check(q8.q8act_gemv_q8_0_f32(w_dev, x_dev, y_dev, m, n, k, ws, ws.numel(), stream))
         y_host.copy_(y_dev, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
