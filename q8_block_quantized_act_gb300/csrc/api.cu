@@ -305,8 +305,9 @@ int q8act_debug_gemv_q4_0_block_dots(const void *w, const int8_t *xq, int32_t *D
 }
 
 // Workspace of the fused GEMMs: [binary16 quants][block-major scales][split region].  The
-// first two are required; with the split region as well, a launch whose last wave would be
-// less than half full cuts those tiles into k pieces.
+// first two are required; with the split region as well, a launch may take the balanced
+// schedule (equal runs of (tile, k group) units per CTA, tiles cut into k pieces at the runs'
+// ends).
 static size_t act_bytes(int64_t m, int64_t k)
 {
     const size_t quants = (size_t)m * (size_t)k * 2;

@@ -53,7 +53,8 @@ cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8
 
 // GEMM on MMQ-layout activations (xqh binary16 quants [m][k], xdt f32 scales [k/32][ldm]).
 // With dots != nullptr the fold is replaced by a store of the block dots D[m][n][k/32].
-// Bytes of the optional workspace region that lets a GEMM split its last partial wave.
+// Bytes of the optional workspace region that lets a GEMM take the balanced schedule (tiles
+// cut into k pieces at the ends of equal per-CTA runs of work).
 size_t gemm_split_bytes();
 // pdl: launch as a programmatic dependent of the stream's previous kernel, which must be the
 // MMQ quantizer producing xqh / xdt (it lets the GEMM start early; the GEMM waits for it

@@ -44,7 +44,7 @@ extern "C" int q8act_gemm_q8_0_noalloc(const void *w, const float *x, float *y, 
     if (!w || !x || !y) return Q8ACT_ERR_NULL;
     const size_t full = q8act_gemm_workspace_bytes(m, k);
     if (full == 0 || n < 1) return Q8ACT_ERR_DIMS;
-    // The quantized activation must fit; the last-wave split region is used only when the
+    // The quantized activation must fit; the split region (balanced schedule) is used only when the
     // rest of the array holds it.
     if (full - Q8ACT_GEMM_SPLIT_BYTES > (size_t)Q8ACT_NOALLOC_WS_BYTES) return Q8ACT_ERR_WORKSPACE;
 

@@ -41,7 +41,8 @@ def test_gemm_matches_oracle(m, n, k, kind):
 
 
 def _min_workspace(m, k):
-    """A workspace without the last-wave split region (the call then never splits)."""
+    """A workspace without the split region (every tile is then done by one CTA over the whole
+    of k)."""
     return torch.empty(q8.q8act_gemm_workspace_bytes(m, k) - q8.Q8ACT_GEMM_SPLIT_BYTES,
                        dtype=torch.uint8, device="cuda")
 

@@ -45,7 +45,7 @@ def test_noalloc_gemm_matches_workspace_gemm_twice():
 def test_noalloc_gemm_refuses_beyond_its_scratch():
     ensure_built()
     k = 4096
-    # the quantized activation must fit in the scratch (the last-wave split region is optional)
+    # the quantized activation must fit in the scratch (the split region is optional)
     m_ok = max(mm for mm in range(2800, 3000)
                if q8.q8act_gemm_workspace_bytes(mm, k) - q8.Q8ACT_GEMM_SPLIT_BYTES <= q8.Q8ACT_NOALLOC_WS_BYTES)
     assert m_ok == 2891
