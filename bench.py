@@ -43,6 +43,7 @@ METRIC = "Q8_0 GEMV GB/s (m=1); Q8_0 MMQ GEMM TOPS (m=512); % of roofline"
 GEMV = dict(m=1, n=64448, k=4096)
 GEMM = dict(m=512, n=4096, k=4096)
 DEQ = dict(n=4096, k=4096)
+VERIFY_M = 8   # the verify tier's token count (7 drafted + 1)
 WORKLOAD = ("decode GEMV m=1 4096->64448 (q8_1 quantize + mmvq) + prefill GEMM m=512 "
             "4096->4096 (q8_1 quantize fused; on raw Q8_0 and on the load-time repack) + "
             "Q8_0->fp16 dequant 4096x4096")
@@ -293,8 +294,19 @@ def run_ours(args, rank, world, local_rank):
         q8.check(q8.q8act_gemv_q8_0_f32(w_gemv, x_gemv, y4, GEMV["m"], GEMV["n"], GEMV["k"], ws_gemv,
                                         ws_gemv.numel(), stream))
 
+    # the verify tier: 8 tokens (7 drafted + 1) against the decode weights, quantized once here
+    mv = VERIFY_M
+    xq_v = torch.empty((mv, GEMV["k"]), dtype=torch.int8, device=dev)
+    xd_v = torch.empty((mv, GEMV["k"] // 32), dtype=torch.float32, device=dev)
+    y_v = torch.empty((mv, GEMV["n"]), dtype=torch.float32, device=dev)
+    x_v = torch.from_numpy(inputs.activations_f32(mv, GEMV["k"], seed=2)).to(dev)
+    q8.check(q8.q8act_quantize_q8_1(x_v, xq_v, xd_v, mv, GEMV["k"], stream))
+
+    def k_verify():
+        q8.check(q8.q8act_gemv_q8_0(w_gemv, xq_v, xd_v, y_v, mv, GEMV["n"], GEMV["k"], stream))
+
     nxt = [("dequant_q4_0_f16", k_deq4, True), ("gemv_q4_0", k_gemv4, False),
-           ("gemv_q8_0_f32", k_gemv_f32, True)]
+           ("gemv_q8_0_f32", k_gemv_f32, True), ("gemv_q8_0_verify", k_verify, False)]
     k_quant()
     for _ in range(args.warmup):
         for _, fn, fl in nxt:
@@ -341,6 +353,7 @@ def run_ours(args, rank, world, local_rank):
     g4 = gemv_q4_0_bytes(**GEMV)
     gf = gemv_bytes(**GEMV) + 4 * GEMV["m"] * GEMV["k"]
     d4 = dequant_q4_0_bytes(**DEQ)
+    gv = gemv_bytes(VERIFY_M, GEMV["n"], GEMV["k"])
     next_rows = {
         "gemv_q4_0": roof("hbm", g4 / (mean4["gemv_q4_0"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
                           mean4["gemv_q4_0"], g4),
@@ -348,8 +361,10 @@ def run_ours(args, rank, world, local_rank):
                                  mean4["dequant_q4_0_f16"], d4),
         "gemv_q8_0_f32": roof("hbm", gf / (mean4["gemv_q8_0_f32"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
                               mean4["gemv_q8_0_f32"], gf),
+        "gemv_q8_0_verify": roof("hbm", gv / (mean4["gemv_q8_0_verify"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                 mean4["gemv_q8_0_verify"], gv),
         "steps": nsteps,
-        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096 on the same seeded weights, and the fused decode call (q8_1 quantization + the Q8_0 GEMV in one call, f32 activation in; bytes = the GEMV's + the f32 activation); timed after the step in a loop of their own (the dequant and the fused call after an L2 flush)",
+        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096 on the same seeded weights, and the fused decode call (q8_1 quantization + the Q8_0 GEMV in one call, f32 activation in; bytes = the GEMV's + the f32 activation), and the verify GEMV (m=8: 7 drafted tokens + 1, 4096->64448, the tensor-core GEMV); timed after the step in a loop of their own (the dequant and the fused call after an L2 flush)",
     }
     dominant = max(mean_ms, key=lambda nm: mean_ms[nm])
     traffic = load_traffic(dominant)

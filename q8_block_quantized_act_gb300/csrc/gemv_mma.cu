@@ -1,13 +1,15 @@
-// gemv_mma.cu -- the multi-token GEMV (3 <= m <= 16: speculative verify and small batches)
+// gemv_mma.cu -- the multi-token GEMV (2 <= m <= 16: speculative verify and small batches)
 // on the warp-level tensor-core MMA.
 //
 // The dp4a GEMV re-reads the activation from shared memory for every row it folds, so above
 // m = 1 it is bound by shared-memory bandwidth.  Here a warp computes a 16-row x 8-token tile
-// of block dots with two mma.sync m16n8k16 (f16 in, f32 accumulate): each row fragment is read
-// once for 8 tokens, each token fragment once for 16 rows.  The quants enter as exact binary16
-// integers and every partial sum of a 32-wide block dot is an integer below 2^19, exact in
-// f32, so the block dot is the exact integer (the int8 mma.sync runs at a third of the f16
-// rate on this part).
+// of block dots on the tensor cores: each row fragment is read once for 8 tokens, each token
+// fragment once for 16 rows.  One token group (m <= 8) takes one mma.sync m16n8k32 (s8 in,
+// s32 out) per block: the block dot itself, converted exactly to f32 (|D| < 2^19).  Two token
+// groups take two mma.sync m16n8k16 per block and group on exact binary16 integers (f32
+// accumulation; every partial sum is an integer below 2^19, exact), so each weight fragment
+// is converted once and serves both groups: the int8 MMA runs at a third of the f16 rate on
+// this part, and two of them per block would bound the kernel.
 //
 // Per (row, token) the fold is the dp4a kernel's, operation for operation: acc = 0, then
 // acc = fma(d_w * d_a, D, acc) over the 8 blocks of each 256-wide group in order, then the
@@ -63,9 +65,8 @@ MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap)
     p.items = p.RT * p.G;
     p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
     p.rs = p.row_bytes + (uint32_t)((16 - (int64_t)(p.row_bytes % 128) + 128) % 128);
-    // one token group (m <= 8): the cache holds binary16 (converted once), rows 32 (mod 128)
-    // bytes apart; two groups: int8, converted per use, rows 16 (mod 128) apart
-    p.xs = mt == 1 ? (uint32_t)(2 * k + 32) : (uint32_t)k + 16;
+    // int8 activation cache, rows 16 (mod 128) bytes apart
+    p.xs = (uint32_t)k + 16;
     p.stage_bytes = (uint32_t)p.R * p.rs;
     p.nchunks = (n + p.R - 1) / p.R;
     p.warp_tree = (p.G <= 32 && 32 % p.G == 0) ? 1 : 0;
@@ -124,6 +125,15 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
           "f"(c[3]));
 }
 
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
 // The quants of row `row` (in its slot) of block j of group g that this lane feeds to the
@@ -151,9 +161,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     int m, int n, int k, MPlan p, int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    // activation cache [8 MT][xs]: binary16 when MT == 1, int8 otherwise
+    // activation cache [8 MT][xs], int8
     uint8_t *xs8 = smem + p.off_x;
-    constexpr bool XH = MT == 1;
+    // one token group: one int8 MMA per block; two: the weight fragment converted to binary16
+    // once and fed to the f16 MMA for both groups
+    constexpr bool I8 = MT == 1;
     float *xds = reinterpret_cast<float *>(smem + p.off_xd);         // f32 [k/32][8 MT]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + MAX_STAGES;
@@ -254,18 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int t = idx / (k / 16), c16 = idx - t * (k / 16);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (t < m) v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + c16 * 16);
-        if (XH) {
-            uint4 h0, h1;
-            s8x4_to_f16x2x2(v.x, h0.x, h0.y);
-            s8x4_to_f16x2x2(v.y, h0.z, h0.w);
-            s8x4_to_f16x2x2(v.z, h1.x, h1.y);
-            s8x4_to_f16x2x2(v.w, h1.z, h1.w);
-            uint4 *dst = reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 32);
-            dst[0] = h0;
-            dst[1] = h1;
-        } else {
-            *reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 16) = v;
-        }
+        *reinterpret_cast<uint4 *>(xs8 + (size_t)t * p.xs + c16 * 16) = v;
     }
     for (int idx = tid; idx < nb * TOK; idx += NW * 32) {
         const int b = idx / TOK, t = idx - b * TOK;
@@ -303,34 +304,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t w0lo, w0hi, w1lo, w1hi;
                 load_row_quants(r0p, g, j, c, w0lo, w0hi);
                 load_row_quants(r1p, g, j, c, w1lo, w1hi);
-                // A fragments: k16 step 0 takes bytes 4c..4c+3, step 1 bytes 16+4c..16+4c+3
+                // f16 A fragments: k16 step 0 takes bytes 4c..4c+3, step 1 bytes 16+4c..16+4c+3;
+                // the int8 m16n8k32 fragment takes the same words as they are
                 uint32_t a0[4], a1[4];
-                s8x4_to_f16x2x2(w0lo, a0[0], a0[2]);
-                s8x4_to_f16x2x2(w1lo, a0[1], a0[3]);
-                s8x4_to_f16x2x2(w0hi, a1[0], a1[2]);
-                s8x4_to_f16x2x2(w1hi, a1[1], a1[3]);
+                if constexpr (I8) {
+                    a0[0] = w0lo; a0[1] = w1lo; a0[2] = w0hi; a0[3] = w1hi;
+                } else {
+                    s8x4_to_f16x2x2(w0lo, a0[0], a0[2]);
+                    s8x4_to_f16x2x2(w1lo, a0[1], a0[3]);
+                    s8x4_to_f16x2x2(w0hi, a1[0], a1[2]);
+                    s8x4_to_f16x2x2(w1hi, a1[1], a1[3]);
+                }
                 const int bo = g * GROUP_BYTES + j * Q8_0_BYTES;
                 const float dw0 = half_bits_to_float(*reinterpret_cast<const uint16_t *>(r0p + bo));
                 const float dw1 = half_bits_to_float(*reinterpret_cast<const uint16_t *>(r1p + bo));
                 const int b = g * GROUP_BLOCKS + j;
 #pragma unroll
                 for (int tg = 0; tg < MT; ++tg) {
-                    uint32_t b0lo, b0hi, b1lo, b1hi;
-                    if (XH) {
-                        const uint8_t *xp = xs8 + (size_t)gl * p.xs + 2 * (32 * b + 4 * c);
-                        const uint2 v0 = *reinterpret_cast<const uint2 *>(xp);
-                        const uint2 v1 = *reinterpret_cast<const uint2 *>(xp + 32);
-                        b0lo = v0.x; b0hi = v0.y; b1lo = v1.x; b1hi = v1.y;
+                    const uint8_t *xp = xs8 + (size_t)(8 * tg + gl) * p.xs + 32 * b + 4 * c;
+                    float D[4];
+                    if constexpr (I8) {
+                        // the exact int32 block dot (|D| < 2^19), converted exactly
+                        int di[4];
+                        mma_s8_16832(di, a0, lds32(xp), lds32(xp + 16));
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) D[e] = __int2float_rn(di[e]);
                     } else {
-                        const uint8_t *xp = xs8 + (size_t)(8 * tg + gl) * p.xs + 32 * b + 4 * c;
+                        uint32_t b0lo, b0hi, b1lo, b1hi;
                         s8x4_to_f16x2x2(lds32(xp), b0lo, b0hi);
                         s8x4_to_f16x2x2(lds32(xp + 16), b1lo, b1hi);
+                        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                        float d[4];
+                        mma_f16_16816(d, a0, b0lo, b0hi, zero);
+                        mma_f16_16816(D, a1, b1lo, b1hi, d);
                     }
-                    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-                    float d[4];
-                    mma_f16_16816(d, a0, b0lo, b0hi, zero);
-                    float D[4];
-                    mma_f16_16816(D, a1, b1lo, b1hi, d);
                     // D[0]: (row gl, token 2c), D[1]: (gl, 2c+1), D[2]: (gl+8, 2c), D[3]: (gl+8, 2c+1)
                     if (DOTS) {
 #pragma unroll
@@ -406,8 +413,8 @@ cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
 
 bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k)
 {
-    // at m = 2 the dp4a kernel is still the faster one (both give the same bits)
-    if (m < 3 || m > 16) return false;
+    // from m = 2 on this kernel is the faster one (both give the same bits)
+    if (m < 2 || m > 16) return false;
     const int mt = m > 8 ? 2 : 1;
     return mplan_ok(make_mplan(mt, 1 << 20, k, dev.max_smem_optin), mt);
 }

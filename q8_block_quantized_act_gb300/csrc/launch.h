@@ -40,7 +40,7 @@ bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);
 cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,
                                    const int64_t *n, int count, const int8_t *xq, const float *xd,
                                    int64_t m, int64_t k, cudaStream_t stream);
-// The tensor-core GEMV for 3 <= m <= 16 (bitwise the same results as launch_gemv_q8_0).
+// The tensor-core GEMV for 2 <= m <= 16 (bitwise the same results as launch_gemv_q8_0).
 bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k);
 // pdl: launch as a programmatic dependent of the stream's previous kernel, which must be the
 // q8_1 quantizer producing xq / xd (the GEMV streams weights while it finishes).
