@@ -305,8 +305,12 @@ def run_ours(args, rank, world, local_rank):
     def k_verify():
         q8.check(q8.q8act_gemv_q8_0(w_gemv, xq_v, xd_v, y_v, mv, GEMV["n"], GEMV["k"], stream))
 
+    def k_verify4():
+        q8.check(q8.q8act_gemv_q4_0(w4_gemv, xq_v, xd_v, y_v, mv, GEMV["n"], GEMV["k"], stream))
+
     nxt = [("dequant_q4_0_f16", k_deq4, True), ("gemv_q4_0", k_gemv4, False),
-           ("gemv_q8_0_f32", k_gemv_f32, True), ("gemv_q8_0_verify", k_verify, False)]
+           ("gemv_q8_0_f32", k_gemv_f32, True), ("gemv_q8_0_verify", k_verify, False),
+           ("gemv_q4_0_verify", k_verify4, False)]
     k_quant()
     for _ in range(args.warmup):
         for _, fn, fl in nxt:
@@ -354,6 +358,7 @@ def run_ours(args, rank, world, local_rank):
     gf = gemv_bytes(**GEMV) + 4 * GEMV["m"] * GEMV["k"]
     d4 = dequant_q4_0_bytes(**DEQ)
     gv = gemv_bytes(VERIFY_M, GEMV["n"], GEMV["k"])
+    gv4 = gemv_q4_0_bytes(VERIFY_M, GEMV["n"], GEMV["k"])
     next_rows = {
         "gemv_q4_0": roof("hbm", g4 / (mean4["gemv_q4_0"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
                           mean4["gemv_q4_0"], g4),
@@ -363,8 +368,10 @@ def run_ours(args, rank, world, local_rank):
                               mean4["gemv_q8_0_f32"], gf),
         "gemv_q8_0_verify": roof("hbm", gv / (mean4["gemv_q8_0_verify"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
                                  mean4["gemv_q8_0_verify"], gv),
+        "gemv_q4_0_verify": roof("hbm", gv4 / (mean4["gemv_q4_0_verify"] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                 mean4["gemv_q4_0_verify"], gv4),
         "steps": nsteps,
-        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096 on the same seeded weights, and the fused decode call (q8_1 quantization + the Q8_0 GEMV in one call, f32 activation in; bytes = the GEMV's + the f32 activation), and the verify GEMV (m=8: 7 drafted tokens + 1, 4096->64448, the tensor-core GEMV); timed after the step in a loop of their own (the dequant and the fused call after an L2 flush)",
+        "note": "Q4_0 (GGUF 18-byte blocks) GEMV m=1 4096->64448 and dequant 4096x4096 on the same seeded weights, and the fused decode call (q8_1 quantization + the Q8_0 GEMV in one call, f32 activation in; bytes = the GEMV's + the f32 activation), and the verify GEMVs (m=8: 7 drafted tokens + 1, 4096->64448, the tensor-core GEMV, on the Q8_0 and the Q4_0 weights); timed after the step in a loop of their own (the dequant and the fused call after an L2 flush)",
     }
     dominant = max(mean_ms, key=lambda nm: mean_ms[nm])
     traffic = load_traffic(dominant)

@@ -284,6 +284,9 @@ static int gemv_q4_0_common(const void *w, const int8_t *xq, const float *xd, fl
     const q8::DeviceInfo *dev;
     int rc = current_device(&dev);
     if (rc) return rc;
+    if (q8::gemv_q4_0_mma_supported(*dev, m, k))
+        return cuda_rc(q8::launch_gemv_q4_0_mma(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
+                                                (cudaStream_t)stream));
     if (!q8::gemv_q4_0_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
     return cuda_rc(q8::launch_gemv_q4_0(*dev, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
                                         (cudaStream_t)stream));

@@ -1,5 +1,5 @@
-// gemv_mma.cu -- the multi-token GEMV (2 <= m <= 16: speculative verify and small batches)
-// on the warp-level tensor-core MMA.
+// gemv_mma.cu -- the multi-token GEMV (speculative verify and small batches, m <= 16) on the
+// warp-level tensor-core MMA, over Q8_0 (from m = 2) or Q4_0 (from m = 5) weights.
 //
 // The dp4a GEMV re-reads the activation from shared memory for every row it folds, so above
 // m = 1 it is bound by shared-memory bandwidth.  Here a warp computes a 16-row x 8-token tile
@@ -45,7 +45,7 @@ struct MPlan {
     int items;          // RT * G
     int stages;
     int warp_tree;      // 1: combine groups pairwise (G divides 32), else left to right
-    uint32_t row_bytes; // Q8_0 bytes per row
+    uint32_t row_bytes; // weight bytes per row
     uint32_t rs;        // padded row slot in shared memory (16 mod 128)
     uint32_t xs;        // padded activation row of the cache
     uint32_t stage_bytes;
@@ -55,7 +55,7 @@ struct MPlan {
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap)
+MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap, int block_bytes)
 {
     MPlan p{};
     p.G = (int)(k / 256);
@@ -63,7 +63,7 @@ MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap)
     if (p.RT < 1) p.RT = 1;
     p.R = 16 * p.RT;
     p.items = p.RT * p.G;
-    p.row_bytes = (uint32_t)(k / QK * Q8_0_BYTES);
+    p.row_bytes = (uint32_t)(k / QK * block_bytes);
     p.rs = p.row_bytes + (uint32_t)((16 - (int64_t)(p.row_bytes % 128) + 128) % 128);
     // int8 activation cache, rows 16 (mod 128) bytes apart
     p.xs = (uint32_t)k + 16;
@@ -136,25 +136,61 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4]
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
-// The quants of row `row` (in its slot) of block j of group g that this lane feeds to the
-// MMA: bytes 4c..4c+3 (lo) and 16+4c..16+4c+3 (hi) of the block's 32.
-__device__ __forceinline__ void load_row_quants(const uint8_t *rowp, int g, int j, int c, uint32_t &lo,
-                                                uint32_t &hi)
-{
-    const int bo = g * GROUP_BYTES + j * Q8_0_BYTES;   // block start (2 mod 4 when j is odd)
-    if ((j & 1) == 0) {
-        // quants start at bo + 2, 2 mod 4: two aligned words each, bytes 2..5 of the pair
-        const uint8_t *q = rowp + bo + 4 * c;
-        lo = __byte_perm(lds32(q), lds32(q + 4), 0x5432);
-        hi = __byte_perm(lds32(q + 16), lds32(q + 20), 0x5432);
-    } else {
-        const uint8_t *q = rowp + bo + 2 + 4 * c;       // word aligned
-        lo = lds32(q);
-        hi = lds32(q + 16);
+// Weight formats.  quants(): the two words of block j of group g of a row (in its slot) that
+// this lane feeds to the int8 MMA: lo holds elements 4c..4c+3 and hi elements 16+4c..16+4c+3
+// of the block, as signed bytes.  The int8 MMA then sums 2^SHIFT * D exactly.
+//
+// Q8_0 (34-byte blocks): the quants themselves, bytes 4c..4c+3 and 16+4c..16+4c+3.
+struct MQ8_0 {
+    static constexpr int BLOCK_BYTES = Q8_0_BYTES;
+    static constexpr int GROUP = GROUP_BYTES;
+    static constexpr int SHIFT = 0;
+    // From m = 2 on this kernel beats the dp4a GEMV (4096 -> 64448: 59.7 vs 61.6 us at m = 2).
+    static constexpr int MIN_M = 2;
+    __device__ static void quants(const uint8_t *rowp, int g, int j, int c, uint32_t &lo, uint32_t &hi)
+    {
+        const int bo = g * GROUP + j * BLOCK_BYTES;   // block start (2 mod 4 when j is odd)
+        if ((j & 1) == 0) {
+            // quants start at bo + 2, 2 mod 4: two aligned words each, bytes 2..5 of the pair
+            const uint8_t *q = rowp + bo + 4 * c;
+            lo = __byte_perm(lds32(q), lds32(q + 4), 0x5432);
+            hi = __byte_perm(lds32(q + 16), lds32(q + 20), 0x5432);
+        } else {
+            const uint8_t *q = rowp + bo + 2 + 4 * c;       // word aligned
+            lo = lds32(q);
+            hi = lds32(q + 16);
+        }
     }
-}
+};
 
-template <int MT, bool DOTS>
+// Q4_0 (GGUF 18-byte blocks): element i < 16 in the low nibble of quant byte i, element i + 16
+// in its high nibble, value d * (nibble - 8).  Quant bytes 4c..4c+3 hold both of this lane's
+// element sets; each nibble is moved to the top of its byte and the byte's sign bit flipped,
+// which is the signed byte 16 * (nibble - 8).
+struct MQ4_0 {
+    static constexpr int BLOCK_BYTES = Q4_0_BYTES;
+    static constexpr int GROUP = Q4_GROUP_BYTES;
+    static constexpr int SHIFT = 4;
+    // Half the bytes of Q8_0 for the same MMA work: the dp4a GEMV stays ahead up to m = 4
+    // (4096 -> 64448: 41.0 / 53.4 / 59.8 us at m = 2 / 3 / 4 against 59.7 here; 95.3 against
+    // 60.5 at m = 8, 229.8 against 90.1 at m = 15).
+    static constexpr int MIN_M = 5;
+    __device__ static void quants(const uint8_t *rowp, int g, int j, int c, uint32_t &lo, uint32_t &hi)
+    {
+        const int bo = g * GROUP + j * BLOCK_BYTES;   // block start (2 mod 4 when j is odd)
+        uint32_t q4;
+        if ((j & 1) == 0) {
+            const uint8_t *q = rowp + bo + 4 * c;     // quant bytes 4c.. start 2 bytes in
+            q4 = __byte_perm(lds32(q), lds32(q + 4), 0x5432);
+        } else {
+            q4 = lds32(rowp + bo + 2 + 4 * c);        // word aligned
+        }
+        lo = ((q4 << 4) & 0xF0F0F0F0u) ^ 0x80808080u;
+        hi = (q4 & 0xF0F0F0F0u) ^ 0x80808080u;
+    }
+};
+
+template <class F, int MT, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 1)
     gemv_mma_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq,
                     const float *__restrict__ xd, float *__restrict__ y, int32_t *__restrict__ dots,
@@ -302,8 +338,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 2
             for (int j = 0; j < GROUP_BLOCKS; ++j) {
                 uint32_t w0lo, w0hi, w1lo, w1hi;
-                load_row_quants(r0p, g, j, c, w0lo, w0hi);
-                load_row_quants(r1p, g, j, c, w1lo, w1hi);
+                F::quants(r0p, g, j, c, w0lo, w0hi);
+                F::quants(r1p, g, j, c, w1lo, w1hi);
                 // f16 A fragments: k16 step 0 takes bytes 4c..4c+3, step 1 bytes 16+4c..16+4c+3;
                 // the int8 m16n8k32 fragment takes the same words as they are
                 uint32_t a0[4], a1[4];
@@ -315,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     s8x4_to_f16x2x2(w0hi, a1[0], a1[2]);
                     s8x4_to_f16x2x2(w1hi, a1[1], a1[3]);
                 }
-                const int bo = g * GROUP_BYTES + j * Q8_0_BYTES;
+                const int bo = g * F::GROUP + j * F::BLOCK_BYTES;
                 const float dw0 = half_bits_to_float(*reinterpret_cast<const uint16_t *>(r0p + bo));
                 const float dw1 = half_bits_to_float(*reinterpret_cast<const uint16_t *>(r1p + bo));
                 const int b = g * GROUP_BLOCKS + j;
@@ -324,11 +360,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint8_t *xp = xs8 + (size_t)(8 * tg + gl) * p.xs + 32 * b + 4 * c;
                     float D[4];
                     if constexpr (I8) {
-                        // the exact int32 block dot (|D| < 2^19), converted exactly
+                        // the exact int32 block dot (|D| < 2^19, a multiple of 2^SHIFT before
+                        // the shift), converted exactly
                         int di[4];
                         mma_s8_16832(di, a0, lds32(xp), lds32(xp + 16));
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) D[e] = __int2float_rn(di[e]);
+                        for (int e = 0; e < 4; ++e) D[e] = __int2float_rn(di[e] >> F::SHIFT);
                     } else {
                         uint32_t b0lo, b0hi, b1lo, b1hi;
                         s8x4_to_f16x2x2(lds32(xp), b0lo, b0hi);
@@ -337,6 +374,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         float d[4];
                         mma_f16_16816(d, a0, b0lo, b0hi, zero);
                         mma_f16_16816(D, a1, b1lo, b1hi, d);
+                        // 2^SHIFT * D is an integer below 2^24 (exact in f32); the scaling by a
+                        // power of two is exact
+                        if (F::SHIFT)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) D[e] *= 1.0f / (float)(1 << F::SHIFT);
                     }
                     // D[0]: (row gl, token 2c), D[1]: (gl, 2c+1), D[2]: (gl+8, 2c), D[3]: (gl+8, 2c+1)
                     if (DOTS) {
@@ -391,14 +433,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-template <int MT, bool DOTS>
+template <class F, int MT, bool DOTS>
 cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
                       int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream, bool pdl)
 {
-    const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin);
+    const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin, F::BLOCK_BYTES);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
-    auto kern = gemv_mma_kernel<MT, DOTS>;
-    cudaError_t e = set_kernel_smem<gemv_mma_kernel<MT, DOTS>>(dev.device, p.smem);
+    auto kern = gemv_mma_kernel<F, MT, DOTS>;
+    cudaError_t e = set_kernel_smem<gemv_mma_kernel<F, MT, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
     if (!pdl) {
@@ -409,25 +451,43 @@ cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
                             dev.status);
 }
 
+template <class F>
+bool supported(const DeviceInfo &dev, int64_t m, int64_t k)
+{
+    // where this kernel is the faster one (both give the same bits)
+    if (m < F::MIN_M || m > 16) return false;
+    const int mt = m > 8 ? 2 : 1;
+    return mplan_ok(make_mplan(mt, 1 << 20, k, dev.max_smem_optin, F::BLOCK_BYTES), mt);
+}
+
+template <class F>
+cudaError_t launch(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
+                   int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream, bool pdl)
+{
+    if (m > 8)
+        return dots ? launch_mt<F, 2, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
+                    : launch_mt<F, 2, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+    return dots ? launch_mt<F, 1, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
+                : launch_mt<F, 1, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+}
+
 }  // namespace
 
-bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k)
-{
-    // from m = 2 on this kernel is the faster one (both give the same bits)
-    if (m < 2 || m > 16) return false;
-    const int mt = m > 8 ? 2 : 1;
-    return mplan_ok(make_mplan(mt, 1 << 20, k, dev.max_smem_optin), mt);
-}
+bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k) { return supported<MQ8_0>(dev, m, k); }
 
 cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
                                  float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream,
                                  bool pdl)
 {
-    if (m > 8)
-        return dots ? launch_mt<2, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
-                    : launch_mt<2, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
-    return dots ? launch_mt<1, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
-                : launch_mt<1, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+    return launch<MQ8_0>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+}
+
+bool gemv_q4_0_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k) { return supported<MQ4_0>(dev, m, k); }
+
+cudaError_t launch_gemv_q4_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
+                                 float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+{
+    return launch<MQ4_0>(dev, w, xq, xd, y, dots, m, n, k, stream, false);
 }
 
 }  // namespace q8

@@ -34,6 +34,11 @@ bool gemv_q4_0_supported(const DeviceInfo &dev, int64_t m, int64_t k);
 cudaError_t launch_gemv_q4_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
                              const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
                              int64_t k, cudaStream_t stream);
+// The tensor-core Q4_0 GEMV for 5 <= m <= 16 (bitwise the same results as launch_gemv_q4_0).
+bool gemv_q4_0_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k);
+cudaError_t launch_gemv_q4_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
+                                 const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
+                                 int64_t k, cudaStream_t stream);
 
 // GEMV: returns cudaErrorInvalidValue when m*k is too large for the shared-memory plan.
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);
