@@ -43,7 +43,7 @@ def test_q4_0_dequant_bit_exact(n, k):
     assert np.array_equal(got, oracle.dequant_q4_0_f16(wb, k))
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 64, 256), (3, 200, 1280), (8, 129, 4096), (15, 40, 2048)])
+@pytest.mark.parametrize("m,n,k", [(1, 64, 256), (3, 200, 1280), (5, 40, 1280), (8, 129, 4096), (15, 40, 2048)])
 def test_q4_0_gemv_block_dots_exact(m, n, k):
     ensure_built()
     _, _, wb, xq, _ = q4_problem(m, n, k, "outliers")
@@ -58,6 +58,8 @@ def test_q4_0_gemv_block_dots_exact(m, n, k):
     (2, 5152, 4096, "outliers"),
     (8, 1000, 1280, "token_scales"),     # k = 5 groups: the shared-memory reduction path
     (15, 77, 4096, "normal"),
+    (5, 333, 1280, "outliers"),          # the tensor-core kernel's first m; 5 groups, ragged n
+    (11, 50, 6144, "token_scales"),      # two token groups, 24 groups per row
 ])
 def test_q4_0_gemv_matches_oracle(m, n, k, kind):
     ensure_built()
