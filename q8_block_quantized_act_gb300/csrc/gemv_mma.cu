@@ -21,7 +21,8 @@
 // cp.async.bulk per row into row slots padded to 16 (mod 128) bytes, so that the 8 rows a
 // warp reads at once fall in distinct banks.  The activation (int8) and its scales sit in
 // shared memory for the whole kernel, padded the same way.  Each MMA warp hands its weight
-// stage back as soon as its reads are done and parks its per-group partial sums in a partial
+// stage back once it has finished the chunk's items (handing it back right after the fragment
+// reads, before the MMAs, measured no faster) and parks its per-group partial sums in a partial
 // slot ([group][token][row]); reducer warps combine a chunk's partials in the fixed order and
 // store y while the MMA warps go on with the next chunk.  Every hand-off is an mbarrier with
 // a bounded wait; there is no CTA-wide barrier in the loop.
