@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // one token group: one int8 MMA per block; two: the weight fragment converted to binary16
     // once and fed to the f16 MMA for both groups
     constexpr bool I8 = MT == 1;
-    constexpr int JU = MT == 1 ? GROUP_BLOCKS : 2;   // blocks of a group unrolled together
     float *xds = reinterpret_cast<float *>(smem + p.off_xd);         // f32 [k/32][8 MT]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + MAX_STAGES;
@@ -337,7 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int rt = it / G, g = it - rt * G;
             const uint8_t *r0p = stage + (size_t)(16 * rt + gl) * p.rs;
             const uint8_t *r1p = r0p + (size_t)8 * p.rs;
-#pragma unroll JU
+            // the group's 8 blocks unrolled (2 -> 8: Q4_0 m = 8 60.8 -> 57.7 us, Q8_0 m = 12
+            // 86.2 -> 81.4 us at 4096 -> 64448)
+#pragma unroll
             for (int j = 0; j < GROUP_BLOCKS; ++j) {
                 uint32_t w0lo, w0hi, w1lo, w1hi;
                 F::quants(r0p, g, j, c, w0lo, w0hi);
