@@ -234,6 +234,9 @@ int q8act_gemv_q8_0_group(const void *const *w, float *const *y, const int64_t *
     const q8::DeviceInfo *dev;
     int rc = current_device(&dev);
     if (rc) return rc;
+    if (q8::gemv_mma_supported(*dev, m, k))
+        return cuda_rc(q8::launch_gemv_q8_0_group_mma(*dev, reinterpret_cast<const uint8_t *const *>(w), y, n, count,
+                                                      xq, xd, m, k, (cudaStream_t)stream));
     if (!q8::gemv_supported(*dev, m, k)) return Q8ACT_ERR_DIMS;
     return cuda_rc(q8::launch_gemv_q8_0_group(*dev, reinterpret_cast<const uint8_t *const *>(w), y, n, count, xq, xd,
                                               m, k, (cudaStream_t)stream));

@@ -228,4 +228,36 @@ cudaError_t set_kernel_smem(int device, size_t smem)
     return cudaSuccess;
 }
 
+// Several weight matrices that share the activation, streamed by one launch (the census's
+// stacked expert gate+up and the fused qkv shapes, as separate buffers): chunk c belongs to
+// matrix i when first_chunk[i] <= c < first_chunk[i + 1].  A single GEMV is a group of one.
+struct Group {
+    int count;
+    const uint8_t *w[Q8ACT_GEMV_MAX_GROUP];
+    float *y[Q8ACT_GEMV_MAX_GROUP];
+    int n[Q8ACT_GEMV_MAX_GROUP];
+    int64_t first_chunk[Q8ACT_GEMV_MAX_GROUP + 1];
+};
+
+struct ChunkRef {
+    const uint8_t *w;
+    float *y;
+    int n;
+    int64_t row0;
+    int rows;
+};
+
+__device__ __forceinline__ ChunkRef chunk_ref(const Group &grp, int64_t chunk, int R)
+{
+    int mi = 0;
+    while (mi + 1 < grp.count && chunk >= grp.first_chunk[mi + 1]) ++mi;
+    ChunkRef c;
+    c.w = grp.w[mi];
+    c.y = grp.y[mi];
+    c.n = grp.n[mi];
+    c.row0 = (chunk - grp.first_chunk[mi]) * R;
+    c.rows = (int)((c.n - c.row0) < R ? (c.n - c.row0) : R);
+    return c;
+}
+
 }  // namespace q8

@@ -52,11 +52,11 @@ struct MPlan {
     uint32_t stage_bytes;
     uint32_t part_bytes; // one partial slot: [G][8 mt][R] f32
     int nparts;          // partial slots (1 or 2)
-    int64_t nchunks;
+    int64_t nchunks;    // chunks of the whole group (set at launch)
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap, int block_bytes)
+MPlan make_mplan(int mt, int64_t k, size_t smem_cap, int block_bytes)
 {
     MPlan p{};
     p.G = (int)(k / 256);
@@ -69,7 +69,6 @@ MPlan make_mplan(int mt, int64_t n, int64_t k, size_t smem_cap, int block_bytes)
     // int8 activation cache, rows 16 (mod 128) bytes apart
     p.xs = (uint32_t)k + 16;
     p.stage_bytes = (uint32_t)p.R * p.rs;
-    p.nchunks = (n + p.R - 1) / p.R;
     p.warp_tree = (p.G <= 32 && 32 % p.G == 0) ? 1 : 0;
     p.part_bytes = (uint32_t)((size_t)p.G * 8 * mt * p.R * 4);
     const size_t x_bytes = (size_t)8 * mt * p.xs;
@@ -193,9 +192,9 @@ struct MQ4_0 {
 
 template <class F, int MT, bool DOTS>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemv_mma_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq,
-                    const float *__restrict__ xd, float *__restrict__ y, int32_t *__restrict__ dots,
-                    int m, int n, int k, MPlan p, int *status)
+    gemv_mma_kernel(const __grid_constant__ Group grp, const int8_t *__restrict__ xq,
+                    const float *__restrict__ xd, int32_t *__restrict__ dots, int m, int k, MPlan p,
+                    int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     // activation cache [8 MT][xs], int8
@@ -239,12 +238,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int64_t i = 0; i < my_chunks; ++i) {
                 const int s = (int)(i % p.stages);
                 if (!mbar_wait(&empty[s], (uint32_t)(((i / p.stages) & 1) ^ 1), status)) break;
-                const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
-                const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+                const ChunkRef cr = chunk_ref(grp, blockIdx.x + i * gridDim.x, p.R);
+                const int64_t row0 = cr.row0;
+                const int rows = cr.rows;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)rows * p.row_bytes);
                 uint8_t *dst = smem + (size_t)s * p.stage_bytes;
                 for (int r = 0; r < rows; ++r)
-                    bulk_g2s_hint(dst + (size_t)r * p.rs, w + (row0 + r) * (int64_t)p.row_bytes, p.row_bytes,
+                    bulk_g2s_hint(dst + (size_t)r * p.rs, cr.w + (row0 + r) * (int64_t)p.row_bytes, p.row_bytes,
                                   &full[s], policy);
                 ++issued;
             }
@@ -262,8 +262,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int ps = (int)(i % p.nparts);
             const bool ok = mbar_wait(&pfull[ps], (uint32_t)((i / p.nparts) & 1), status);
             if (__any_sync(0xffffffffu, !ok)) break;
-            const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
-            const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+            const ChunkRef cr = chunk_ref(grp, blockIdx.x + i * gridDim.x, p.R);
+            const int64_t row0 = cr.row0;
+            const int rows = cr.rows;
             const float *part = reinterpret_cast<const float *>(smem + p.off_part + (size_t)ps * p.part_bytes);
             const size_t gstride = (size_t)TOK * p.R;
             for (int idx = rtid; idx < rows * m; idx += NR * 32) {
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sum = pr[0];
                     for (int gg = 1; gg < G; ++gg) sum = __fadd_rn(sum, pr[gg * gstride]);
                 }
-                y[(int64_t)t * n + row0 + r] = sum;
+                cr.y[(int64_t)t * cr.n + row0 + r] = sum;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&pempty[ps]);
@@ -317,7 +318,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = (int)(i % p.stages);
         const bool ok = mbar_wait(&full[s], (uint32_t)((i / p.stages) & 1), status);
         if (__any_sync(0xffffffffu, !ok)) break;
+        // (the block-dot export serves a group of one)
         const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+        const int n = grp.n[0];
         const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
         const uint8_t *stage = smem + (size_t)s * p.stage_bytes;
 
@@ -437,20 +440,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <class F, int MT, bool DOTS>
-cudaError_t launch_mt(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
-                      int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream, bool pdl)
+cudaError_t launch_mt(const DeviceInfo &dev, Group grp, const int8_t *xq, const float *xd, int32_t *dots, int64_t m,
+                      int64_t k, cudaStream_t stream, bool pdl)
 {
-    const MPlan p = make_mplan(MT, n, k, dev.max_smem_optin, F::BLOCK_BYTES);
+    MPlan p = make_mplan(MT, k, dev.max_smem_optin, F::BLOCK_BYTES);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
+    grp.first_chunk[0] = 0;
+    for (int i = 0; i < grp.count; ++i) grp.first_chunk[i + 1] = grp.first_chunk[i] + (grp.n[i] + p.R - 1) / p.R;
+    p.nchunks = grp.first_chunk[grp.count];
     auto kern = gemv_mma_kernel<F, MT, DOTS>;
     cudaError_t e = set_kernel_smem<gemv_mma_kernel<F, MT, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
     if (!pdl) {
-        kern<<<(int)grid, THREADS, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n, (int)k, p, dev.status);
+        kern<<<(int)grid, THREADS, p.smem, stream>>>(grp, xq, xd, dots, (int)m, (int)k, p, dev.status);
         return cudaGetLastError();
     }
-    return launch_dependent(kern, (unsigned)grid, THREADS, p.smem, stream, w, xq, xd, y, dots, (int)m, (int)n, (int)k, p,
+    return launch_dependent(kern, (unsigned)grid, THREADS, p.smem, stream, grp, xq, xd, dots, (int)m, (int)k, p,
                             dev.status);
 }
 
@@ -460,18 +466,28 @@ bool supported(const DeviceInfo &dev, int64_t m, int64_t k)
     // where this kernel is the faster one (both give the same bits)
     if (m < F::MIN_M || m > 16) return false;
     const int mt = m > 8 ? 2 : 1;
-    return mplan_ok(make_mplan(mt, 1 << 20, k, dev.max_smem_optin, F::BLOCK_BYTES), mt);
+    return mplan_ok(make_mplan(mt, k, dev.max_smem_optin, F::BLOCK_BYTES), mt);
 }
 
 template <class F>
-cudaError_t launch(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
-                   int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream, bool pdl)
+cudaError_t launch(const DeviceInfo &dev, const Group &grp, const int8_t *xq, const float *xd, int32_t *dots,
+                   int64_t m, int64_t k, cudaStream_t stream, bool pdl)
 {
     if (m > 8)
-        return dots ? launch_mt<F, 2, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
-                    : launch_mt<F, 2, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
-    return dots ? launch_mt<F, 1, true>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl)
-                : launch_mt<F, 1, false>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+        return dots ? launch_mt<F, 2, true>(dev, grp, xq, xd, dots, m, k, stream, pdl)
+                    : launch_mt<F, 2, false>(dev, grp, xq, xd, dots, m, k, stream, pdl);
+    return dots ? launch_mt<F, 1, true>(dev, grp, xq, xd, dots, m, k, stream, pdl)
+                : launch_mt<F, 1, false>(dev, grp, xq, xd, dots, m, k, stream, pdl);
+}
+
+Group group_of_one(const uint8_t *w, float *y, int64_t n)
+{
+    Group grp{};
+    grp.count = 1;
+    grp.w[0] = w;
+    grp.y[0] = y;
+    grp.n[0] = (int)n;
+    return grp;
 }
 
 }  // namespace
@@ -482,7 +498,22 @@ cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const 
                                  float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream,
                                  bool pdl)
 {
-    return launch<MQ8_0>(dev, w, xq, xd, y, dots, m, n, k, stream, pdl);
+    return launch<MQ8_0>(dev, group_of_one(w, y, n), xq, xd, dots, m, k, stream, pdl);
+}
+
+cudaError_t launch_gemv_q8_0_group_mma(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,
+                                       const int64_t *n, int count, const int8_t *xq, const float *xd,
+                                       int64_t m, int64_t k, cudaStream_t stream)
+{
+    if (count < 1 || count > Q8ACT_GEMV_MAX_GROUP) return cudaErrorInvalidValue;
+    Group grp{};
+    grp.count = count;
+    for (int i = 0; i < count; ++i) {
+        grp.w[i] = w[i];
+        grp.y[i] = y[i];
+        grp.n[i] = (int)n[i];
+    }
+    return launch<MQ8_0>(dev, grp, xq, xd, nullptr, m, k, stream, false);
 }
 
 bool gemv_q4_0_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k) { return supported<MQ4_0>(dev, m, k); }
@@ -490,7 +521,7 @@ bool gemv_q4_0_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k) { retu
 cudaError_t launch_gemv_q4_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
                                  float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
 {
-    return launch<MQ4_0>(dev, w, xq, xd, y, dots, m, n, k, stream, false);
+    return launch<MQ4_0>(dev, group_of_one(w, y, n), xq, xd, dots, m, k, stream, false);
 }
 
 }  // namespace q8

@@ -52,6 +52,11 @@ bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k);
 cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
                                  float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream,
                                  bool pdl = false);
+// The grouped GEMV (several weight matrices, one activation) on the tensor-core kernel, for the
+// m that gemv_mma_supported accepts (bitwise the same results as launch_gemv_q8_0_group).
+cudaError_t launch_gemv_q8_0_group_mma(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,
+                                       const int64_t *n, int count, const int8_t *xq, const float *xd,
+                                       int64_t m, int64_t k, cudaStream_t stream);
 cudaError_t launch_gemv_q8_0(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq,
                              const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
                              int64_t k, cudaStream_t stream, bool pdl = false);

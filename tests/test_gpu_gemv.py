@@ -41,7 +41,7 @@ def test_gemv_matches_oracle(m, n, k, kind):
     assert_within_tolerance(y, y64, S)
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 512, 256), (4, 300, 1280), (8, 130, 4096), (15, 70, 4096)])
+@pytest.mark.parametrize("m,n,k", [(1, 512, 256), (2, 77, 1280), (4, 300, 1280), (8, 130, 4096), (15, 70, 4096)])
 def test_gemv_block_dots_exact(m, n, k):
     ensure_built()
     _, _, wb, xq, _ = problem(m, n, k)
