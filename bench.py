@@ -222,10 +222,12 @@ def run_ours(args, rank, world, local_rank):
     def k_deq():
         q8.check(q8.q8act_dequant_q8_0_f16(w_gemm, w16, DEQ["n"], DEQ["k"], stream))
 
-    # Order: GEMM and dequant (L2 flushed before each), then the decode path -- the token's
-    # q8_1 quantization and the GEMV.  The quantizer's 16 KB input was evicted by the previous
-    # step's 280 MB GEMV stream and the two flushes; the GEMV's input is larger than L2.
-    parts = [("gemm_q8_0", k_gemm), ("gemm_q8_0_repacked", k_gemm_rp), ("dequant_q8_0_f16", k_deq),
+    # Order: the dequant and the two GEMMs (L2 flushed before each), then the decode path -- the
+    # token's q8_1 quantization and the GEMV.  The decode path follows a GEMM (8.4 MB output),
+    # not the load-time dequant, whose 33.5 MB output would otherwise be written back from L2
+    # inside the GEMV's stream.  The quantizer's 16 KB input was evicted by the previous step's
+    # 280 MB GEMV stream and the flushes; the GEMV's input is larger than L2.
+    parts = [("dequant_q8_0_f16", k_deq), ("gemm_q8_0", k_gemm), ("gemm_q8_0_repacked", k_gemm_rp),
              ("quantize_q8_1", k_quant), ("gemv_q8_0", k_gemv)]
     launches_per_step = {"quantize_q8_1": 1, "gemv_q8_0": 1, "gemm_q8_0": 2, "gemm_q8_0_repacked": 2,
                          "dequant_q8_0_f16": 1}
