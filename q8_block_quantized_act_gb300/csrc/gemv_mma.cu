@@ -445,6 +445,7 @@ cudaError_t launch_mt(const DeviceInfo &dev, Group grp, const int8_t *xq, const 
 {
     MPlan p = make_mplan(MT, k, dev.max_smem_optin, F::BLOCK_BYTES);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
+    if (DOTS && grp.count != 1) return cudaErrorInvalidValue;   // the export serves one matrix
     grp.first_chunk[0] = 0;
     for (int i = 0; i < grp.count; ++i) grp.first_chunk[i + 1] = grp.first_chunk[i] + (grp.n[i] + p.R - 1) / p.R;
     p.nchunks = grp.first_chunk[grp.count];
