@@ -370,8 +370,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // the shift), converted exactly
                         int di[4];
                         mma_s8_16832(di, a0, lds32(xp), lds32(xp + 16));
+                        // int -> f32 without the conversion pipe: for |D| < 2^22 the f32 with
+                        // the bits of D + bits(1.5 * 2^23) is exactly 1.5 * 2^23 + D (unit
+                        // spacing there), and subtracting 1.5 * 2^23 leaves D exactly
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) D[e] = __int2float_rn(di[e] >> F::SHIFT);
+                        for (int e = 0; e < 4; ++e)
+                            D[e] = __fsub_rn(__int_as_float((di[e] >> F::SHIFT) + 0x4B400000), 12582912.0f);
                     } else {
                         uint32_t b0lo, b0hi, b1lo, b1hi;
                         s8x4_to_f16x2x2(lds32(xp), b0lo, b0hi);
