@@ -91,7 +91,9 @@ def test_gemv_k_limit(m, kmax):
 
 
 @pytest.mark.parametrize("m,k,ns", [(1, 4096, (4096, 5152, 777)), (2, 1280, (4096, 33)),
-                                    (4, 4096, (64, 4096, 20480, 1)), (9, 2048, (300, 200, 100))])
+                                    (4, 4096, (64, 4096, 20480, 1)), (9, 2048, (300, 200, 100)),
+                                    # the largest group; 5 groups per row (64-row chunks), ragged sizes
+                                    (12, 1280, (130, 64, 1, 777, 65, 200, 1000, 63))])
 def test_gemv_group_equals_single_calls(m, k, ns):
     """One grouped launch gives each matrix bitwise the result of its own GEMV."""
     ensure_built()
