@@ -145,7 +145,7 @@ struct MQ8_0 {
     static constexpr int BLOCK_BYTES = Q8_0_BYTES;
     static constexpr int GROUP = GROUP_BYTES;
     static constexpr int SHIFT = 0;
-    // From m = 2 on this kernel beats the dp4a GEMV (4096 -> 64448: 59.7 vs 61.6 us at m = 2).
+    // From m = 2 on this kernel beats the dp4a GEMV (4096 -> 64448: 58.5 vs 61.6 us at m = 2).
     static constexpr int MIN_M = 2;
     __device__ static void quants(const uint8_t *rowp, int g, int j, int c, uint32_t &lo, uint32_t &hi)
     {
@@ -171,9 +171,9 @@ struct MQ4_0 {
     static constexpr int BLOCK_BYTES = Q4_0_BYTES;
     static constexpr int GROUP = Q4_GROUP_BYTES;
     static constexpr int SHIFT = 4;
-    // Half the bytes of Q8_0 for the same MMA work: the dp4a GEMV stays ahead up to m = 4
-    // (4096 -> 64448: 41.0 / 53.4 / 59.8 us at m = 2 / 3 / 4 against 59.7 here; 95.3 against
-    // 60.5 at m = 8, 229.8 against 90.1 at m = 15).
+    // Half the bytes of Q8_0 for the same MMA work: the dp4a GEMV stays ahead up to m = 3 and
+    // ties at m = 4 (4096 -> 64448: 36.1 / 45.5 / 59.7 us at m = 2 / 3 / 4 against ~57.5 here,
+    // ahead at 4096 x 4096); 95.3 against 57.7 at m = 8, 229.8 against ~84 at m = 15.
     static constexpr int MIN_M = 5;
     __device__ static void quants(const uint8_t *rowp, int g, int j, int c, uint32_t &lo, uint32_t &hi)
     {
