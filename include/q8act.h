@@ -35,7 +35,10 @@
  *
  * Kernels time out instead of hanging: a pipeline wait that exceeds about two seconds makes
  * the kernel record an error in a device-side status word and return early.
- * q8act_device_status() reads and clears that word.
+ * q8act_device_status() reads and clears that word.  Before a CTA exits, its producer waits
+ * (with the same limit) for every copy it issued into its shared memory; those copies are
+ * built from tensor maps and sizes checked on the host, so they always complete, and a
+ * timeout there is reported separately (Q8ACT_ERR_DRAIN_TIMEOUT).
  */
 #ifndef Q8ACT_H
 #define Q8ACT_H
@@ -54,6 +57,8 @@ extern "C" {
 #define Q8ACT_ERR_WORKSPACE (-4)  /* workspace missing or smaller than required        */
 #define Q8ACT_ERR_DEVICE (-5)     /* current device is not an sm_103 (GB300) GPU       */
 #define Q8ACT_ERR_TIMEOUT (-6)    /* a kernel gave up waiting (see q8act_device_status) */
+#define Q8ACT_ERR_DRAIN_TIMEOUT (-7) /* a kernel gave up waiting for its own copies
+                                        before exiting (see q8act_device_status)       */
 #define Q8ACT_ERR_CUDA_BASE 1000  /* 1000 + cudaError_t                                */
 
 /* Largest supported k (values per row). */
@@ -182,9 +187,13 @@ int q8act_gemm_q8_0_preq(const void *w, const uint16_t *xqh, const float *xdt, f
  *   w, x, y, m, n, k, stream: as for q8act_gemm_q8_0; no workspace argument.
  * The activation quants and scales go into one fixed device array of Q8ACT_NOALLOC_WS_BYTES
  * that the library reserves on every GPU that loads it, until the process exits.  Returns
- * Q8ACT_ERR_WORKSPACE (nothing launched) when q8act_gemm_workspace_bytes(m, k) exceeds that
- * size (for k = 4096: m up to 2891).  The call never allocates or frees memory.  Its first
- * call on a device looks up the array's address (cudaGetSymbolAddress, with that device
+ * Q8ACT_ERR_WORKSPACE (nothing launched) when the quantized activation,
+ * q8act_gemm_workspace_bytes(m, k) - Q8ACT_GEMM_SPLIT_BYTES bytes, exceeds that size (for
+ * k = 4096: m up to 2891).  The split region is optional: when it fits in the rest of the
+ * array too (m * k up to about 2M at k = 4096) the GEMM may take its balanced schedule,
+ * otherwise every tile is done by one CTA.  The call never allocates or frees memory.  Its
+ * first call on a device (and the first after that device's CUDA context was torn down and
+ * created again) looks up the array's address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture.  All calls on a device share
  * the array and it keeps the previous call's contents; nothing in it needs to start at zero.
  * Calls that can overlap on the GPU (unordered streams) race on the array.
@@ -232,9 +241,11 @@ int q8act_gemm_q8_0_repacked(const uint16_t *wq16, const float *wdt, const float
 
 /*
  * Test hooks: export the exact per-block integer dots D[t][r][b] (int32, [m][n][k/32]) as
- * computed by the block-dot stage of the GEMV (its int8 dot-product path; 1 <= m <= 8) or of
- * the GEMM (its tensor-core path; m >= 1, activation in the MMQ layout).  The fold is
- * replaced by a store of D; everything before it is the production code path.
+ * computed by the block-dot stage of the GEMV (1 <= m <= 15, routed exactly as
+ * q8act_gemv_q8_0 routes: the tensor-core GEMV -- int8 mma.sync for m <= 8, binary16
+ * mma.sync for m = 9..15 -- where its shared-memory plan fits, else the dp4a GEMV) or of the
+ * GEMM (its tensor-core path; m >= 1, activation in the MMQ layout).  The fold is replaced by
+ * a store of D; everything before it is the production code path.
  */
 int q8act_debug_gemv_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m,
                                 int64_t n, int64_t k, void *stream);
@@ -289,9 +300,21 @@ int q8act_debug_gemv_q4_0_block_dots(const void *w, const int8_t *xq, int32_t *D
 
 /*
  * Synchronizes `stream`, then reads and clears the device-side status word that kernels set
- * when a pipeline wait times out.  Returns Q8ACT_OK, Q8ACT_ERR_TIMEOUT, or a CUDA error code.
+ * when a pipeline wait times out.  Returns Q8ACT_OK, Q8ACT_ERR_DRAIN_TIMEOUT (a producer gave
+ * up waiting for its own copies before its CTA exited), Q8ACT_ERR_TIMEOUT (a pipeline wait
+ * gave up and the kernel returned early; its outputs are incomplete), or a CUDA error code.
  */
 int q8act_device_status(void *stream);
+
+/*
+ * Test hook for the timeout path: launches one thread that waits, through the same bounded
+ * mbarrier wait the pipelines use, on a barrier that nothing ever arrives on, with a limit of
+ * limit_ns nanoseconds (1e3 .. 1e9) instead of the pipelines' two seconds.  The wait runs
+ * out, records a pipeline timeout in the status word (q8act_device_status then returns
+ * Q8ACT_ERR_TIMEOUT) and the kernel exits; nothing else is in flight, so the device stays
+ * usable.  Returns Q8ACT_ERR_DIMS for a limit out of range.
+ */
+int q8act_debug_wait_timeout(int64_t limit_ns, void *stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,8 @@ from ._lib import (  # noqa: F401  (re-exported ABI)
     q8act_quantize_q8_1, q8act_quantize_q8_1_mmq, q8act_strerror, q8act_version, strerror,
     q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots,
     q8act_gemv_q8_0_group, Q8ACT_GEMV_MAX_GROUP, q8act_quantize_q4_0, q8act_dequant_q4_0_f16,
-    q8act_gemv_q4_0, q8act_debug_gemv_q4_0_block_dots, q8act_gemv_workspace_bytes, q8act_gemv_q8_0_f32)
+    q8act_gemv_q4_0, q8act_debug_gemv_q4_0_block_dots, q8act_gemv_workspace_bytes, q8act_gemv_q8_0_f32,
+    q8act_debug_wait_timeout, Q8ACT_ERR_DRAIN_TIMEOUT)
 
 QK = 32
 Q8_0_BYTES = 34

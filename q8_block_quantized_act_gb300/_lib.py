@@ -25,6 +25,7 @@ Q8ACT_ERR_ALIGN = -3
 Q8ACT_ERR_WORKSPACE = -4
 Q8ACT_ERR_DEVICE = -5
 Q8ACT_ERR_TIMEOUT = -6
+Q8ACT_ERR_DRAIN_TIMEOUT = -7
 Q8ACT_ERR_CUDA_BASE = 1000
 Q8ACT_MAX_K = 65536
 Q8ACT_GEMV_MAX_M = 15
@@ -38,7 +39,7 @@ EXPORTED = (
     "q8act_gemm_q8_0_noalloc", "q8act_repack_q8_0", "q8act_repack_ldn",
     "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots", "q8act_gemv_q8_0_group",
     "q8act_quantize_q4_0", "q8act_dequant_q4_0_f16", "q8act_gemv_q4_0", "q8act_debug_gemv_q4_0_block_dots",
-    "q8act_gemv_workspace_bytes", "q8act_gemv_q8_0_f32",
+    "q8act_gemv_workspace_bytes", "q8act_gemv_q8_0_f32", "q8act_debug_wait_timeout",
 )
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 Q8ACT_GEMM_SPLIT_BYTES = 320 * 65536 + 160 * 64
@@ -93,6 +94,7 @@ def lib() -> ctypes.CDLL:
                 "q8act_debug_gemv_q4_0_block_dots": ([P, P, P, I64, I64, I64, P], I32),
                 "q8act_gemv_workspace_bytes": ([I64, I64], SZ),
                 "q8act_gemv_q8_0_f32": ([P, P, P, I64, I64, I64, P, SZ, P], I32),
+                "q8act_debug_wait_timeout": ([I64, P], I32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -243,3 +245,9 @@ def q8act_gemv_workspace_bytes(m, k) -> int:
 
 def q8act_gemv_q8_0_f32(w, x, y, m, n, k, ws, ws_bytes, stream=None) -> int:
     return lib().q8act_gemv_q8_0_f32(_p(w), _p(x), _p(y), m, n, k, _p(ws), ws_bytes, _s(stream))
+
+
+def q8act_debug_wait_timeout(limit_ns, stream=None) -> int:
+    """Test hook: a kernel whose bounded wait on a barrier nobody arrives on runs out after
+    limit_ns nanoseconds and records a pipeline timeout in the device status word."""
+    return lib().q8act_debug_wait_timeout(int(limit_ns), _s(stream))

@@ -15,6 +15,7 @@ __device__ int g_status;
 
 struct DeviceSlot {
     bool ready = false;
+    unsigned long long ctx = 0;   // context whose status-word address `info` holds
     int rc = Q8ACT_OK;
     q8::DeviceInfo info{};
 };
@@ -24,16 +25,18 @@ std::mutex g_mutex;
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? Q8ACT_OK : Q8ACT_ERR_CUDA_BASE + (int)e; }
 
-// Current device's info; checks once per device that it is an sm_103 GPU.
+// Current device's info; checks once per device (and context: the status word's address
+// belongs to the context) that it is an sm_103 GPU.
 int current_device(const q8::DeviceInfo **out)
 {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_rc(e);
     if (dev < 0 || dev >= kMaxDevices) return Q8ACT_ERR_DEVICE;
+    const unsigned long long ctx = q8::current_context_id();
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceSlot &s = g_slots[dev];
-    if (!s.ready) {
+    if (!s.ready || ctx == 0 || ctx != s.ctx) {
         int major = 0, minor = 0, sms = 0, smem = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
@@ -51,6 +54,7 @@ int current_device(const q8::DeviceInfo **out)
             s.info.status = static_cast<int *>(status);
             s.rc = Q8ACT_OK;
         }
+        s.ctx = ctx;
         s.ready = true;
     }
     *out = &s.info;
@@ -92,6 +96,7 @@ const char *q8act_strerror(int rc)
     case Q8ACT_ERR_WORKSPACE: return "workspace missing or too small";
     case Q8ACT_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
     case Q8ACT_ERR_TIMEOUT: return "a kernel timed out waiting in its pipeline";
+    case Q8ACT_ERR_DRAIN_TIMEOUT: return "a kernel timed out waiting for its own copies before exit";
     default:
         if (rc >= Q8ACT_ERR_CUDA_BASE) return cudaGetErrorString((cudaError_t)(rc - Q8ACT_ERR_CUDA_BASE));
         return "unknown error";
@@ -427,6 +432,30 @@ int q8act_debug_gemm_block_dots(const void *w, const uint16_t *xqh, int32_t *D, 
     return gemm_core(w, xqh, reinterpret_cast<const float *>(xqh), nullptr, D, m, n, k, nullptr, 0, false, stream);
 }
 
+// Test hook: one thread waits on an mbarrier that nothing arrives on, through the pipelines'
+// own bounded wait, until limit_ns passes; the wait then records STATUS_TIMEOUT.  Nothing
+// else is in flight (no copies, no tensor-core work), so the exit is clean.
+__global__ void wait_timeout_kernel(unsigned long long limit_ns, int *status)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        q8::mbar_init(&bar, 1);
+        q8::fence_mbar_init();
+        q8::mbar_wait_for(&bar, 0, status, limit_ns, q8::STATUS_TIMEOUT);
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(q8::smem_u32(&bar)) : "memory");
+    }
+}
+
+int q8act_debug_wait_timeout(int64_t limit_ns, void *stream)
+{
+    if (limit_ns < 1000 || limit_ns > 1000000000) return Q8ACT_ERR_DIMS;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((unsigned long long)limit_ns, dev->status);
+    return cuda_rc(cudaGetLastError());
+}
+
 int q8act_device_status(void *stream)
 {
     const q8::DeviceInfo *dev;
@@ -438,6 +467,7 @@ int q8act_device_status(void *stream)
     const int zero = 0;
     if ((e = cudaMemcpyFromSymbol(&host, g_status, sizeof(int))) != cudaSuccess) return cuda_rc(e);
     if (host && (e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int))) != cudaSuccess) return cuda_rc(e);
+    if (host & q8::STATUS_DRAIN_TIMEOUT) return Q8ACT_ERR_DRAIN_TIMEOUT;
     return host ? Q8ACT_ERR_TIMEOUT : Q8ACT_OK;
 }
 

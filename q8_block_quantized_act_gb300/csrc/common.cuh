@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "q8act.h"
 
@@ -22,7 +23,8 @@ constexpr int Q4_GROUP_BYTES = GROUP_BLOCKS * Q4_0_BYTES;   // 144 = 9 x 16 B
 constexpr int K_ALIGN = 256;      // k must be a multiple of this (row start 16 B aligned)
 
 // Device status word bits (read back by q8act_device_status).
-constexpr int STATUS_TIMEOUT = 1;
+constexpr int STATUS_TIMEOUT = 1;        // a pipeline wait gave up; the kernel left its loop
+constexpr int STATUS_DRAIN_TIMEOUT = 2;  // a wait for the CTA's own copies in flight gave up
 
 // A pipeline wait gives up after this long (the kernel then records STATUS_TIMEOUT and
 // leaves its loop instead of hanging the GPU).
@@ -121,20 +123,36 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 
 constexpr uint32_t WAIT_HINT_NS = 200000;
 
-// Wait until the phase with the given parity has completed.  Returns false (after setting
-// STATUS_TIMEOUT in *status) if that takes longer than WAIT_TIMEOUT_NS.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status)
+// Wait until the phase with the given parity has completed.  Returns false (after OR-ing
+// `bit` into *status) if that takes longer than limit_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, int *status,
+                                              unsigned long long limit_ns, int bit)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
+    const uint32_t hint = limit_ns < WAIT_HINT_NS ? (uint32_t)limit_ns : WAIT_HINT_NS;
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return true;
-        if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
-            atomicOr(status, STATUS_TIMEOUT);
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+        if (globaltimer() - t0 > limit_ns) {
+            atomicOr(status, bit);
             return false;
         }
     }
+}
+
+// A pipeline wait: gives up (STATUS_TIMEOUT) after WAIT_TIMEOUT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status)
+{
+    return mbar_wait_for(bar, parity, status, WAIT_TIMEOUT_NS, STATUS_TIMEOUT);
+}
+
+// A producer's final wait for its own copies into shared memory before the CTA exits: gives
+// up (STATUS_DRAIN_TIMEOUT, the more serious condition -- a copy may then still land in
+// shared memory after the CTA is gone) after WAIT_TIMEOUT_NS.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, int *status)
+{
+    return mbar_wait_for(bar, parity, status, WAIT_TIMEOUT_NS, STATUS_DRAIN_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -226,6 +244,38 @@ cudaError_t set_kernel_smem(int device, size_t smem)
     cudaFuncSetAttribute(Kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (cache) done[device].store(smem, std::memory_order_relaxed);
     return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------------------
+// Host: a process-unique id of the calling thread's current CUDA context (0 when there is
+// none yet or the driver entry points are unavailable).  Addresses of __device__ variables
+// belong to a context: a per-device cache of such an address is keyed on this id, so that a
+// context torn down and created again (cudaDeviceReset, a primary context released and
+// retained) gets its addresses looked up afresh.
+// ---------------------------------------------------------------------------------------
+inline unsigned long long current_context_id()
+{
+    typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+    typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) == cudaSuccess &&
+            r1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) == cudaSuccess &&
+            r2 == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+            get_id = reinterpret_cast<CtxGetIdFn>(q);
+        }
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
 }
 
 // Several weight matrices that share the activation, streamed by one launch (the census's

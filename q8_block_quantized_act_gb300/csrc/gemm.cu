@@ -347,11 +347,11 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
             }
             // Drain: never leave with a copy into this CTA's shared memory in flight.
             for (int i = issued_raw > RAW_STAGES ? issued_raw - RAW_STAGES : 0; i < issued_raw; ++i)
-                mbar_wait(&bars.raw_full[i % RAW_STAGES], (i / RAW_STAGES) & 1, status);
+                mbar_wait_drain(&bars.raw_full[i % RAW_STAGES], (i / RAW_STAGES) & 1, status);
             for (int i = issued_act > STAGES ? issued_act - STAGES : 0; i < issued_act; ++i)
-                mbar_wait(&bars.stage_full[i % STAGES], (i / STAGES) & 1, status);
+                mbar_wait_drain(&bars.stage_full[i % STAGES], (i / STAGES) & 1, status);
             for (int i = issued_sc > SC_STAGES ? issued_sc - SC_STAGES : 0; i < issued_sc; ++i)
-                mbar_wait(&bars.sc_full[i % SC_STAGES], (i / SC_STAGES) & 1, status);
+                mbar_wait_drain(&bars.sc_full[i % SC_STAGES], (i / SC_STAGES) & 1, status);
         }
     } else if (warp >= MMA_WARP) {
         // ------------------------------ MMA issuers ------------------------------
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
             }
             // All MMAs of both issuers have completed once this phase completes.
             tc_commit(bars.mma_done);
-            mbar_wait(bars.mma_done, 0, status);
+            mbar_wait_drain(bars.mma_done, 0, status);
         }
     } else if (warp < NUM_CONV_WARPS) {
         if (REPACKED) {

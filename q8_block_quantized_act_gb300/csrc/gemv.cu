@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
             }
             // Do not leave while copies into this CTA's shared memory may be in flight.
             for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
-                mbar_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+                mbar_wait_drain(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
         }
         return;
     }

@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ++issued;
             }
             for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
-                mbar_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+                mbar_wait_drain(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
         }
         return;
     }

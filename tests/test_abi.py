@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_version_and_strerror(L):
     assert q8.q8act_version() >= 100
-    for rc in (0, -1, -2, -3, -4, -5, -6, 1002):
+    for rc in (0, -1, -2, -3, -4, -5, -6, -7, 1002):
         assert isinstance(q8.strerror(rc), str) and q8.strerror(rc)
 
 
@@ -119,6 +119,15 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, 1, 8, 256, None, 1 << 20, S0), q8.Q8ACT_ERR_WORKSPACE),
     (lambda: q8.q8act_gemv_q8_0_f32(A, A, A, 1, 8, 256, A, 16, S0), q8.Q8ACT_ERR_WORKSPACE),
     (lambda: q8.q8act_gemv_q8_0_f32(A, MIS, A, 1, 8, 256, A, 1 << 20, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(None, A, A, 16, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(A, None, A, 16, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, None, 16, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, A, 0, 8, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, A, 16, 0, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, A, 16, 8, 300, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, A, 2892, 8, 4096, S0), q8.Q8ACT_ERR_WORKSPACE),
+    (lambda: q8.q8act_debug_wait_timeout(0, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_debug_wait_timeout(10 ** 10, S0), q8.Q8ACT_ERR_DIMS),
 ])
 def test_host_side_refusals(L, call, want):
     assert call() == want

@@ -107,7 +107,34 @@ def test_gemm_balanced_schedule(m, n, k):
     assert np.array_equal(y_bal.view(np.uint32), y_rp.view(np.uint32))
 
 
-@pytest.mark.parametrize("m,n", [(512, 4096), (512, 5152), (2048, 20480), (512, 64448)])
+def edge_and_sampled_rows(n, count, tail=40):
+    """A seeded sample of weight rows plus the last `tail` rows (the ragged last tile)."""
+    rows = np.union1d(sample_rows(n, count), np.arange(max(0, n - tail), n))
+    return rows.astype(np.int64)
+
+
+@pytest.mark.parametrize("repacked", [False, True])
+def test_gemm_block_dots_full_shape_sampled(repacked):
+    """m = 512, 4096 -> 5152 (164 tiles, the last one ragged): the production block dots of the
+    raw and the repacked GEMM at full size, exact on a seeded row sample and the last rows."""
+    ensure_built()
+    m, n, k = 512, 5152, 4096
+    _, x, wb, xq, _ = problem(m, n, k, "token_scales")
+    xqh, _ = q8.quantize_q8_1_mmq(cuda(x))
+    D = torch.full((m, n, k // 32), -7, dtype=torch.int32, device="cuda")
+    if repacked:
+        wq16, wdt = q8.repack_q8_0(cuda(wb), n, k)
+        q8.check(q8.q8act_debug_gemm_repacked_block_dots(wq16, wdt, xqh, D, m, n, k))
+    else:
+        q8.check(q8.q8act_debug_gemm_block_dots(cuda(wb), xqh, D, m, n, k))
+    device_ok()
+    rows = edge_and_sampled_rows(n, 256)
+    got = host(D[:, torch.from_numpy(rows).cuda(), :])
+    assert np.array_equal(got, oracle.block_dots(wb, xq, k, rows=rows))
+
+
+@pytest.mark.parametrize("m,n", [(512, 4096), (512, 5152), (512, 20480), (2048, 20480), (512, 64448),
+                                 (2048, 64448)])
 def test_gemm_serving_shapes_sampled(m, n):
     """The prefill shapes at full size: every token, a seeded sample of weight rows."""
     ensure_built()

@@ -51,6 +51,22 @@ def test_gemv_block_dots_exact(m, n, k):
     assert np.array_equal(host(D), oracle.block_dots(wb, xq, k))
 
 
+@pytest.mark.parametrize("m", [1, 8, 15])
+def test_gemv_block_dots_full_shape_sampled(m):
+    """4096 -> 64448 (the LM-head half; its last row chunk is ragged): the production block
+    dots of the GEMV at full size -- dp4a at m = 1, int8 mma.sync at m = 8, binary16 mma.sync
+    at m = 15 -- exact on a seeded row sample plus the last 40 rows."""
+    ensure_built()
+    n, k = 64448, 4096
+    _, _, wb, xq, _ = problem(m, n, k, "outliers")
+    D = torch.full((m, n, k // 32), -7, dtype=torch.int32, device="cuda")
+    q8.check(q8.q8act_debug_gemv_block_dots(cuda(wb), cuda(xq), D, m, n, k))
+    device_ok()
+    rows = np.union1d(sample_rows(n, 256), np.arange(n - 40, n)).astype(np.int64)
+    got = host(D[:, torch.from_numpy(rows).cuda(), :])
+    assert np.array_equal(got, oracle.block_dots(wb, xq, k, rows=rows))
+
+
 @pytest.mark.parametrize("n,k", [(4096, 4096), (4096, 1280), (20480, 4096), (64448, 4096)])
 def test_gemv_serving_shapes_batch_invariant(n, k):
     """decode == verify: token t's output is bitwise the same for every m of the GEMV."""

@@ -60,7 +60,8 @@ def test_gemm_repacked_matches_oracle_and_raw(m, n, k, kind):
     assert np.array_equal(y_whole.view(np.uint32), y_raw.view(np.uint32))
 
 
-@pytest.mark.parametrize("m,n", [(512, 4096), (2048, 20480)])
+@pytest.mark.parametrize("m,n", [(512, 4096), (512, 5152), (512, 20480), (2048, 20480), (512, 64448),
+                                 (2048, 64448)])
 def test_gemm_repacked_serving_shapes_sampled(m, n):
     ensure_built()
     k = 4096

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import q8_block_quantized_act_gb300 as q8
-from gpu_util import RTOL, assert_within_tolerance, cuda, ensure_built, host, problem
+from gpu_util import RTOL, assert_within_tolerance, cuda, ensure_built, host, problem, sample_rows
 
 
 @pytest.mark.gpu
@@ -36,6 +36,35 @@ def test_noalloc_gemm_matches_workspace_gemm_twice():
         xq, xd = oracle.quantize_q8_1(x)
         _, y64, S = oracle.matmul(wb, xq, xd, k)
         a, b = host(y_na), host(y_ref)
+        err = np.abs(a.astype(np.float64) - b.astype(np.float64))
+        assert np.all(err <= RTOL * S), float((err / np.maximum(S, 1e-300)).max())
+        assert_within_tolerance(a, y64, S)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("m", [1024, 2891])
+def test_noalloc_gemm_prefill_sizes(m):
+    """Prefill sizes where the split region no longer fits beside the quantized activation
+    (every tile then done by one CTA), up to the largest m the scratch holds at k = 4096: the
+    result matches the workspace entry point's within the parity tolerance, twice in a row."""
+    ensure_built()
+    n, k = 640, 4096
+    _, x1, wb, _, _ = problem(m, n, k, "token_scales", xseed=1)
+    x2 = problem(m, n, k, "outliers", xseed=5)[1]
+    w_d = cuda(wb)
+    ws = q8.gemm_workspace(m, k, w_d.device)
+    rows = sample_rows(n, 96)
+    for x in (x1, x2):
+        x_d = cuda(x)
+        y_ref = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        y_na = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+        q8.check(q8.q8act_gemm_q8_0(w_d, x_d, y_ref, m, n, k, ws, ws.numel()))
+        q8.check(q8.q8act_gemm_q8_0_noalloc(w_d, x_d, y_na, m, n, k))
+        torch.cuda.synchronize()
+        q8.device_status()
+        xq, xd = oracle.quantize_q8_1(x)
+        _, y64, S = oracle.matmul(wb, xq, xd, k, rows=rows)
+        a, b = host(y_na)[:, rows], host(y_ref)[:, rows]
         err = np.abs(a.astype(np.float64) - b.astype(np.float64))
         assert np.all(err <= RTOL * S), float((err / np.maximum(S, 1e-300)).max())
         assert_within_tolerance(a, y64, S)
