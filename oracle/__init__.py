@@ -19,6 +19,11 @@ it with gcc and exposes numpy-facing wrappers:
     dequant_q4_0_f16(w, k)            O7b Q4_0 -> fp16 bits [n, k]
     block_dots_q4_0(w, xq, k, rows)   O7c exact int32 D[t, r, b] of Q4_0 weights
     matmul_q4_0(w, xq, xd, k, rows)   O7d (y32, y64, S) over Q4_0 weights
+    f64_to_f16(x)                     O8  binary64 -> binary16 bits (round to nearest even)
+    dequant_kq_f16(fmt, w, k)         O8a K-quant superblocks -> fp16 bits [n, k]
+                                          (fmt: "q6_k", "q4_k", "q5_k")
+    block_dots_kq(fmt, w, xq, k, rows)  O8b exact int32 per-32-block integers [t, r, b]
+    matmul_kq(fmt, w, xq, xd, k, rows)  O8c (y32, y64, S) over K-quant weights
 
 Each C function cites the page passage it follows (memra-engine docs.rs pages:
 accprobe_bench.rs, decode_kernel_census.rs, f16_ffi.rs).
@@ -42,6 +47,8 @@ _LIB = None
 QK = 32
 Q8_0_BYTES = 34
 Q4_0_BYTES = 18
+QK_K = 256
+KQ_FORMATS = {"q6_k": (6, 210), "q4_k": (4, 144), "q5_k": (5, 176)}   # code, superblock bytes
 
 
 def build(force: bool = False) -> str:
@@ -73,11 +80,18 @@ def _bind(lib):
     lib.oracle_dequant_q4_0_f16.argtypes = [P, P, I64, I64]
     lib.oracle_block_dots_q4_0.argtypes = [P, P, P, I64, I64, I64, P, I64]
     lib.oracle_matmul_q4_0.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P, P]
+    I32 = ctypes.c_int
+    lib.oracle_f64_to_f16.argtypes = [ctypes.c_double]
+    lib.oracle_f64_to_f16.restype = ctypes.c_uint16
+    lib.oracle_dequant_kq_f16.argtypes = [I32, P, P, I64, I64]
+    lib.oracle_block_dots_kq.argtypes = [I32, P, P, P, I64, I64, I64, P, I64]
+    lib.oracle_matmul_kq.argtypes = [I32, P, P, P, I64, I64, I64, P, I64, P, P, P]
     for name in ("oracle_f32_to_f16_array", "oracle_f16_to_f32_array",
                  "oracle_quantize_q8_1", "oracle_quantize_q8_0", "oracle_block_dots",
                  "oracle_matmul", "oracle_dequant_f16", "oracle_repack_q8_0",
                  "oracle_quantize_q4_0", "oracle_dequant_q4_0_f16", "oracle_block_dots_q4_0",
-                 "oracle_matmul_q4_0"):
+                 "oracle_matmul_q4_0", "oracle_dequant_kq_f16", "oracle_block_dots_kq",
+                 "oracle_matmul_kq"):
         getattr(lib, name).restype = None
     return lib
 
@@ -270,11 +284,76 @@ def matmul_q4_0(w: np.ndarray, xq: np.ndarray, xd: np.ndarray, k: int, rows=None
     return y32, y64, S
 
 
+def _kq(fmt: str):
+    if fmt not in KQ_FORMATS:
+        raise ValueError(f"unknown K-quant format {fmt!r}")
+    return KQ_FORMATS[fmt]
+
+
+def _check_kk(k: int) -> None:
+    if k <= 0 or k % QK_K:
+        raise ValueError(f"k must be a positive multiple of {QK_K}, got {k}")
+
+
+def f64_to_f16(x, _o: Oracle | None = None) -> np.ndarray:
+    """O8: element-wise binary64 -> binary16 bits (uint16), round to nearest even."""
+    x = np.asarray(x, dtype=np.float64)
+    f = (_o or _DEFAULT).lib().oracle_f64_to_f16
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def dequant_kq_f16(fmt: str, w: np.ndarray, k: int, _o: Oracle | None = None) -> np.ndarray:
+    """O8a: K-quant superblock bytes (fmt "q6_k", "q4_k" or "q5_k") -> fp16 bits uint16 [n, k],
+    each the correctly rounded binary16 of the weight's exact value."""
+    code, sbytes = _kq(fmt)
+    _check_kk(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    n = w.size // (k // QK_K * sbytes)
+    out = np.empty((n, k), dtype=np.uint16)
+    (_o or _DEFAULT).lib().oracle_dequant_kq_f16(code, _ptr(w), _ptr(out), n, k)
+    return out
+
+
+def block_dots_kq(fmt: str, w: np.ndarray, xq: np.ndarray, k: int, rows=None, _o: Oracle | None = None):
+    """O8b: the exact int32 integers of every 32-wide block [t, j, b] that the fold consumes
+    (Q6_K: the scale-weighted sum of its two 16-wide dots; Q4_K / Q5_K: sum q * xq)."""
+    code, sbytes = _kq(fmt)
+    _check_kk(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    n = w.size // (k // QK_K * sbytes)
+    m = xq.size // k
+    rows, nr = _rows_arg(rows, n)
+    D = np.empty((m, nr, k // QK), dtype=np.int32)
+    (_o or _DEFAULT).lib().oracle_block_dots_kq(code, _ptr(w), _ptr(xq), _ptr(D), m, n, k, _ptr(rows), nr)
+    return D
+
+
+def matmul_kq(fmt: str, w: np.ndarray, xq: np.ndarray, xd: np.ndarray, k: int, rows=None,
+              _o: Oracle | None = None):
+    """O8c: returns (y32 f32 [m, nr], y64 f64 [m, nr], S f64 [m, nr]) over K-quant weights."""
+    code, sbytes = _kq(fmt)
+    _check_kk(k)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xd = np.ascontiguousarray(xd, dtype=np.float32)
+    n = w.size // (k // QK_K * sbytes)
+    m = xq.size // k
+    rows, nr = _rows_arg(rows, n)
+    y32 = np.empty((m, nr), dtype=np.float32)
+    y64 = np.empty((m, nr), dtype=np.float64)
+    S = np.empty((m, nr), dtype=np.float64)
+    (_o or _DEFAULT).lib().oracle_matmul_kq(code, _ptr(w), _ptr(xq), _ptr(xd), m, n, k, _ptr(rows), nr,
+                                            _ptr(y32), _ptr(y64), _ptr(S))
+    return y32, y64, S
+
+
 _DEFAULT = Oracle()
 
 _PUBLIC = ("f32_to_f16", "f16_to_f32", "quantize_q8_0", "quantize_q8_1", "block_dots",
            "matmul", "dequant_f16", "repack_q8_0", "quantize_q4_0", "dequant_q4_0_f16",
-           "block_dots_q4_0", "matmul_q4_0")
+           "block_dots_q4_0", "matmul_q4_0", "f64_to_f16", "dequant_kq_f16", "block_dots_kq",
+           "matmul_kq")
 
 
 def bound(o: Oracle):

@@ -410,3 +410,235 @@ void oracle_matmul_q4_0(const uint8_t *w, const int8_t *xq, const float *xd, int
                 S[t * nr + j] = abs64;
         }
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* O8: K-quant superblocks, [f16_ffi] memra_q6_K_dequant_f16 / memra_q4_K_dequant_f16 /   */
+/* memra_q5_K_dequant_f16 ("GGUF Q6_K 210B / Q4_K 144B / Q5_K 176B superblocks ->         */
+/* row-major fp16 mirror").  The page names the GGUF formats and their superblock sizes;  */
+/* the layouts read here are those formats' (256 weights per superblock):                 */
+/*                                                                                        */
+/* Q6_K (210 bytes): ql[128] at +0, qh[64] at +128, int8 scales[16] at +192, fp16 d at    */
+/*   +208.  Weight e (0..255) lies in half h = e / 128, at p = e % 128 = 32 g + l (g 0..3, */
+/*   l 0..31); its 6-bit code q = (low 4 bits: the low nibble (g < 2) or high nibble       */
+/*   (g >= 2) of ql[64 h + 32 (g % 2) + l]) + 16 * ((qh[32 h + l] >> 2 g) & 3), and its    */
+/*   value is d * scales[e / 16] * (q - 32).                                               */
+/* Q4_K (144 bytes): fp16 d at +0, fp16 dmin at +2, 12 scale bytes at +4, qs[128] at +16.  */
+/*   Sub-block j (0..7) of 32 weights has a 6-bit scale sc_j and a 6-bit min m_j:          */
+/*   j < 4:  sc = s[j] & 63,  m = s[j + 4] & 63;                                           */
+/*   j >= 4: sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4),                                */
+/*           m  = (s[j + 4] >> 4) | ((s[j] >> 6) << 4).                                    */
+/*   Weight e = 64 g + 32 u + l (g 0..3, u 0..1) is in sub-block j = 2 g + u, its 4-bit    */
+/*   code q is the low (u = 0) or high (u = 1) nibble of qs[32 g + l], and its value is   */
+/*   d * sc_j * q - dmin * m_j.                                                            */
+/* Q5_K (176 bytes): as Q4_K with qh[32] at +16 and qs[128] at +48; the code gains a fifth */
+/*   bit, q += 16 * ((qh[l] >> j) & 1).                                                    */
+/*                                                                                        */
+/* Readings (the pages are silent): the fp16 mirror is the correctly rounded binary16 of   */
+/* each weight's exact value (as for Q8_0, where the f32 product is already exact); the    */
+/* matmul with the q8_1 activation takes, per 32-wide activation block b, exact integers   */
+/* -- Q6_K: E_b = sc_2i * sum_{first 16} (q - 32) xq + sc_2i+1 * sum_{last 16} (q - 32) xq */
+/* (i = b % 8); Q4_K / Q5_K: D_b = sum q xq and X_b = sum xq -- and folds them with the    */
+/* block's scales: y += d d_a E_b, or y += d_a (d sc_j D_b - dmin m_j X_b).                */
+/* ------------------------------------------------------------------------------------ */
+#define QK_K 256
+#define Q6_K_BYTES 210
+#define Q4_K_BYTES 144
+#define Q5_K_BYTES 176
+
+enum { KQ_Q6_K = 6, KQ_Q4_K = 4, KQ_Q5_K = 5 };
+
+static int kq_bytes(int fmt)
+{
+    return fmt == KQ_Q6_K ? Q6_K_BYTES : fmt == KQ_Q4_K ? Q4_K_BYTES : Q5_K_BYTES;
+}
+
+static float f16_at(const uint8_t *p)
+{
+    return oracle_f16_to_f32((uint16_t)(p[0] | (p[1] << 8)));
+}
+
+/* The 6-bit scale and min of sub-block j of a Q4_K / Q5_K superblock (12 scale bytes s). */
+static void k4_scale_min(const uint8_t *s, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *m = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* The unsigned code of weight e of a superblock (Q6_K: 0..63, Q4_K: 0..15, Q5_K: 0..31). */
+static int kq_code(int fmt, const uint8_t *sb, int e)
+{
+    if (fmt == KQ_Q6_K) {
+        int h = e / 128, p = e % 128, g = p / 32, l = p % 32;
+        int byte = sb[64 * h + 32 * (g % 2) + l];
+        int lo = (g < 2) ? (byte & 15) : (byte >> 4);
+        int hi = (sb[128 + 32 * h + l] >> (2 * g)) & 3;
+        return lo + 16 * hi;
+    }
+    int g = e / 64, u = (e / 32) % 2, l = e % 32;
+    const uint8_t *qs = sb + (fmt == KQ_Q4_K ? 16 : 48);
+    int byte = qs[32 * g + l];
+    int q = u ? (byte >> 4) : (byte & 15);
+    if (fmt == KQ_Q5_K)
+        q += 16 * ((sb[16 + l] >> (2 * g + u)) & 1);
+    return q;
+}
+
+/* The exact value of weight e of a superblock, in double (every such value is an integer
+   multiple of 2^-24 below 2^28 in magnitude, so double holds it exactly). */
+static double kq_value(int fmt, const uint8_t *sb, int e)
+{
+    int q = kq_code(fmt, sb, e);
+    if (fmt == KQ_Q6_K) {
+        int sc = (int)(int8_t)sb[192 + e / 16];
+        return (double)f16_at(sb + 208) * (double)sc * (double)(q - 32);
+    }
+    int sc, m;
+    k4_scale_min(sb + 4, e / 32, &sc, &m);
+    return (double)f16_at(sb) * (double)sc * (double)q - (double)f16_at(sb + 2) * (double)m;
+}
+
+/* binary64 -> binary16, round to nearest even (gradual underflow, overflow to infinity),
+   written from the two formats' definitions like oracle_f32_to_f16. */
+uint16_t oracle_f64_to_f16(double x)
+{
+    uint64_t b;
+    memcpy(&b, &x, sizeof b);
+    uint16_t sign = (uint16_t)((b >> 48) & 0x8000u);
+    uint32_t ebits = (uint32_t)((b >> 52) & 0x7ffu);
+    uint64_t frac = b & 0xfffffffffffffull;
+    if (ebits == 0x7ffu)
+        return frac ? (uint16_t)(sign | 0x7e00u) : (uint16_t)(sign | 0x7c00u);
+    if (ebits == 0)
+        return sign;                                  /* zero or < 2^-1022 */
+    int e = (int)ebits - 1023;                        /* |x| = sig * 2^(e - 52) */
+    uint64_t sig = frac | (1ull << 52);
+    if (e > 15)
+        return (uint16_t)(sign | 0x7c00u);
+    int shift = (e >= -14) ? 42 : (28 - e);           /* bits dropped: result unit 2^-24 below 2^-14 */
+    if (shift > 53)
+        return sign;                                  /* |x| < 2^-25 */
+    uint64_t q = sig >> shift;
+    uint64_t rem = sig & ((1ull << shift) - 1ull);
+    uint64_t half = 1ull << (shift - 1);
+    if (rem > half || (rem == half && (q & 1u)))
+        q += 1u;
+    uint64_t enc = (e >= -14) ? ((uint64_t)(e + 14) << 10) + q : q;
+    if (enc > 0x7c00u)
+        enc = 0x7c00u;
+    return (uint16_t)(sign | (uint16_t)enc);
+}
+
+/* O8a: K-quant -> fp16 row-major dequant: w16[r][e] = fp16_rn(exact value of weight e). */
+void oracle_dequant_kq_f16(int fmt, const uint8_t *w, uint16_t *out, int64_t n, int64_t k)
+{
+    int64_t ns = k / QK_K, sbytes = kq_bytes(fmt);
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t s = 0; s < ns; s++) {
+            const uint8_t *sb = w + (r * ns + s) * sbytes;
+            for (int e = 0; e < QK_K; e++)
+                out[r * k + s * QK_K + e] = oracle_f64_to_f16(kq_value(fmt, sb, e));
+        }
+}
+
+/* The exact integers of 32-wide activation block i (0..7) of a superblock: *E for Q6_K;
+   *D = sum q xq and *X = sum xq for Q4_K / Q5_K. */
+static void kq_block_ints(int fmt, const uint8_t *sb, int i, const int8_t *xq, int32_t *E, int32_t *D, int32_t *X)
+{
+    int32_t d0 = 0, d1 = 0, x = 0;
+    for (int l = 0; l < QK; l++) {
+        int e = 32 * i + l;
+        int q = kq_code(fmt, sb, e);
+        x += xq[l];
+        if (fmt == KQ_Q6_K) {
+            if (l < 16)
+                d0 += (q - 32) * xq[l];
+            else
+                d1 += (q - 32) * xq[l];
+        } else {
+            d0 += q * xq[l];
+        }
+    }
+    if (fmt == KQ_Q6_K) {
+        *E = (int32_t)(int8_t)sb[192 + 2 * i] * d0 + (int32_t)(int8_t)sb[192 + 2 * i + 1] * d1;
+        *D = 0;
+    } else {
+        *E = 0;
+        *D = d0;
+    }
+    *X = x;
+}
+
+/* O8b: the exact per-block integers the fold consumes, [t][j][b] for the selected rows:
+   Q6_K: E_b; Q4_K / Q5_K: D_b (X_b depends on the activation only). */
+void oracle_block_dots_kq(int fmt, const uint8_t *w, const int8_t *xq, int32_t *out, int64_t m,
+                          int64_t n, int64_t k, const int64_t *rows, int64_t nrows)
+{
+    int64_t ns = k / QK_K, nb = k / QK, sbytes = kq_bytes(fmt);
+    int64_t nr = rows ? nrows : n;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t j = 0; j < nr; j++) {
+            int64_t r = rows ? rows[j] : j;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *sb = w + (r * ns + b / 8) * sbytes;
+                int32_t E, D, X;
+                kq_block_ints(fmt, sb, (int)(b % 8), xq + t * k + b * QK, &E, &D, &X);
+                out[(t * nr + j) * nb + b] = (fmt == KQ_Q6_K) ? E : D;
+            }
+        }
+}
+
+/* O8c: the fold over K-quant weights.  Per 32-wide block b (ascending):
+     Q6_K:          term = d * d_a * E_b
+     Q4_K / Q5_K:   term = d_a * (d * sc_j * D_b - dmin * m_j * X_b)
+   y32: f32, each operation rounded, in the order written; y64: double; S: the sum over
+   blocks of the magnitudes of the term's products (d d_a E, or |d_a d sc D| + |d_a dmin m X|). */
+void oracle_matmul_kq(int fmt, const uint8_t *w, const int8_t *xq, const float *xd, int64_t m,
+                      int64_t n, int64_t k, const int64_t *rows, int64_t nrows, float *y32,
+                      double *y64, double *S)
+{
+    int64_t ns = k / QK_K, nb = k / QK, sbytes = kq_bytes(fmt);
+    int64_t nr = rows ? nrows : n;
+    for (int64_t t = 0; t < m; t++)
+        for (int64_t j = 0; j < nr; j++) {
+            int64_t r = rows ? rows[j] : j;
+            float acc32 = 0.0f;
+            double acc64 = 0.0, abs64 = 0.0;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *sb = w + (r * ns + b / 8) * sbytes;
+                int i = (int)(b % 8);
+                int32_t E, D, X;
+                kq_block_ints(fmt, sb, i, xq + t * k + b * QK, &E, &D, &X);
+                float da = xd[t * nb + b];
+                if (fmt == KQ_Q6_K) {
+                    float d = f16_at(sb + 208);
+                    float s = d * da;
+                    acc32 = acc32 + s * (float)E;
+                    double term = (double)d * (double)da * (double)E;
+                    acc64 += term;
+                    abs64 += fabs(term);
+                } else {
+                    int sc, mn;
+                    k4_scale_min(sb + 4, i, &sc, &mn);
+                    float d = f16_at(sb), dmin = f16_at(sb + 2);
+                    float dsc = d * (float)sc, dmm = dmin * (float)mn;
+                    float v = dsc * (float)D - dmm * (float)X;
+                    acc32 = acc32 + da * v;
+                    double p1 = (double)da * (double)d * (double)sc * (double)D;
+                    double p2 = (double)da * (double)dmin * (double)mn * (double)X;
+                    acc64 += p1 - p2;
+                    abs64 += fabs(p1) + fabs(p2);
+                }
+            }
+            if (y32)
+                y32[t * nr + j] = acc32;
+            if (y64)
+                y64[t * nr + j] = acc64;
+            if (S)
+                S[t * nr + j] = abs64;
+        }
+}

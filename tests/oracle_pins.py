@@ -387,6 +387,113 @@ def pin_q4_0_dots_and_fold_bruteforce(o, seed=12):
         assert np.array_equal(sy32, y32[:, rows]) and np.array_equal(sy64, y64[:, rows])
 
 
+# ---------------------------------------------------------------------------------------
+# K-quant superblocks (Q6_K, Q4_K, Q5_K): tests/golden/kquant_superblocks.json holds one
+# superblock of each format built from chosen codes and scales (the encoding direction of
+# the GGUF layouts), with hand-worked values; the oracle must read those choices back.
+# ---------------------------------------------------------------------------------------
+def _kq_golden():
+    return _golden("kquant_superblocks.json")["superblocks"]
+
+
+def _kq_expected(sb):
+    """The exact values of the golden superblock's 256 weights, from its chosen codes and
+    scales (float64: every one is exact)."""
+    e = np.arange(256)
+    codes = np.array(sb["codes"], dtype=np.float64)
+    if sb["format"] == "q6_k":
+        return sb["d"] * np.array(sb["scales"], dtype=np.float64)[e // 16] * (codes - 32)
+    sc = np.array(sb["sub_scales"], dtype=np.float64)[e // 32]
+    mn = np.array(sb["sub_mins"], dtype=np.float64)[e // 32]
+    return sb["d"] * sc * codes - sb["dmin"] * mn
+
+
+def _kq_bytes(sb):
+    return np.frombuffer(bytes.fromhex(sb["bytes"]), dtype=np.uint8).reshape(1, -1).copy()
+
+
+def pin_kq_golden_dequant(o):
+    """The fp16 mirror of each golden superblock: numpy's binary16 rounding of the chosen
+    exact values, and the hand-worked encodings (including round-to-even ties)."""
+    for sb in _kq_golden():
+        h = o.dequant_kq_f16(sb["format"], _kq_bytes(sb), 256)[0]
+        want = _kq_expected(sb).astype(np.float16).view(np.uint16)
+        assert np.array_equal(h, want), sb["format"]
+        for w in sb["worked"]:
+            assert abs(_kq_expected(sb)[w["e"]] - w["value"]) == 0.0, (sb["format"], w["e"])
+            if "f16" in w:
+                assert int(h[w["e"]]) == int(w["f16"], 16), (sb["format"], w["e"])
+
+
+def pin_kq_golden_onehot(o):
+    """Each weight read alone through the block integers and the fold: with the one-hot
+    activation of element e (quant 1, scale 1) the block integer is the weight's scaled code
+    (Q6_K: scale * (code - 32); Q4_K / Q5_K: the code) and y64 is the weight's exact value."""
+    for sb in _kq_golden():
+        fmt = sb["format"]
+        wb = _kq_bytes(sb)
+        xq = np.eye(256, dtype=np.int8)
+        xd = np.ones((256, 8), dtype=np.float32)
+        D = o.block_dots_kq(fmt, wb, xq, 256)[:, 0, :]
+        codes = np.array(sb["codes"], dtype=np.int64)
+        e = np.arange(256)
+        if fmt == "q6_k":
+            want = np.array(sb["scales"], dtype=np.int64)[e // 16] * (codes - 32)
+        else:
+            want = codes
+        got = D[e, e // 32]
+        assert np.array_equal(got.astype(np.int64), want), fmt
+        mask = np.ones_like(D, dtype=bool)
+        mask[e, e // 32] = False
+        assert not D[mask].any(), fmt
+        _, y64, S = o.matmul_kq(fmt, wb, xq, xd, 256)
+        assert np.array_equal(y64[:, 0], _kq_expected(sb)), fmt
+        assert np.all(S[:, 0] >= np.abs(y64[:, 0]))
+
+
+def pin_kq_fold_bruteforce(o, seed=13):
+    """y64 over rows of golden superblocks (repeated, and with one superblock's scale bytes
+    changed) equals the plain float64 dot of the exact weights with the dequantized
+    activation; y32 is within the f32 summation bound; a row subset gives the same rows."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for sb in _kq_golden():
+        fmt = sb["format"]
+        one = _kq_bytes(sb)[0]
+        vals = _kq_expected(sb)
+        k = 512
+        row = np.concatenate([one, one])
+        w = np.stack([row, row[::1]]).copy()
+        m = 3
+        x = rng.standard_normal((m, k)).astype(np.float32) * np.float32(3.0)
+        xq, xd = o.quantize_q8_1(x)
+        _, y64, S = o.matmul_kq(fmt, w, xq, xd, k)
+        wv = np.concatenate([vals, vals])
+        xv = (xd.astype(np.float64)[:, :, None] * xq.astype(np.float64).reshape(m, k // QK, QK)).reshape(m, k)
+        plain = xv @ wv
+        assert np.all(np.abs(y64[:, 0] - plain) <= 1e-12 * np.maximum(S[:, 0], 1e-300)), fmt
+        y32, _, _ = o.matmul_kq(fmt, w, xq, xd, k)
+        assert np.all(np.abs(y32.astype(np.float64) - y64) <= (k // QK + 4) * 2.0 ** -23 * S + 1e-30), fmt
+        sy32, sy64, _ = o.matmul_kq(fmt, w, xq, xd, k, rows=np.array([1], dtype=np.int64))
+        assert np.array_equal(sy64[:, 0], y64[:, 1]) and np.array_equal(sy32[:, 0], y32[:, 1])
+
+
+def pin_f64_to_f16_vs_numpy(o, seed=14):
+    """binary64 -> binary16 against numpy's own conversion: random values over the whole
+    binary16 range (and past it), every midpoint between neighbouring binary16 values of a
+    few binades and its neighbours one double ulp away, zeros, infinities."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal(20000) * np.exp2(rng.integers(-28, 18, size=20000))
+    h = np.arange(0, 0x7c00, 97, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2
+    x = np.concatenate([x, mid, np.nextafter(mid, 0), np.nextafter(mid, np.inf), -mid,
+                        [0.0, -0.0, np.inf, -np.inf, 65504.0, 65519.99, 65520.0, 2.0 ** -25, 3 * 2.0 ** -26]])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(o.f64_to_f16(x), want)
+
+
 ALL_PINS = [
     pin_f16_decode_exhaustive,
     pin_f16_encode_vs_numpy,
@@ -404,4 +511,8 @@ ALL_PINS = [
     pin_q4_0_dequant_vs_numpy,
     pin_q4_0_writer_invariants,
     pin_q4_0_dots_and_fold_bruteforce,
+    pin_kq_golden_dequant,
+    pin_kq_golden_onehot,
+    pin_kq_fold_bruteforce,
+    pin_f64_to_f16_vs_numpy,
 ]

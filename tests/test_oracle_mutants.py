@@ -42,6 +42,22 @@ MUTANTS = {
                               "for (int64_t b = 0; b < nb - 1; b++) {\n                const uint8_t *blk = q4_0_block_ptr(w, r, b, nb);\n                int32_t dot"),
     "q4_dequant_unrounded_scale": ("out[r * k + b * QK + i] = oracle_f32_to_f16(dw * (float)q4_0_value(blk, i));",
                                    "out[r * k + b * QK + i] = oracle_f32_to_f16(dw * 1.0001f * (float)q4_0_value(blk, i));"),
+    # K-quant superblocks
+    "q6k_scale_per_32": ("int sc = (int)(int8_t)sb[192 + e / 16];", "int sc = (int)(int8_t)sb[192 + e / 32];"),
+    "q6k_qh_shift": ("int hi = (sb[128 + 32 * h + l] >> (2 * g)) & 3;", "int hi = (sb[128 + 32 * h + l] >> g) & 3;"),
+    "q6k_ql_halves": ("int byte = sb[64 * h + 32 * (g % 2) + l];", "int byte = sb[64 * h + 32 * (g / 2) + l];"),
+    "q6k_offset_31": ("return (double)f16_at(sb + 208) * (double)sc * (double)(q - 32);",
+                      "return (double)f16_at(sb + 208) * (double)sc * (double)(q - 31);"),
+    "q6k_block_scale_pair": ("*E = (int32_t)(int8_t)sb[192 + 2 * i] * d0 + (int32_t)(int8_t)sb[192 + 2 * i + 1] * d1;",
+                             "*E = (int32_t)(int8_t)sb[192 + i] * d0 + (int32_t)(int8_t)sb[192 + i + 8] * d1;"),
+    "k4_high_bits_swapped": ("*sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);", "*sc = (s[j + 4] & 15) | ((s[j] >> 6) << 4);"),
+    "k4_scale_min_nibbles": ("*m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);", "*m = (s[j + 4] & 15) | ((s[j] >> 6) << 4);"),
+    "k4_nibble_order": ("int q = u ? (byte >> 4) : (byte & 15);", "int q = u ? (byte & 15) : (byte >> 4);"),
+    "k5_qh_bit": ("q += 16 * ((sb[16 + l] >> (2 * g + u)) & 1);", "q += 16 * ((sb[16 + l] >> (g + 4 * u)) & 1);"),
+    "k4_min_added": ("return (double)f16_at(sb) * (double)sc * (double)q - (double)f16_at(sb + 2) * (double)m;",
+                     "return (double)f16_at(sb) * (double)sc * (double)q + (double)f16_at(sb + 2) * (double)m;"),
+    "k4_fold_min_dropped": ("float v = dsc * (float)D - dmm * (float)X;", "float v = dsc * (float)D;"),
+    "f64_f16_subnormal_shift": ("int shift = (e >= -14) ? 42 : (28 - e);", "int shift = (e >= -14) ? 42 : (29 - e);"),
 }
 
 
