@@ -299,6 +299,56 @@ int q8act_debug_gemv_q4_0_block_dots(const void *w, const int8_t *xq, int32_t *D
                                      int64_t n, int64_t k, void *stream);
 
 /*
+ * K-quant weights -- the GGUF superblocks named by memra-engine 0.81.0 f16_ffi.rs
+ * (memra_q6_K_dequant_f16: "GGUF Q6_K 210B superblocks", memra_q4_K_dequant_f16: "Q4_K 144B",
+ * memra_q5_K_dequant_f16: "Q5_K 176B", each "-> row-major fp16 mirror").  A row of k weights
+ * is k/256 superblocks; weight e (0..255) of a superblock:
+ *   Q6_K (210 bytes): ql[128] at +0, qh[64] at +128, int8 scales[16] at +192, binary16 d at
+ *     +208.  With e = 128h + 32g + l, its 6-bit code is the low (g < 2) or high (g >= 2) nibble
+ *     of ql[64h + 32(g%2) + l] plus 16 times bits 2g..2g+1 of qh[32h + l]; its value is
+ *     d * scales[e/16] * (code - 32).
+ *   Q4_K (144 bytes): binary16 d at +0, binary16 dmin at +2, 12 scale bytes s at +4, qs[128]
+ *     at +16.  Sub-block j = e/32 has a 6-bit scale and min: j < 4: s[j] & 63, s[j+4] & 63;
+ *     j >= 4: (s[j+4] & 15) | (s[j-4] >> 6) << 4 and (s[j+4] >> 4) | (s[j] >> 6) << 4.  With
+ *     e = 64g + 32u + l the code is nibble u of qs[32g + l]; the value is
+ *     d * scale_j * code - dmin * min_j.
+ *   Q5_K (176 bytes): as Q4_K with qh[32] at +16 and qs[128] at +48; bit j of qh[l] is the
+ *     code's fifth bit (code += 16).
+ * k: a positive multiple of 256; pointers 16-byte aligned; errors as for the Q8_0 calls.
+ *
+ * q8act_dequant_q{6,4,5}_k_f16: w16[r][e] = the binary16 nearest to the weight's exact value
+ *   (ties to even), row-major [n][k].
+ * q8act_gemv_q{6,4,5}_k: the decode GEMV on the q8_1 activation (xq [m][k] int8, xd [m][k/32]
+ *   f32, y [m][n] f32 overwritten), 1 <= m <= Q8ACT_GEMV_KQ_MAX_M.  Per 32-wide activation
+ *   block b (sub-block j of a superblock) exact integers and an f32 fold:
+ *     Q6_K:        E_b = scales[2i] * sum_{16} (code - 32) xq + scales[2i+1] * sum_{16} (code - 32) xq,
+ *                  y += (d * d_a) * E_b;
+ *     Q4_K, Q5_K:  D_b = sum code * xq,  X_b = sum xq,
+ *                  y += d_a * ((d * scale_j) * D_b - (dmin * min_j) * X_b);
+ *   blocks ascending within a superblock, superblocks summed in a fixed order, so token t's
+ *   result does not depend on m.  k is bounded by shared memory as for q8act_gemv_q8_0
+ *   (Q8ACT_ERR_DIMS beyond it).
+ * q8act_debug_gemv_q{6,4,5}_k_block_dots: that GEMV's exact integers per block, [m][n][k/32]
+ *   int32 (E_b for Q6_K, D_b for Q4_K / Q5_K) (test hook).
+ */
+#define Q8ACT_GEMV_KQ_MAX_M 8
+int q8act_dequant_q6_k_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
+int q8act_dequant_q4_k_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
+int q8act_dequant_q5_k_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream);
+int q8act_gemv_q6_k(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m,
+                    int64_t n, int64_t k, void *stream);
+int q8act_gemv_q4_k(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m,
+                    int64_t n, int64_t k, void *stream);
+int q8act_gemv_q5_k(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m,
+                    int64_t n, int64_t k, void *stream);
+int q8act_debug_gemv_q6_k_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m,
+                                     int64_t n, int64_t k, void *stream);
+int q8act_debug_gemv_q4_k_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m,
+                                     int64_t n, int64_t k, void *stream);
+int q8act_debug_gemv_q5_k_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m,
+                                     int64_t n, int64_t k, void *stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device-side status word that kernels set
  * when a pipeline wait times out.  Returns Q8ACT_OK, Q8ACT_ERR_DRAIN_TIMEOUT (a producer gave
  * up waiting for its own copies before its CTA exited), Q8ACT_ERR_TIMEOUT (a pipeline wait

@@ -23,7 +23,10 @@ from ._lib import (  # noqa: F401  (re-exported ABI)
     q8act_repack_q8_0, q8act_repack_ldn, q8act_gemm_q8_0_repacked, q8act_debug_gemm_repacked_block_dots,
     q8act_gemv_q8_0_group, Q8ACT_GEMV_MAX_GROUP, q8act_quantize_q4_0, q8act_dequant_q4_0_f16,
     q8act_gemv_q4_0, q8act_debug_gemv_q4_0_block_dots, q8act_gemv_workspace_bytes, q8act_gemv_q8_0_f32,
-    q8act_debug_wait_timeout, Q8ACT_ERR_DRAIN_TIMEOUT)
+    q8act_debug_wait_timeout, Q8ACT_ERR_DRAIN_TIMEOUT, Q8ACT_GEMV_KQ_MAX_M,
+    q8act_dequant_q6_k_f16, q8act_dequant_q4_k_f16, q8act_dequant_q5_k_f16,
+    q8act_gemv_q6_k, q8act_gemv_q4_k, q8act_gemv_q5_k,
+    q8act_debug_gemv_q6_k_block_dots, q8act_debug_gemv_q4_k_block_dots, q8act_debug_gemv_q5_k_block_dots)
 
 QK = 32
 Q8_0_BYTES = 34
@@ -194,4 +197,26 @@ def gemv_q8_0_f32(w, x, n: int, ws=None, out=None):
         ws = gemv_workspace(m, k, x.device)
     y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=x.device)
     check(q8act_gemv_q8_0_f32(w, x, y, m, n, k, ws, ws.numel()), "q8act_gemv_q8_0_f32")
+    return y
+
+
+KQ_BYTES = {"q6_k": 210, "q4_k": 144, "q5_k": 176}   # bytes per 256-weight superblock
+
+
+def dequant_kq_f16(fmt: str, w, n: int, k: int, out=None):
+    """K-quant superblocks (fmt "q6_k", "q4_k" or "q5_k") -> row-major float16 [n, k]."""
+    import torch
+    w16 = out if out is not None else torch.empty((n, k), dtype=torch.float16, device=w.device)
+    fn = {"q6_k": q8act_dequant_q6_k_f16, "q4_k": q8act_dequant_q4_k_f16, "q5_k": q8act_dequant_q5_k_f16}[fmt]
+    check(fn(w, w16, n, k), f"q8act_dequant_{fmt}_f16")
+    return w16
+
+
+def gemv_kq(fmt: str, w, xq, xd, n: int, out=None):
+    """Decode GEMV over K-quant weights (n rows) with the q8_1 activation of m <= 8 tokens."""
+    import torch
+    m, k = xq.shape
+    y = out if out is not None else torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    fn = {"q6_k": q8act_gemv_q6_k, "q4_k": q8act_gemv_q4_k, "q5_k": q8act_gemv_q5_k}[fmt]
+    check(fn(w, xq, xd, y, m, n, k), f"q8act_gemv_{fmt}")
     return y

@@ -40,7 +40,11 @@ EXPORTED = (
     "q8act_gemm_q8_0_repacked", "q8act_debug_gemm_repacked_block_dots", "q8act_gemv_q8_0_group",
     "q8act_quantize_q4_0", "q8act_dequant_q4_0_f16", "q8act_gemv_q4_0", "q8act_debug_gemv_q4_0_block_dots",
     "q8act_gemv_workspace_bytes", "q8act_gemv_q8_0_f32", "q8act_debug_wait_timeout",
+    "q8act_dequant_q6_k_f16", "q8act_dequant_q4_k_f16", "q8act_dequant_q5_k_f16",
+    "q8act_gemv_q6_k", "q8act_gemv_q4_k", "q8act_gemv_q5_k",
+    "q8act_debug_gemv_q6_k_block_dots", "q8act_debug_gemv_q4_k_block_dots", "q8act_debug_gemv_q5_k_block_dots",
 )
+Q8ACT_GEMV_KQ_MAX_M = 8
 Q8ACT_NOALLOC_WS_BYTES = 24 << 20
 Q8ACT_GEMM_SPLIT_BYTES = 320 * 65536 + 160 * 64
 
@@ -96,6 +100,10 @@ def lib() -> ctypes.CDLL:
                 "q8act_gemv_q8_0_f32": ([P, P, P, I64, I64, I64, P, SZ, P], I32),
                 "q8act_debug_wait_timeout": ([I64, P], I32),
             }
+            for f in ("q6_k", "q4_k", "q5_k"):
+                sig[f"q8act_dequant_{f}_f16"] = ([P, P, I64, I64, P], I32)
+                sig[f"q8act_gemv_{f}"] = ([P, P, P, P, I64, I64, I64, P], I32)
+                sig[f"q8act_debug_gemv_{f}_block_dots"] = ([P, P, P, I64, I64, I64, P], I32)
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
                 f.argtypes = args
@@ -251,3 +259,39 @@ def q8act_debug_wait_timeout(limit_ns, stream=None) -> int:
     """Test hook: a kernel whose bounded wait on a barrier nobody arrives on runs out after
     limit_ns nanoseconds and records a pipeline timeout in the device status word."""
     return lib().q8act_debug_wait_timeout(int(limit_ns), _s(stream))
+
+
+def q8act_dequant_q6_k_f16(w, w16, n, k, stream=None) -> int:
+    return lib().q8act_dequant_q6_k_f16(_p(w), _p(w16), n, k, _s(stream))
+
+
+def q8act_dequant_q4_k_f16(w, w16, n, k, stream=None) -> int:
+    return lib().q8act_dequant_q4_k_f16(_p(w), _p(w16), n, k, _s(stream))
+
+
+def q8act_dequant_q5_k_f16(w, w16, n, k, stream=None) -> int:
+    return lib().q8act_dequant_q5_k_f16(_p(w), _p(w16), n, k, _s(stream))
+
+
+def q8act_gemv_q6_k(w, xq, xd, y, m, n, k, stream=None) -> int:
+    return lib().q8act_gemv_q6_k(_p(w), _p(xq), _p(xd), _p(y), m, n, k, _s(stream))
+
+
+def q8act_gemv_q4_k(w, xq, xd, y, m, n, k, stream=None) -> int:
+    return lib().q8act_gemv_q4_k(_p(w), _p(xq), _p(xd), _p(y), m, n, k, _s(stream))
+
+
+def q8act_gemv_q5_k(w, xq, xd, y, m, n, k, stream=None) -> int:
+    return lib().q8act_gemv_q5_k(_p(w), _p(xq), _p(xd), _p(y), m, n, k, _s(stream))
+
+
+def q8act_debug_gemv_q6_k_block_dots(w, xq, D, m, n, k, stream=None) -> int:
+    return lib().q8act_debug_gemv_q6_k_block_dots(_p(w), _p(xq), _p(D), m, n, k, _s(stream))
+
+
+def q8act_debug_gemv_q4_k_block_dots(w, xq, D, m, n, k, stream=None) -> int:
+    return lib().q8act_debug_gemv_q4_k_block_dots(_p(w), _p(xq), _p(D), m, n, k, _s(stream))
+
+
+def q8act_debug_gemv_q5_k_block_dots(w, xq, D, m, n, k, stream=None) -> int:
+    return lib().q8act_debug_gemv_q5_k_block_dots(_p(w), _p(xq), _p(D), m, n, k, _s(stream))

@@ -315,6 +315,89 @@ int q8act_debug_gemv_q4_0_block_dots(const void *w, const int8_t *xq, int32_t *D
     return gemv_q4_0_common(w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
 }
 
+// ---- K-quant superblocks (GGUF Q6_K 210 B, Q4_K 144 B, Q5_K 176 B; 256 weights each) ----
+
+static int dequant_kq_common(int fmt, const void *w, void *w16, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !w16) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || n < 1 || n > INT32_MAX || n * k > ((int64_t)1 << 34)) return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(w16)) return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return cuda_rc(q8::launch_dequant_kq_f16(*dev, fmt, static_cast<const uint8_t *>(w), static_cast<uint16_t *>(w16),
+                                             n, k, (cudaStream_t)stream));
+}
+
+int q8act_dequant_q6_k_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream)
+{
+    return dequant_kq_common(6, w, w16, n, k, stream);
+}
+int q8act_dequant_q4_k_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream)
+{
+    return dequant_kq_common(4, w, w16, n, k, stream);
+}
+int q8act_dequant_q5_k_f16(const void *w, void *w16, int64_t n, int64_t k, void *stream)
+{
+    return dequant_kq_common(5, w, w16, n, k, stream);
+}
+
+static int gemv_kq_common(int fmt, const void *w, const int8_t *xq, const float *xd, float *y, int32_t *dots,
+                          int64_t m, int64_t n, int64_t k, void *stream)
+{
+    if (!w || !xq || !xd || (!y && !dots)) return Q8ACT_ERR_NULL;
+    if (check_k(k) != Q8ACT_OK || m < 1 || m > Q8ACT_GEMV_KQ_MAX_M || n < 1 || n > INT32_MAX / 2 ||
+        n * k > ((int64_t)1 << 36))
+        return Q8ACT_ERR_DIMS;
+    if (!aligned16(w) || !aligned16(xq) || !aligned16(xd) || (y && !aligned16(y)) || (dots && !aligned16(dots)))
+        return Q8ACT_ERR_ALIGN;
+    const q8::DeviceInfo *dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if (!q8::gemv_kq_supported(*dev, fmt, m, k)) return Q8ACT_ERR_DIMS;
+    return cuda_rc(q8::launch_gemv_kq(*dev, fmt, static_cast<const uint8_t *>(w), xq, xd, y, dots, m, n, k,
+                                      (cudaStream_t)stream));
+}
+
+int q8act_gemv_q6_k(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m, int64_t n, int64_t k,
+                    void *stream)
+{
+    if (!y) return Q8ACT_ERR_NULL;
+    return gemv_kq_common(6, w, xq, xd, y, nullptr, m, n, k, stream);
+}
+int q8act_gemv_q4_k(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m, int64_t n, int64_t k,
+                    void *stream)
+{
+    if (!y) return Q8ACT_ERR_NULL;
+    return gemv_kq_common(4, w, xq, xd, y, nullptr, m, n, k, stream);
+}
+int q8act_gemv_q5_k(const void *w, const int8_t *xq, const float *xd, float *y, int64_t m, int64_t n, int64_t k,
+                    void *stream)
+{
+    if (!y) return Q8ACT_ERR_NULL;
+    return gemv_kq_common(5, w, xq, xd, y, nullptr, m, n, k, stream);
+}
+
+// The block-integer stage needs a readable scale array; the quants are readable and larger.
+int q8act_debug_gemv_q6_k_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n, int64_t k,
+                                     void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    return gemv_kq_common(6, w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
+}
+int q8act_debug_gemv_q4_k_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n, int64_t k,
+                                     void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    return gemv_kq_common(4, w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
+}
+int q8act_debug_gemv_q5_k_block_dots(const void *w, const int8_t *xq, int32_t *D, int64_t m, int64_t n, int64_t k,
+                                     void *stream)
+{
+    if (!D) return Q8ACT_ERR_NULL;
+    return gemv_kq_common(5, w, xq, reinterpret_cast<const float *>(xq), nullptr, D, m, n, k, stream);
+}
+
 // Workspace of the fused GEMMs: [binary16 quants][block-major scales][split region].  The
 // first two are required; with the split region as well, a launch may take the balanced
 // schedule (equal runs of (tile, k group) units per CTA, tiles cut into k pieces at the runs'

@@ -1,0 +1,624 @@
+// kquant.cu -- the GGUF K-quant superblocks (256 weights each) that memra-engine 0.81.0
+// f16_ffi.rs names beside Q8_0 and Q4_0: Q6_K (210 bytes), Q4_K (144 bytes), Q5_K (176 bytes).
+// Two passes over them:
+//   * the fp16 mirror (memra_q6_K / q4_K / q5_K_dequant_f16): every weight's exact value,
+//     rounded once to binary16;
+//   * the decode GEMV with the q8_1 activation (1 <= m <= 8), exact integer dots per 32-wide
+//     activation block and an f32 fold.
+// Superblock layouts (the GGUF formats'), weight e = 0..255:
+//   Q6_K: ql[128] | qh[64] | int8 scales[16] | fp16 d.  e = 128h + 32g + l: code = low 4 bits
+//         from ql[64h + 32(g&1) + l] (low nibble for g < 2, high for g >= 2) + 16 * 2 bits
+//         (qh[32h + l] >> 2g); value = d * scales[e/16] * (code - 32).
+//   Q4_K: fp16 d | fp16 dmin | 12 scale bytes | qs[128].  Sub-block j = e/32 has a 6-bit scale
+//         and min (j < 4: s[j] & 63, s[j+4] & 63; j >= 4: (s[j+4] & 15) | (s[j-4] >> 6) << 4,
+//         (s[j+4] >> 4) | (s[j] >> 6) << 4); e = 64g + 32u + l: code = nibble u of qs[32g + l];
+//         value = d * sc_j * code - dmin * m_j.
+//   Q5_K: as Q4_K with qh[32] before qs; the code gains bit j of qh[l] as its fifth bit.
+// Both passes stream chunks of whole rows into a shared-memory ring with cp.async.bulk, as
+// the Q8_0 kernels do.  Q6_K rows are a 16-byte multiple only when k is a multiple of 2048,
+// so a chunk holds a multiple of 8 rows (8 rows always are) and the last chunk's final
+// 0..14 bytes are copied by the producer thread itself.
+#include "common.cuh"
+#include "launch.h"
+
+namespace q8 {
+namespace {
+
+constexpr int QK_K = 256;
+constexpr int KMAX_STAGES = 6;
+
+struct KQ6 {
+    static constexpr int BYTES = 210;
+    static constexpr int WORDS = 53;   // 212 bytes cover the superblock from any 2-byte offset
+};
+struct KQ4 {
+    static constexpr int BYTES = 144;
+    static constexpr int WORDS = 36;
+};
+struct KQ5 {
+    static constexpr int BYTES = 176;
+    static constexpr int WORDS = 44;
+};
+
+__host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+
+// Rows per chunk must make every chunk start (and every stage) 16-byte aligned.
+inline int row_align(uint32_t row_bytes) { return 16 / gcd_int((int)(row_bytes % 16 == 0 ? 16 : row_bytes % 16), 16); }
+
+// The superblock at p (2-byte aligned for Q6_K, 16-byte aligned otherwise) as 32-bit words
+// of its bytes, read from shared memory.
+template <class F>
+__device__ __forceinline__ void load_superblock(const uint8_t *p, uint32_t (&w)[F::WORDS])
+{
+    if constexpr (F::BYTES % 16 == 0) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+        for (int c = 0; c < F::WORDS / 4; ++c) {
+            const uint4 v = src[c];
+            w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+    } else {
+        // Aligned words from the word below p, funnel-shifted by the 0 or 2 bytes of offset.
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        const uint32_t *base = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        const uint32_t sh = (uint32_t)(a & 3) * 8;
+        uint32_t prev = base[0];
+#pragma unroll
+        for (int i = 0; i < F::WORDS; ++i) {
+            const uint32_t nxt = base[i + 1];
+            w[i] = __funnelshift_r(prev, nxt, sh);
+            prev = nxt;
+        }
+    }
+}
+
+// Byte i (0..11) of the Q4_K / Q5_K scale bytes, which occupy words 1..3.
+template <int N>
+__device__ __forceinline__ uint32_t sbyte(const uint32_t (&w)[N], int i) { return (w[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu; }
+
+__device__ __forceinline__ void k4_scale_min(const uint32_t *w, int j, int &sc, int &mn)
+{
+    auto b = [&](int i) { return (int)((w[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu); };
+    if (j < 4) {
+        sc = b(j) & 63;
+        mn = b(j + 4) & 63;
+    } else {
+        sc = (b(j + 4) & 15) | ((b(j - 4) >> 6) << 4);
+        mn = (b(j + 4) >> 4) | ((b(j) >> 6) << 4);
+    }
+}
+
+// The codes of 32-wide block j of a superblock, as 8 words of 4 bytes each (element order),
+// ready for dp4a: Q6_K gives the signed bytes code - 32; Q4_K / Q5_K the unsigned codes.
+template <class F>
+__device__ __forceinline__ void block_codes(const uint32_t (&w)[F::WORDS], int j, uint32_t (&q)[8])
+{
+    if constexpr (F::BYTES == KQ6::BYTES) {
+        const int n = j >> 2, g = j & 3;
+        const int qlw = 16 * n + 8 * (g & 1), qhw = 32 + 8 * n;
+        const int s1 = 4 * (g >> 1), s2 = 2 * g;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t code = ((w[qlw + c] >> s1) & 0x0F0F0F0Fu) | (((w[qhw + c] >> s2) & 0x03030303u) << 4);
+            // code - 32 as a signed byte: flip bit 5; where it is now set (code < 32) the byte
+            // is code + 32 and must become code + 32 - 64, i.e. gain bits 6 and 7.
+            const uint32_t t = code ^ 0x20202020u;
+            const uint32_t s = t & 0x20202020u;
+            q[c] = t | (s << 1) | (s << 2);
+        }
+    } else {
+        const int g = j >> 1, u = j & 1;
+        constexpr int QS = F::BYTES == KQ4::BYTES ? 4 : 12;   // word of qs[0]
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t code = (w[QS + 8 * g + c] >> (4 * u)) & 0x0F0F0F0Fu;
+            if constexpr (F::BYTES == KQ5::BYTES) code |= ((w[4 + c] >> j) & 0x01010101u) << 4;
+            q[c] = code;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Streaming plan and producer shared by both passes
+// ---------------------------------------------------------------------------------------
+struct KPlan {
+    int G;              // superblocks per row (k / 256)
+    int R;              // rows per chunk (a multiple of the row alignment)
+    int U;              // units (superblocks) per chunk
+    int stages;
+    int ctas_per_sm;
+    int warp_reduce;    // 1: a row's units are consecutive lanes of one warp (G divides 32)
+    uint32_t row_bytes;
+    uint32_t chunk_bytes;
+    int64_t nchunks;
+    size_t off_x, off_xd, off_xs, off_part, off_bar, smem;
+};
+
+// Copy rows [row0, row0 + rows) of w into dst, completing on `bar`: a bulk copy of the
+// 16-byte multiple, then (for the last, ragged chunk of a Q6_K matrix) the few bytes after it
+// with plain stores, made before the arrival so that they are visible with the copy.
+__device__ __forceinline__ void produce_chunk(uint8_t *dst, const uint8_t *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy)
+{
+    const uint32_t main = bytes & ~15u;
+    for (uint32_t i = main; i < bytes; ++i) dst[i] = src[i];
+    mbar_arrive_expect_tx(bar, main);
+    if (main) bulk_g2s_hint(dst, src, main, bar, policy);
+}
+
+// ---------------------------------------------------------------------------------------
+// fp16 mirror
+// ---------------------------------------------------------------------------------------
+constexpr int DQ_WARPS = 16;
+constexpr int DQ_THREADS = (DQ_WARPS + 1) * 32;
+constexpr int DQ_TARGET_CHUNK = 17408;
+
+// Round-to-odd difference of two f32 values: the truncated difference with its last bit set
+// when the difference is inexact.  Rounding that to binary16 (11 bits, far fewer than f32's
+// 24) gives the correctly rounded binary16 of the exact difference.
+__device__ __forceinline__ float sub_round_odd(float a, float b)
+{
+    const float z = __fsub_rz(a, b);
+    const bool inexact = __fsub_ru(a, b) != __fsub_rd(a, b);
+    return inexact ? __uint_as_float(__float_as_uint(z) | 1u) : z;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    const __half2 h = __halves2half2(__float2half_rn(lo), __float2half_rn(hi));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <class F>
+__global__ void __launch_bounds__(DQ_THREADS, 2)
+    kq_dequant_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out, int n, int k, KPlan p, int *status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + KMAX_STAGES;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], DQ_WARPS);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int64_t my_chunks = blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (warp == DQ_WARPS) {
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            int64_t issued = 0;
+            for (int64_t i = 0; i < my_chunks; ++i) {
+                const int s = (int)(i % p.stages);
+                if (!mbar_wait(&empty[s], (uint32_t)(((i / p.stages) & 1) ^ 1), status)) break;
+                const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+                const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
+                produce_chunk(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, (uint32_t)rows * p.row_bytes,
+                              &full[s], policy);
+                ++issued;
+            }
+            for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
+                mbar_wait_drain(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+        }
+        return;
+    }
+
+    // Lane j of a warp converts weights 8j .. 8j + 7 of a superblock (one 16-byte output piece).
+    const int e0 = 8 * lane;
+    for (int64_t i = 0; i < my_chunks; ++i) {
+        const int s = (int)(i % p.stages);
+        const bool ok = mbar_wait(&full[s], (uint32_t)((i / p.stages) & 1), status);
+        if (__any_sync(0xffffffffu, !ok)) break;
+        const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+        const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+        const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
+        const int units = rows * p.G;
+        for (int u = warp; u < units; u += DQ_WARPS) {
+            const uint8_t *sb = sbase + (size_t)u * F::BYTES;
+            float v[8];
+            if constexpr (F::BYTES == KQ6::BYTES) {
+                const int h = e0 >> 7, pp = e0 & 127, g = pp >> 5, l0 = pp & 31;
+                const uint8_t *ql = sb + 64 * h + 32 * (g & 1) + l0;
+                const uint8_t *qh = sb + 128 + 32 * h + l0;
+                const float d = half_bits_to_float((uint32_t)sb[208] | ((uint32_t)sb[209] << 8));
+                const float ds = __fmul_rn(d, (float)(int8_t)sb[192 + (e0 >> 4)]);   // exact
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int code = (((int)ql[c] >> (4 * (g >> 1))) & 15) | ((((int)qh[c] >> (2 * g)) & 3) << 4);
+                    v[c] = __fmul_rn(ds, (float)(code - 32));                        // exact
+                }
+            } else {
+                const uint32_t *sw = reinterpret_cast<const uint32_t *>(sb);
+                uint32_t head[4] = {sw[0], sw[1], sw[2], sw[3]};
+                const int g = e0 >> 6, u2 = (e0 >> 5) & 1, l0 = e0 & 31, j = e0 >> 5;
+                int sc, mn;
+                k4_scale_min(head, j, sc, mn);
+                const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
+                const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);   // exact
+                constexpr int QS = F::BYTES == KQ4::BYTES ? 16 : 48;
+                const uint2 qv = *reinterpret_cast<const uint2 *>(sb + QS + 32 * g + l0);
+                uint2 hv = make_uint2(0, 0);
+                if constexpr (F::BYTES == KQ5::BYTES) hv = *reinterpret_cast<const uint2 *>(sb + 16 + l0);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t qb = ((c < 4 ? qv.x : qv.y) >> (8 * (c & 3))) & 0xFFu;
+                    int code = (int)((qb >> (4 * u2)) & 15u);
+                    if constexpr (F::BYTES == KQ5::BYTES)
+                        code += 16 * (int)((((c < 4 ? hv.x : hv.y) >> (8 * (c & 3))) >> j) & 1u);
+                    v[c] = sub_round_odd(__fmul_rn(dsc, (float)code), dmm);
+                }
+            }
+            const int row = u / p.G, gsb = u - row * p.G;
+            const uint4 o = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
+            __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)gsb * QK_K) / 8 + lane, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+KPlan dequant_plan(int64_t n, int64_t k, int sb_bytes, size_t smem_cap)
+{
+    KPlan p{};
+    p.G = (int)(k / QK_K);
+    p.row_bytes = (uint32_t)(p.G * sb_bytes);
+    const int ra = row_align(p.row_bytes);
+    p.R = (int)(DQ_TARGET_CHUNK / p.row_bytes) / ra * ra;
+    if (p.R < ra) p.R = ra;
+    if ((int64_t)p.R > n) p.R = (int)((n + ra - 1) / ra * ra);
+    p.chunk_bytes = (uint32_t)p.R * p.row_bytes;
+    p.nchunks = (n + p.R - 1) / p.R;
+    const size_t room = smem_cap > 2 * KMAX_STAGES * 8 + 64 ? smem_cap - 2 * KMAX_STAGES * 8 - 64 : 0;
+    int64_t st = (int64_t)(room / p.chunk_bytes);
+    p.stages = (int)(st > KMAX_STAGES ? KMAX_STAGES : st);
+    p.off_bar = (size_t)p.stages * p.chunk_bytes;
+    p.smem = p.off_bar + 2 * KMAX_STAGES * 8;
+    return p;
+}
+
+template <class F>
+cudaError_t launch_kq_dequant(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16, int64_t n, int64_t k,
+                              cudaStream_t stream)
+{
+    const size_t half_sm = 113 * 1024;
+    KPlan p = dequant_plan(n, k, F::BYTES, half_sm < dev.max_smem_optin ? half_sm : dev.max_smem_optin);
+    int per_sm = 2;
+    if (p.stages < 3) {
+        p = dequant_plan(n, k, F::BYTES, dev.max_smem_optin);
+        per_sm = 1;
+    }
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    cudaError_t e = set_kernel_smem<kq_dequant_kernel<F>>(dev.device, p.smem);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (int64_t)dev.num_sms * per_sm;
+    const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
+    kq_dequant_kernel<F><<<(int)grid, DQ_THREADS, p.smem, stream>>>(w, reinterpret_cast<uint4 *>(w16), (int)n, (int)k,
+                                                                   p, dev.status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// GEMV
+// ---------------------------------------------------------------------------------------
+constexpr int GV_CONSUMERS = 128;
+constexpr int XG_WORDS = 68;    // activation quants per (token, 256-group): 64 words + 4 pad
+constexpr int XDG_WORDS = 12;   // activation scales per (token, group): 8 + 4 pad
+
+KPlan gemv_plan(int64_t m, int64_t n, int64_t k, int sb_bytes, size_t smem_cap, int r_cap)
+{
+    KPlan p{};
+    p.G = (int)(k / QK_K);
+    p.row_bytes = (uint32_t)(p.G * sb_bytes);
+    const int ra = row_align(p.row_bytes);
+    int R = p.G <= GV_CONSUMERS ? GV_CONSUMERS / p.G : 1;
+    if (R > r_cap) R = r_cap;
+    R = R / ra * ra;
+    if (R < ra) R = ra;
+    if ((int64_t)R > n) R = (int)((n + ra - 1) / ra * ra);
+    p.R = R;
+    p.U = p.R * p.G;
+    p.chunk_bytes = (uint32_t)p.R * p.row_bytes;
+    p.nchunks = (n + p.R - 1) / p.R;
+    const size_t x_bytes = (size_t)m * p.G * XG_WORDS * 4;
+    const size_t xd_bytes = (size_t)m * p.G * XDG_WORDS * 4;
+    const size_t xs_bytes = (size_t)m * p.G * 8 * 4;
+    const size_t part_bytes = 2 * (size_t)p.U * m * 4;
+    const size_t fixed = 16 + x_bytes + xd_bytes + xs_bytes + part_bytes + 2 * KMAX_STAGES * 8 + 64;
+    const size_t room = smem_cap > fixed ? smem_cap - fixed : 0;
+    int64_t st = (int64_t)(room / p.chunk_bytes);
+    p.stages = (int)(st > KMAX_STAGES ? KMAX_STAGES : st);
+    // 16 bytes after the ring: the Q6_K word loads read up to 6 bytes past a superblock.
+    p.off_x = (size_t)p.stages * p.chunk_bytes + 16;
+    p.off_xd = p.off_x + x_bytes;
+    p.off_xs = p.off_xd + xd_bytes;
+    p.off_part = p.off_xs + xs_bytes;
+    p.off_bar = (p.off_part + part_bytes + 7) & ~(size_t)7;
+    p.smem = p.off_bar + 2 * KMAX_STAGES * 8;
+    p.ctas_per_sm = 1;
+    p.warp_reduce = (p.G <= 32 && 32 % p.G == 0) ? 1 : 0;
+    return p;
+}
+
+__device__ __forceinline__ bool kbar_red_or(int id, int nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// MM: the largest token count of the instance; the call's m (<= MM) tokens are folded, each
+// with the same operations in the same order for every MM (decode == verify).
+template <class F, int MM>
+__global__ void __launch_bounds__(GV_CONSUMERS + 32, 2)
+    kq_gemv_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq, const float *__restrict__ xd,
+                   float *__restrict__ y, int32_t *__restrict__ dots, int m, int n, int k, KPlan p, int *status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem + p.off_x);
+    float *xds = reinterpret_cast<float *>(smem + p.off_xd);
+    int *xsum = reinterpret_cast<int *>(smem + p.off_xs);
+    float *part = reinterpret_cast<float *>(smem + p.off_part);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + KMAX_STAGES;
+    const int tid = threadIdx.x;
+    const int G = p.G;
+    const int nb = k / QK;
+
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], GV_CONSUMERS / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid < GV_CONSUMERS) {
+        // The activation cache: quants [t][group][68 words], scales [t][group][12], and the
+        // sum of each 32-wide block's quants (the Q4_K / Q5_K min term).
+        for (int idx = tid; idx < m * G * 16; idx += GV_CONSUMERS) {
+            const int t = idx / (G * 16), rem = idx - t * G * 16, g = rem >> 4, c = rem & 15;
+            const uint4 v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + g * 256 + c * 16);
+            *reinterpret_cast<uint4 *>(xs + (t * G + g) * XG_WORDS + c * 4) = v;
+        }
+        for (int idx = tid; idx < m * G * 2; idx += GV_CONSUMERS) {
+            const int t = idx / (G * 2), rem = idx - t * G * 2, g = rem >> 1, c = rem & 1;
+            const float4 v = *reinterpret_cast<const float4 *>(xd + (int64_t)t * nb + g * 8 + c * 4);
+            *reinterpret_cast<float4 *>(xds + (t * G + g) * XDG_WORDS + c * 4) = v;
+        }
+        named_bar_sync(2, GV_CONSUMERS);
+        for (int idx = tid; idx < m * G * 8; idx += GV_CONSUMERS) {
+            const int tg = idx >> 3, j = idx & 7;
+            const uint32_t *xv = xs + tg * XG_WORDS + 8 * j;
+            int sum = 0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) sum = dp4a(0x01010101u, xv[c], sum);
+            xsum[idx] = sum;
+        }
+        named_bar_sync(2, GV_CONSUMERS);
+    }
+
+    const int64_t my_chunks = blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (tid >= GV_CONSUMERS) {
+        if (tid == GV_CONSUMERS) {
+            const uint64_t policy = l2_policy_evict_first();
+            int64_t issued = 0;
+            for (int64_t i = 0; i < my_chunks; ++i) {
+                const int s = (int)(i % p.stages);
+                if (!mbar_wait(&empty[s], (uint32_t)(((i / p.stages) & 1) ^ 1), status)) break;
+                const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+                const int64_t rows = (n - row0) < p.R ? (n - row0) : p.R;
+                produce_chunk(smem + (size_t)s * p.chunk_bytes, w + row0 * p.row_bytes, (uint32_t)rows * p.row_bytes,
+                              &full[s], policy);
+                ++issued;
+            }
+            for (int64_t i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
+                mbar_wait_drain(&full[i % p.stages], (uint32_t)((i / p.stages) & 1), status);
+        }
+        return;
+    }
+
+    for (int64_t i = 0; i < my_chunks; ++i) {
+        const int s = (int)(i % p.stages);
+        const bool ok = mbar_wait(&full[s], (uint32_t)((i / p.stages) & 1), status);
+        if (p.warp_reduce ? __any_sync(0xffffffffu, !ok) : kbar_red_or(1, GV_CONSUMERS, !ok)) break;
+        const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
+        const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
+        const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
+        float *pbuf = part + (size_t)(i & 1) * p.U * MM;
+        const int ulimit = p.warp_reduce ? (p.U + 31) / 32 * 32 : p.U;
+        for (int u = tid; u < ulimit; u += GV_CONSUMERS) {
+            const int row = u / G;
+            const int g = u - row * G;
+            float acc[MM];
+#pragma unroll
+            for (int t = 0; t < MM; ++t) acc[t] = 0.0f;
+            if (row < rows) {
+                uint32_t wv[F::WORDS];
+                load_superblock<F>(sbase + (size_t)row * p.row_bytes + (size_t)g * F::BYTES, wv);
+                float d, dmin = 0.0f;
+                if constexpr (F::BYTES == KQ6::BYTES) {
+                    d = half_bits_to_float(wv[52] & 0xffffu);
+                } else {
+                    d = half_bits_to_float(wv[0] & 0xffffu);
+                    dmin = half_bits_to_float(wv[0] >> 16);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t q[8];
+                    block_codes<F>(wv, j, q);
+                    int sc0 = 0, sc1 = 0;
+                    float dsc = 0.0f, dmm = 0.0f;
+                    if constexpr (F::BYTES == KQ6::BYTES) {
+                        const uint32_t sw = wv[48 + (j >> 1)] >> (16 * (j & 1));
+                        sc0 = (int)(int8_t)(sw & 0xFFu);
+                        sc1 = (int)(int8_t)((sw >> 8) & 0xFFu);
+                    } else {
+                        int sc, mn;
+                        k4_scale_min(wv, j, sc, mn);
+                        dsc = __fmul_rn(d, (float)sc);       // exact
+                        dmm = __fmul_rn(dmin, (float)mn);    // exact
+                    }
+#pragma unroll
+                    for (int t = 0; t < MM; ++t) {
+                        if (t >= m) break;
+                        const uint4 *xv = reinterpret_cast<const uint4 *>(xs + (t * G + g) * XG_WORDS + j * 8);
+                        const uint4 a = xv[0], b = xv[1];
+                        int D0 = dp4a(q[0], a.x, 0);
+                        int D1 = dp4a(q[4], b.x, 0);
+                        D0 = dp4a(q[1], a.y, D0);
+                        D1 = dp4a(q[5], b.y, D1);
+                        D0 = dp4a(q[2], a.z, D0);
+                        D1 = dp4a(q[6], b.z, D1);
+                        D0 = dp4a(q[3], a.w, D0);
+                        D1 = dp4a(q[7], b.w, D1);
+                        const float da = xds[(t * G + g) * XDG_WORDS + j];
+                        if constexpr (F::BYTES == KQ6::BYTES) {
+                            const int E = sc0 * D0 + sc1 * D1;                       // exact
+                            if (dots)
+                                dots[((int64_t)t * n + row0 + row) * nb + g * 8 + j] = E;
+                            else
+                                acc[t] = __fmaf_rn(__fmul_rn(d, da), __int2float_rn(E), acc[t]);
+                        } else {
+                            const int D = D0 + D1;                                   // exact
+                            if (dots) {
+                                dots[((int64_t)t * n + row0 + row) * nb + g * 8 + j] = D;
+                            } else {
+                                const int X = xsum[(t * G + g) * 8 + j];
+                                const float v = __fsub_rn(__fmul_rn(dsc, __int2float_rn(D)),
+                                                          __fmul_rn(dmm, __int2float_rn(X)));
+                                acc[t] = __fmaf_rn(da, v, acc[t]);
+                            }
+                        }
+                    }
+                }
+            }
+            if (dots) continue;
+            if (p.warp_reduce) {
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    if (o >= G) break;
+#pragma unroll
+                    for (int t = 0; t < MM; ++t) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xffffffffu, acc[t], o));
+                }
+                if (g == 0 && row < rows) {
+#pragma unroll
+                    for (int t = 0; t < MM; ++t)
+                        if (t < m) y[(int64_t)t * n + row0 + row] = acc[t];
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < MM; ++t) pbuf[u * MM + t] = acc[t];
+            }
+        }
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&empty[s]);
+        if (dots || p.warp_reduce) continue;
+        named_bar_sync(1, GV_CONSUMERS);
+        for (int idx = tid; idx < rows * m; idx += GV_CONSUMERS) {
+            const int t = idx / rows, r = idx - t * rows;
+            const float *pr = pbuf + (size_t)r * G * MM + t;
+            float sum = pr[0];
+            for (int g = 1; g < G; ++g) sum = __fadd_rn(sum, pr[g * MM]);
+            y[(int64_t)t * n + row0 + r] = sum;
+        }
+    }
+}
+
+template <class F>
+KPlan choose_gemv_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin, int *per_sm)
+{
+    const size_t half_sm = 113 * 1024;
+    KPlan p = gemv_plan(m, n, k, F::BYTES, half_sm < smem_optin ? half_sm : smem_optin, GV_CONSUMERS);
+    if (p.stages >= 3) {
+        *per_sm = 2;
+        return p;
+    }
+    *per_sm = 1;
+    p = gemv_plan(m, n, k, F::BYTES, smem_optin, GV_CONSUMERS);
+    for (int r_cap = p.R / 2; p.stages < 2 && r_cap >= 1; r_cap /= 2)
+        p = gemv_plan(m, n, k, F::BYTES, smem_optin, r_cap);
+    return p;
+}
+
+template <class F, int MM>
+cudaError_t launch_kq_gemv_m(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
+                             int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+{
+    int per_sm = 1;
+    KPlan p = choose_gemv_plan<F>(MM, n, k, dev.max_smem_optin, &per_sm);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    cudaError_t e = set_kernel_smem<kq_gemv_kernel<F, MM>>(dev.device, p.smem);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (int64_t)dev.num_sms * per_sm;
+    const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
+    kq_gemv_kernel<F, MM><<<(int)grid, GV_CONSUMERS + 32, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n,
+                                                                           (int)k, p, dev.status);
+    return cudaGetLastError();
+}
+
+template <class F>
+cudaError_t launch_kq_gemv(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd, float *y,
+                           int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+{
+    if (m <= 1) return launch_kq_gemv_m<F, 1>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    if (m <= 2) return launch_kq_gemv_m<F, 2>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    if (m <= 4) return launch_kq_gemv_m<F, 4>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    if (m <= 8) return launch_kq_gemv_m<F, 8>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    return cudaErrorInvalidValue;
+}
+
+template <class F>
+bool kq_gemv_fits(const DeviceInfo &dev, int64_t m, int64_t k)
+{
+    int per_sm = 1;
+    const int mm = m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : 8;
+    return choose_gemv_plan<F>(mm, 1 << 20, k, dev.max_smem_optin, &per_sm).stages >= 2;
+}
+
+}  // namespace
+
+cudaError_t launch_dequant_kq_f16(const DeviceInfo &dev, int fmt, const uint8_t *w, uint16_t *w16, int64_t n,
+                                  int64_t k, cudaStream_t stream)
+{
+    switch (fmt) {
+    case 6: return launch_kq_dequant<KQ6>(dev, w, w16, n, k, stream);
+    case 4: return launch_kq_dequant<KQ4>(dev, w, w16, n, k, stream);
+    case 5: return launch_kq_dequant<KQ5>(dev, w, w16, n, k, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+bool gemv_kq_supported(const DeviceInfo &dev, int fmt, int64_t m, int64_t k)
+{
+    if (m < 1 || m > 8) return false;
+    switch (fmt) {
+    case 6: return kq_gemv_fits<KQ6>(dev, m, k);
+    case 4: return kq_gemv_fits<KQ4>(dev, m, k);
+    case 5: return kq_gemv_fits<KQ5>(dev, m, k);
+    default: return false;
+    }
+}
+
+cudaError_t launch_gemv_kq(const DeviceInfo &dev, int fmt, const uint8_t *w, const int8_t *xq, const float *xd,
+                           float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
+{
+    switch (fmt) {
+    case 6: return launch_kq_gemv<KQ6>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    case 4: return launch_kq_gemv<KQ4>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    case 5: return launch_kq_gemv<KQ5>(dev, w, xq, xd, y, dots, m, n, k, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace q8

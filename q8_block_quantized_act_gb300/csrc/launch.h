@@ -40,6 +40,14 @@ cudaError_t launch_gemv_q4_0_mma(const DeviceInfo &dev, const uint8_t *w, const 
                                  const float *xd, float *y, int32_t *dots, int64_t m, int64_t n,
                                  int64_t k, cudaStream_t stream);
 
+// K-quant superblocks (fmt 6: Q6_K, 4: Q4_K, 5: Q5_K): the fp16 mirror and the GEMV
+// (1 <= m <= 8; dots != nullptr stores the exact per-32-block integers instead of folding).
+cudaError_t launch_dequant_kq_f16(const DeviceInfo &dev, int fmt, const uint8_t *w, uint16_t *w16, int64_t n,
+                                  int64_t k, cudaStream_t stream);
+bool gemv_kq_supported(const DeviceInfo &dev, int fmt, int64_t m, int64_t k);
+cudaError_t launch_gemv_kq(const DeviceInfo &dev, int fmt, const uint8_t *w, const int8_t *xq, const float *xd,
+                           float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
 // GEMV: returns cudaErrorInvalidValue when m*k is too large for the shared-memory plan.
 bool gemv_supported(const DeviceInfo &dev, int64_t m, int64_t k);
 cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *w, float *const *y,

@@ -52,6 +52,35 @@ def activations_f32(m: int, k: int, kind: str = "normal", seed: int = ACT_SEED,
     return x
 
 
+KQUANT_LAYOUT = {
+    # bytes per 256-weight superblock, and the byte offsets of its binary16 scale fields
+    "q6_k": (210, (208,)),
+    "q4_k": (144, (0, 2)),
+    "q5_k": (176, (0, 2)),
+}
+
+
+def kquant_superblocks(fmt: str, n: int, k: int, seed: int = WEIGHT_SEED) -> np.ndarray:
+    """uint8 [n, k/256 * bytes] of K-quant superblocks: every code and sub-block scale byte
+    drawn uniformly from all its bit patterns, and each binary16 scale field (d, and dmin for
+    Q4_K / Q5_K) a positive binary16 with a uniformly drawn fraction and an exponent field in
+    5..8 (2^-10 .. 2^-7 times 1..2).  Random bits cover every code, every sub-block scale
+    and min and every sign of the Q6_K scales; the weight magnitudes (up to ~16 for Q6_K) are
+    not those of a trained model, which neither the exact integers nor the relative error
+    bound depend on."""
+    nbytes, scale_offsets = KQUANT_LAYOUT[fmt]
+    rng = _rng(seed)
+    nsb = n * (k // 256)
+    sb = rng.integers(0, 256, size=(nsb, nbytes), dtype=np.uint16).astype(np.uint8)
+    for off in scale_offsets:
+        frac = rng.integers(0, 1024, size=nsb, dtype=np.uint16)
+        expo = rng.integers(5, 9, size=nsb, dtype=np.uint16)
+        bits = (expo << 10) | frac
+        sb[:, off] = (bits & 0xFF).astype(np.uint8)
+        sb[:, off + 1] = (bits >> 8).astype(np.uint8)
+    return sb.reshape(n, (k // 256) * nbytes)
+
+
 # The serving shapes the pages time (decode_kernel_census.rs main, accprobe_bench.rs): each
 # case is (name, m, n, k, activation kind).
 GEMV_CASES = [

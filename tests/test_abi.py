@@ -127,6 +127,14 @@ S0 = 0               # legacy stream handle
     (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, A, 16, 8, 300, S0), q8.Q8ACT_ERR_DIMS),
     (lambda: q8.q8act_gemm_q8_0_noalloc(A, A, A, 2892, 8, 4096, S0), q8.Q8ACT_ERR_WORKSPACE),
     (lambda: q8.q8act_debug_wait_timeout(0, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_dequant_q6_k_f16(A, None, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_dequant_q4_k_f16(A, A, 8, 100, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_dequant_q5_k_f16(MIS, A, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_gemv_q6_k(A, A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
+    (lambda: q8.q8act_gemv_q4_k(A, A, A, A, 9, 8, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q5_k(A, A, A, A, 1, 0, 256, S0), q8.Q8ACT_ERR_DIMS),
+    (lambda: q8.q8act_gemv_q5_k(A, MIS, A, A, 1, 8, 256, S0), q8.Q8ACT_ERR_ALIGN),
+    (lambda: q8.q8act_debug_gemv_q6_k_block_dots(A, A, None, 1, 8, 256, S0), q8.Q8ACT_ERR_NULL),
     (lambda: q8.q8act_debug_wait_timeout(10 ** 10, S0), q8.Q8ACT_ERR_DIMS),
 ])
 def test_host_side_refusals(L, call, want):
