@@ -337,6 +337,12 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public API: host f32 in (pinned), host f32 out ----
     e2e = run_e2e(args, q8, torch, dev, stream)
 
+    # ---- every configuration of the workload table ----
+    configs = None
+    if not args.no_configs:
+        configs = run_configs(args, q8, torch, dev, stream, load_peaks(), flush_l2,
+                              {(GEMV["n"], GEMV["k"]): w_gemv, (GEMM["n"], GEMM["k"]): w_gemm})
+
     if rank != 0:
         return None
     peaks = load_peaks()
@@ -400,6 +406,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "configs": configs,
         "gpu_launches": sum(launches_per_step.values()) * args.steps,
         "clocks": clocks,
         "impl": "ours",
@@ -491,6 +498,197 @@ def run_e2e(args, q8, torch, dev, stream):
 
 
 # ------------------------------------------------------------------------------------
+# every configuration of the workload table, one row each
+# ------------------------------------------------------------------------------------
+def cpu_description():
+    """The host CPU's model name and core count (lscpu on Arm, /proc/cpuinfo elsewhere)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    return {"model": model or "unknown", "nproc": os.cpu_count()}
+
+
+def time_events(fn, reps, warmup, stream, torch, flush=None):
+    """CUDA-event time of each of `reps` calls (ms), after `warmup` untimed ones; `flush` runs
+    before every call, outside the events."""
+    for _ in range(warmup):
+        if flush:
+            flush()
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        if flush:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def oracle_time(wf32_rows, x, k, sample_rows, n):
+    """Seconds the single-threaded oracle takes for the whole configuration: its q8_1
+    quantization of x plus the fold over `sample_rows` weight rows, scaled by n / sample_rows
+    (exact when the sample is every row)."""
+    import oracle
+    oracle.build()
+    wb = oracle.quantize_q8_0(wf32_rows)
+    t0 = time.perf_counter()
+    xq, xd = oracle.quantize_q8_1(x)
+    t1 = time.perf_counter()
+    oracle.matmul(wb, xq, xd, k)
+    t2 = time.perf_counter()
+    return (t1 - t0) + (t2 - t1) * n / sample_rows
+
+
+def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
+    """Each configuration of the workload table: the GEMV rows (m = 1..8, pre-quantized activation,
+    as the pages' decode census times mmvq), the fused-quantize GEMMs on raw Q8_0 and on the
+    load-time repack, and the fp16 dequants.  Per row: median and mean us per call, throughput,
+    the fraction of the measured peak, and the oracle's time for the same configuration on the
+    same seeded inputs (a row sample scaled to all rows, marked extrapolated)."""
+    from q8_block_quantized_act_gb300 import inputs
+    reps = max(5, min(args.config_reps, 200))
+    rows_out = []
+    weights = dict(resident)           # (n, k) -> device Q8_0 bytes already built by the step
+    host_rows = {}
+
+    def wq(n, k):
+        if (n, k) not in weights:
+            w32 = torch.from_numpy(inputs.weights_f32(n, k)).to(dev)
+            weights[(n, k)] = q8.quantize_q8_0(w32)
+            del w32
+        if (n, k) not in host_rows:
+            # the generator fills rows in order: these are the matrix's first rows
+            host_rows[(n, k)] = inputs.weights_f32(min(n, 512), k)
+        return weights[(n, k)]
+
+    def orc(n, k, x, sample):
+        sample = min(sample, n)
+        return oracle_time(host_rows[(n, k)][:sample], x, k, sample, n), sample < n, sample
+
+    for name, m, n, k, kind in inputs.GEMV_CASES:
+        w = wq(n, k)
+        x = inputs.activations_f32(m, k, kind=kind)
+        xq, xd = q8.quantize_q8_1(torch.from_numpy(x).to(dev))
+        y = torch.empty((m, n), dtype=torch.float32, device=dev)
+        big = n * row_bytes(k) > 200e6
+
+        def fn():
+            q8.check(q8.q8act_gemv_q8_0(w, xq, xd, y, m, n, k, stream))
+
+        t = time_events(fn, reps, 3, stream, torch, None if big else flush_l2)
+        med, mean = float(np.median(t)), float(np.mean(t))
+        by = gemv_bytes(m, n, k)
+        o_s, extrap, smp = (None, None, None) if args.no_cpu_baseline else orc(n, k, x, 512)
+        rows_out.append({"config": name, "op": "gemv", "m": m, "n": n, "k": k, "act": kind,
+                         "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
+                         "gbs": round(by / (med * 1e-3) / 1e9, 1), "bound": "hbm",
+                         "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "l2": "resident weights larger than L2" if big else "flushed before each call",
+                         "oracle_s": None if o_s is None else round(o_s, 4), "oracle_extrapolated": extrap,
+                         "oracle_rows": smp})
+    ws = None
+    for name, m, n, k, kind in inputs.GEMM_CASES:
+        w = wq(n, k)
+        wq16, wdt = q8.repack_q8_0(w, n, k)
+        x = inputs.activations_f32(m, k, kind=kind)
+        x_d = torch.from_numpy(x).to(dev)
+        y = torch.empty((m, n), dtype=torch.float32, device=dev)
+        need = q8.q8act_gemm_workspace_bytes(m, k)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+        def raw():
+            q8.check(q8.q8act_gemm_q8_0(w, x_d, y, m, n, k, ws, ws.numel(), stream))
+
+        def rp():
+            q8.check(q8.q8act_gemm_q8_0_repacked(wq16, wdt, x_d, y, m, n, k, ws, ws.numel(), stream))
+
+        fl = gemm_flops(m, n, k)
+        o_s, extrap, smp = (None, None, None) if args.no_cpu_baseline else orc(n, k, x, 32)
+        for variant, fn in (("raw", raw), ("repacked", rp)):
+            t = time_events(fn, max(5, reps // 4) if fl > 1e11 else reps, 3, stream, torch, flush_l2)
+            med, mean = float(np.median(t)), float(np.mean(t))
+            tf = fl / (med * 1e-3) / 1e12
+            rows_out.append({"config": name, "op": f"gemm_{variant}", "m": m, "n": n, "k": k, "act": kind,
+                             "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
+                             "tflops": round(tf, 1), "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),
+                             "l2": "flushed before each call",
+                             "oracle_s": None if o_s is None else round(o_s, 3), "oracle_extrapolated": extrap,
+                             "oracle_rows": smp})
+        del wq16, wdt, x_d, y
+    for n, k in ((4096, 4096), (5152, 4096)):
+        w = wq(n, k)
+        w16 = torch.empty((n, k), dtype=torch.float16, device=dev)
+
+        def deq():
+            q8.check(q8.q8act_dequant_q8_0_f16(w, w16, n, k, stream))
+
+        t = time_events(deq, reps, 3, stream, torch, flush_l2)
+        med, mean = float(np.median(t)), float(np.mean(t))
+        by = dequant_bytes(n, k)
+        rows_out.append({"config": f"dequant_{k}x{n}", "op": "dequant_q8_0_f16", "m": 0, "n": n, "k": k,
+                         "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
+                         "gbs": round(by / (med * 1e-3) / 1e9, 1), "bound": "hbm",
+                         "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "l2": "flushed before each call", "oracle_s": None, "oracle_extrapolated": None,
+                         "oracle_rows": None})
+    # K-quant superblocks (Q6_K, Q4_K, Q5_K): the fp16 mirror of a 4096 x 4096 weight and the
+    # m = 1 GEMV at 4096 -> 64448, on seeded random superblocks
+    xq1, xd1 = q8.quantize_q8_1(torch.from_numpy(inputs.activations_f32(1, 4096)).to(dev))
+    for fmt, sbytes in (("q6_k", 210), ("q4_k", 144), ("q5_k", 176)):
+        for n, k, what in ((4096, 4096, "dequant"), (64448, 4096, "gemv")):
+            wk = torch.from_numpy(inputs.kquant_superblocks(fmt, n, k)).to(dev)
+            wbytes = n * (k // 256) * sbytes
+            if what == "dequant":
+                w16 = torch.empty((n, k), dtype=torch.float16, device=dev)
+                fn_dq = getattr(q8, f"q8act_dequant_{fmt}_f16")
+
+                def kq():
+                    q8.check(fn_dq(wk, w16, n, k, stream))
+                by = wbytes + 2 * n * k
+                big = False
+            else:
+                yk = torch.empty((1, n), dtype=torch.float32, device=dev)
+                fn_gv = getattr(q8, f"q8act_gemv_{fmt}")
+
+                def kq():
+                    q8.check(fn_gv(wk, xq1, xd1, yk, 1, n, k, stream))
+                by = wbytes + k + (k // 32) * 4 + n * 4
+                big = True
+            t = time_events(kq, reps, 3, stream, torch, None if big else flush_l2)
+            med, mean = float(np.median(t)), float(np.mean(t))
+            rows_out.append({"config": f"{what}_{fmt}_{k}x{n}", "op": f"{what}_{fmt}", "m": 1 if what == "gemv" else 0,
+                             "n": n, "k": k, "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
+                             "gbs": round(by / (med * 1e-3) / 1e9, 1), "bound": "hbm",
+                             "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                             "l2": "weights larger than L2" if big else "flushed before each call",
+                             "oracle_s": None, "oracle_extrapolated": None, "oracle_rows": None})
+            del wk
+    torch.cuda.synchronize()
+    q8.device_status(stream)
+    cpu = cpu_description()
+    cpu["oracle_threads"] = 1
+    return {"rows": rows_out, "reps": reps, "cpu": cpu,
+            "note": "GEMV rows: the pre-quantized-activation GEMV (as the pages' census times mmvq); GEMM rows: "
+                    "the whole fused call (q8_1 quantize + GEMM); oracle_s: the single-threaded C oracle on "
+                    "the same inputs (q8_1 quantize + fold), timed on oracle_rows weight rows and scaled to n "
+                    "(oracle_extrapolated)"}
+
+
+# ------------------------------------------------------------------------------------
 # the CPU oracle (reference arm and cpu_baseline)
 # ------------------------------------------------------------------------------------
 def oracle_gemv_sample(min_seconds=10.0, max_seconds=30.0, rows_per_rep=16384):
@@ -558,6 +756,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
+    ap.add_argument("--config-reps", type=int, default=40, help="timed calls per configuration row")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
