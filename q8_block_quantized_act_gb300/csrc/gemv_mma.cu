@@ -56,11 +56,16 @@ struct MPlan {
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-MPlan make_mplan(int mt, int64_t k, size_t smem_cap, int block_bytes)
+// rt_cap: at most this many 16-row tiles per chunk.  A chunk takes enough tiles to give each
+// MMA warp an item (16 / G of them), unless the matrix is then cut into fewer chunks than
+// there are SMs: short rows (k = 1280: five groups per row) on a 4096-row matrix would give
+// 64 chunks of 64 rows, leaving most SMs idle, so fewer tiles per chunk are taken there.
+MPlan make_mplan(int mt, int64_t k, size_t smem_cap, int block_bytes, int rt_cap = 1 << 20)
 {
     MPlan p{};
     p.G = (int)(k / 256);
     p.RT = (NW + p.G - 1) / p.G;
+    if (p.RT > rt_cap) p.RT = rt_cap;
     if (p.RT < 1) p.RT = 1;
     p.R = 16 * p.RT;
     p.items = p.RT * p.G;
@@ -447,7 +452,17 @@ template <class F, int MT, bool DOTS>
 cudaError_t launch_mt(const DeviceInfo &dev, Group grp, const int8_t *xq, const float *xd, int32_t *dots, int64_t m,
                       int64_t k, cudaStream_t stream, bool pdl)
 {
-    MPlan p = make_mplan(MT, k, dev.max_smem_optin, F::BLOCK_BYTES);
+    // 16-row tiles of the whole group, and the most tiles per chunk that still give every SM
+    // a chunk (when the matrix has that many tiles at all)
+    int64_t tiles = 0;
+    for (int i = 0; i < grp.count; ++i) tiles += (grp.n[i] + 15) / 16;
+    int rt_cap = 1 << 20;
+    {
+        const int g = (int)(k / 256), rt0 = (NW + g - 1) / g;
+        for (rt_cap = rt0 > 1 ? rt0 : 1; rt_cap > 1 && tiles / rt_cap < dev.num_sms; --rt_cap) {
+        }
+    }
+    MPlan p = make_mplan(MT, k, dev.max_smem_optin, F::BLOCK_BYTES, rt_cap);
     if (!mplan_ok(p, MT)) return cudaErrorInvalidValue;
     if (DOTS && grp.count != 1) return cudaErrorInvalidValue;   // the export serves one matrix
     grp.first_chunk[0] = 0;

@@ -87,9 +87,12 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__rest
 }
 
 // x [m][k] f32 -> xqh [m][k] binary16 (exact small integers), xdt [k/32][ldm] f32.
-// Grid: (ceil(k/4 / 256), min(m, 65535)); thread (token t = blockIdx.y + i * gridDim.y,
-// chunk c of its row).  k/4 is a multiple of 64, so every warp is either fully inside the
-// row or fully past its end.
+// Grid: (ceil(k/4 / 256), min(ceil(m / MMQ_TPT), 65535)); thread (chunk c of the row of each
+// of its tokens t = blockIdx.y + (i * MMQ_TPT + j) * gridDim.y).  A thread loads its MMQ_TPT
+// tokens' chunks before quantizing any of them (loads in flight); k/4 is a multiple of 64 and
+// the token test is the same for every lane of a warp, so every warp is either fully inside
+// a row or fully past its end, as the block's shuffles need.
+constexpr int MMQ_TPT = 4;
 __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__restrict__ x,
                                                                 uint2 *__restrict__ xqh,
                                                                 float *__restrict__ xdt,
@@ -101,14 +104,26 @@ __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__
     griddep_launch_dependents();
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= chunks_per_row) return;
-    for (int64_t t = blockIdx.y; t < m; t += gridDim.y) {
-        const int64_t g = t * chunks_per_row + c;
-        Block4 b = quantize4(load_stream(x + g));
-        uint32_t h[4];
+    const int64_t ys = gridDim.y;
+    for (int64_t t0 = blockIdx.y; t0 < m; t0 += ys * MMQ_TPT) {
+        float4 v[MMQ_TPT];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__int2half_rn(b.q[j]));
-        xqh[g] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-        if ((c & 7) == 0) xdt[(int64_t)(c >> 3) * ldm + t] = b.d;
+        for (int j = 0; j < MMQ_TPT; ++j) {
+            const int64_t t = t0 + j * ys;
+            v[j] = t < m ? load_stream(x + t * chunks_per_row + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < MMQ_TPT; ++j) {
+            const int64_t t = t0 + j * ys;
+            if (t >= m) break;
+            const int64_t g = t * chunks_per_row + c;
+            Block4 b = quantize4(v[j]);
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = __half_as_ushort(__int2half_rn(b.q[e]));
+            xqh[g] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+            if ((c & 7) == 0) xdt[(int64_t)(c >> 3) * ldm + t] = b.d;
+        }
     }
 }
 
@@ -213,7 +228,8 @@ cudaError_t launch_quantize_q8_1_mmq(const DeviceInfo &dev, const float *x, uint
 {
     const int cpr = (int)(k / 4);
     set_max_carveout(quantize_q8_1_mmq_kernel);
-    const dim3 grid((unsigned)((cpr + 255) / 256), (unsigned)(m < 65535 ? m : 65535));
+    const int64_t gy = (m + MMQ_TPT - 1) / MMQ_TPT;
+    const dim3 grid((unsigned)((cpr + 255) / 256), (unsigned)(gy < 65535 ? gy : 65535));
     quantize_q8_1_mmq_kernel<<<grid, 256, 0, stream>>>(
         reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xqh), xdt, m, cpr, ldm);
     return cudaGetLastError();
