@@ -72,13 +72,15 @@ __device__ __forceinline__ void load_superblock(const uint8_t *p, uint32_t (&w)[
     }
 }
 
-// Byte i (0..11) of the Q4_K / Q5_K scale bytes, which occupy words 1..3.
-template <int N>
-__device__ __forceinline__ uint32_t sbyte(const uint32_t (&w)[N], int i) { return (w[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu; }
-
+// The 6-bit scale and min of sub-block j from the 12 scale bytes held in words w[1..3] (selects
+// rather than an indexed register array, so that a lane-dependent j stays in registers).
 __device__ __forceinline__ void k4_scale_min(const uint32_t *w, int j, int &sc, int &mn)
 {
-    auto b = [&](int i) { return (int)((w[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu); };
+    const uint32_t w1 = w[1], w2 = w[2], w3 = w[3];
+    auto b = [&](int i) {
+        const uint32_t x = i < 4 ? w1 : (i < 8 ? w2 : w3);
+        return (int)((x >> (8 * (i & 3))) & 0xFFu);
+    };
     if (j < 4) {
         sc = b(j) & 63;
         mn = b(j + 4) & 63;
@@ -169,6 +171,73 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// The bytes lane j needs for weights e0 = 8j .. 8j + 7 of a superblock, read from shared
+// memory (load), and those weights' binary16-bound values (values).
+template <class F, bool Q6 = F::BYTES == KQ6::BYTES>
+struct KqPiece;
+
+template <class F>
+struct KqPiece<F, true> {
+    uint32_t ql0, ql1, qh0, qh1, head;   // 8 ql bytes, 8 qh bytes, d and the scale byte
+    __device__ void load(const uint8_t *sb, int e0)
+    {
+        const int h = e0 >> 7, pp = e0 & 127, g = pp >> 5, l0 = pp & 31;
+        const uint8_t *ql = sb + 64 * h + 32 * (g & 1) + l0;   // 2-byte aligned
+        const uint8_t *qh = sb + 128 + 32 * h + l0;
+        const uint16_t *a = reinterpret_cast<const uint16_t *>(ql), *b = reinterpret_cast<const uint16_t *>(qh);
+        ql0 = a[0] | ((uint32_t)a[1] << 16);
+        ql1 = a[2] | ((uint32_t)a[3] << 16);
+        qh0 = b[0] | ((uint32_t)b[1] << 16);
+        qh1 = b[2] | ((uint32_t)b[3] << 16);
+        head = *reinterpret_cast<const uint16_t *>(sb + 208) | ((uint32_t)sb[192 + (e0 >> 4)] << 16);
+    }
+    __device__ void values(int e0, float (&v)[8]) const
+    {
+        const int g = (e0 & 127) >> 5;
+        const float d = half_bits_to_float(head & 0xffffu);
+        const float ds = __fmul_rn(d, (float)(int8_t)(head >> 16));   // exact
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t qlb = ((c < 4 ? ql0 : ql1) >> (8 * (c & 3))) & 0xFFu;
+            const uint32_t qhb = ((c < 4 ? qh0 : qh1) >> (8 * (c & 3))) & 0xFFu;
+            const int code = (int)((qlb >> (4 * (g >> 1))) & 15u) | (int)(((qhb >> (2 * g)) & 3u) << 4);
+            v[c] = __fmul_rn(ds, (float)(code - 32));                     // exact
+        }
+    }
+};
+
+template <class F>
+struct KqPiece<F, false> {
+    uint32_t head[4];
+    uint2 qv, hv;
+    __device__ void load(const uint8_t *sb, int e0)
+    {
+        const uint4 hd = *reinterpret_cast<const uint4 *>(sb);
+        head[0] = hd.x; head[1] = hd.y; head[2] = hd.z; head[3] = hd.w;
+        const int g = e0 >> 6, l0 = e0 & 31;
+        constexpr int QS = F::BYTES == KQ4::BYTES ? 16 : 48;
+        qv = *reinterpret_cast<const uint2 *>(sb + QS + 32 * g + l0);
+        hv = make_uint2(0, 0);
+        if constexpr (F::BYTES == KQ5::BYTES) hv = *reinterpret_cast<const uint2 *>(sb + 16 + l0);
+    }
+    __device__ void values(int e0, float (&v)[8]) const
+    {
+        const int u2 = (e0 >> 5) & 1, j = e0 >> 5;
+        int sc, mn;
+        k4_scale_min(head, j, sc, mn);
+        const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
+        const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);   // exact
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t qb = ((c < 4 ? qv.x : qv.y) >> (8 * (c & 3))) & 0xFFu;
+            int code = (int)((qb >> (4 * u2)) & 15u);
+            if constexpr (F::BYTES == KQ5::BYTES)
+                code += 16 * (int)((((c < 4 ? hv.x : hv.y) >> (8 * (c & 3))) >> j) & 1u);
+            v[c] = sub_round_odd(__fmul_rn(dsc, (float)code), dmm);
+        }
+    }
+};
+
 template <class F>
 __global__ void __launch_bounds__(DQ_THREADS, 2)
     kq_dequant_kernel(const uint8_t *__restrict__ w, uint4 *__restrict__ out, int n, int k, KPlan p, int *status)
@@ -216,44 +285,26 @@ __global__ void __launch_bounds__(DQ_THREADS, 2)
         const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
         const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
         const int units = rows * p.G;
-        for (int u = warp; u < units; u += DQ_WARPS) {
-            const uint8_t *sb = sbase + (size_t)u * F::BYTES;
-            float v[8];
-            if constexpr (F::BYTES == KQ6::BYTES) {
-                const int h = e0 >> 7, pp = e0 & 127, g = pp >> 5, l0 = pp & 31;
-                const uint8_t *ql = sb + 64 * h + 32 * (g & 1) + l0;
-                const uint8_t *qh = sb + 128 + 32 * h + l0;
-                const float d = half_bits_to_float((uint32_t)sb[208] | ((uint32_t)sb[209] << 8));
-                const float ds = __fmul_rn(d, (float)(int8_t)sb[192 + (e0 >> 4)]);   // exact
+        // Two superblocks per warp step: both are read from shared memory before either is
+        // converted (more loads in flight per warp).
+        constexpr int UNR = 2;
+        for (int u0 = warp; u0 < units; u0 += UNR * DQ_WARPS) {
+            KqPiece<F> pc[UNR];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int code = (((int)ql[c] >> (4 * (g >> 1))) & 15) | ((((int)qh[c] >> (2 * g)) & 3) << 4);
-                    v[c] = __fmul_rn(ds, (float)(code - 32));                        // exact
-                }
-            } else {
-                const uint32_t *sw = reinterpret_cast<const uint32_t *>(sb);
-                uint32_t head[4] = {sw[0], sw[1], sw[2], sw[3]};
-                const int g = e0 >> 6, u2 = (e0 >> 5) & 1, l0 = e0 & 31, j = e0 >> 5;
-                int sc, mn;
-                k4_scale_min(head, j, sc, mn);
-                const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
-                const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);   // exact
-                constexpr int QS = F::BYTES == KQ4::BYTES ? 16 : 48;
-                const uint2 qv = *reinterpret_cast<const uint2 *>(sb + QS + 32 * g + l0);
-                uint2 hv = make_uint2(0, 0);
-                if constexpr (F::BYTES == KQ5::BYTES) hv = *reinterpret_cast<const uint2 *>(sb + 16 + l0);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t qb = ((c < 4 ? qv.x : qv.y) >> (8 * (c & 3))) & 0xFFu;
-                    int code = (int)((qb >> (4 * u2)) & 15u);
-                    if constexpr (F::BYTES == KQ5::BYTES)
-                        code += 16 * (int)((((c < 4 ? hv.x : hv.y) >> (8 * (c & 3))) >> j) & 1u);
-                    v[c] = sub_round_odd(__fmul_rn(dsc, (float)code), dmm);
-                }
+            for (int e = 0; e < UNR; ++e) {
+                const int u = u0 + e * DQ_WARPS;
+                pc[e].load(sbase + (size_t)(u < units ? u : u0) * F::BYTES, e0);
             }
-            const int row = u / p.G, gsb = u - row * p.G;
-            const uint4 o = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
-            __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)gsb * QK_K) / 8 + lane, o);
+#pragma unroll
+            for (int e = 0; e < UNR; ++e) {
+                const int u = u0 + e * DQ_WARPS;
+                if (u >= units) break;
+                float v[8];
+                pc[e].values(e0, v);
+                const int row = u / p.G, gsb = u - row * p.G;
+                const uint4 o = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
+                __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)gsb * QK_K) / 8 + lane, o);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -359,7 +410,7 @@ __device__ __forceinline__ bool kbar_red_or(int id, int nthreads, bool pred)
 // MM: the largest token count of the instance; the call's m (<= MM) tokens are folded, each
 // with the same operations in the same order for every MM (decode == verify).
 template <class F, int MM>
-__global__ void __launch_bounds__(GV_CONSUMERS + 32, 2)
+__global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
     kq_gemv_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq, const float *__restrict__ xd,
                    float *__restrict__ y, int32_t *__restrict__ dots, int m, int n, int k, KPlan p, int *status)
 {
@@ -535,10 +586,20 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, 2)
     }
 }
 
+// Three CTAs per SM when three stages fit in a third of shared memory (the consumers of these
+// formats work harder per streamed byte than Q8_0's, so more of them pay), else two when three
+// stages fit in half, else one CTA with as many stages as fit.
 template <class F>
 KPlan choose_gemv_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin, int *per_sm)
 {
-    const size_t half_sm = 113 * 1024;
+    const size_t third_sm = 74 * 1024, half_sm = 113 * 1024;
+    if (m <= 2) {
+        KPlan p3 = gemv_plan(m, n, k, F::BYTES, third_sm < smem_optin ? third_sm : smem_optin, GV_CONSUMERS);
+        if (p3.stages >= 3) {
+            *per_sm = 3;
+            return p3;
+        }
+    }
     KPlan p = gemv_plan(m, n, k, F::BYTES, half_sm < smem_optin ? half_sm : smem_optin, GV_CONSUMERS);
     if (p.stages >= 3) {
         *per_sm = 2;
@@ -560,6 +621,12 @@ cudaError_t launch_kq_gemv_m(const DeviceInfo &dev, const uint8_t *w, const int8
     if (p.stages < 2) return cudaErrorInvalidValue;
     cudaError_t e = set_kernel_smem<kq_gemv_kernel<F, MM>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
+    // never more CTAs than are resident at once (registers may allow fewer than the plan)
+    int resident = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kq_gemv_kernel<F, MM>, GV_CONSUMERS + 32, p.smem) ==
+            cudaSuccess &&
+        resident >= 1 && resident < per_sm)
+        per_sm = resident;
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
     kq_gemv_kernel<F, MM><<<(int)grid, GV_CONSUMERS + 32, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n,
