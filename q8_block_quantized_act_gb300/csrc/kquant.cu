@@ -586,16 +586,17 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
     }
 }
 
-// Three CTAs per SM when three stages fit in a third of shared memory (the consumers of these
-// formats work harder per streamed byte than Q8_0's, so more of them pay), else two when three
-// stages fit in half, else one CTA with as many stages as fit.
+// Three CTAs per SM when three stages (two for Q6_K, whose 27 KB chunks leave room for only
+// two) fit in a third of shared memory -- the consumers of these formats work harder per
+// streamed byte than Q8_0's, so more of them pay -- else two when three stages fit in half,
+// else one CTA with as many stages as fit.
 template <class F>
 KPlan choose_gemv_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin, int *per_sm)
 {
     const size_t third_sm = 74 * 1024, half_sm = 113 * 1024;
     if (m <= 2) {
         KPlan p3 = gemv_plan(m, n, k, F::BYTES, third_sm < smem_optin ? third_sm : smem_optin, GV_CONSUMERS);
-        if (p3.stages >= 3) {
+        if (p3.stages >= (F::BYTES == KQ6::BYTES ? 2 : 3)) {
             *per_sm = 3;
             return p3;
         }
