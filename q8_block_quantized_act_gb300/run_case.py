@@ -4,7 +4,9 @@
     python -m q8_block_quantized_act_gb300.run_case gemm --m 512 --n 4096 --k 4096 --reps 2
 
 Kernels: quantize (q8_1), quantize_mmq, quantize_q8_0, gemv, gemm (fused quantize),
-gemm_preq, gemm_repacked (fused quantize, load-time repacked weights), repack, dequant.
+gemm_preq, gemm_repacked (fused quantize, load-time repacked weights), repack, dequant,
+gemv_q4_0, dequant_q4_0, and the K-quant passes gemv_q6_k / gemv_q4_k / gemv_q5_k and
+dequant_q6_k / dequant_q4_k / dequant_q5_k (on seeded random superblocks).
 Inputs are the seeded synthetic ones of q8_block_quantized_act_gb300.inputs;
 one warm-up launch precedes the `--reps` launches.
 """
@@ -17,7 +19,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", choices=("quantize", "quantize_mmq", "quantize_q8_0", "gemv", "gemm",
                                        "gemm_preq", "gemm_repacked", "repack", "dequant", "gemv_q4_0",
-                                       "dequant_q4_0"))
+                                       "dequant_q4_0", "gemv_q6_k", "gemv_q4_k", "gemv_q5_k",
+                                       "dequant_q6_k", "dequant_q4_k", "dequant_q5_k"))
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=4096)
@@ -40,6 +43,8 @@ def main(argv=None):
           if a.kernel in ("gemv_q4_0", "dequant_q4_0") else None)
     xq, xd = q8.quantize_q8_1(x)
     xqh, xdt = q8.quantize_q8_1_mmq(x)
+    kq = a.kernel.split("_", 1)[1] if a.kernel.endswith("_k") else None   # "q6_k", "q4_k", "q5_k"
+    wk = torch.from_numpy(inputs.kquant_superblocks(kq, n, k)).to(dev) if kq else None
     ws = q8.gemm_workspace(m, k, dev) if a.kernel in ("gemm", "gemm_repacked") else None
     wq16, wdt = q8.repack_q8_0(w, n, k) if a.kernel in ("gemm_repacked", "repack") else (None, None)
     torch.cuda.synchronize()
@@ -65,6 +70,10 @@ def main(argv=None):
             q8.gemv_q4_0(w4, xq, xd, n)
         elif a.kernel == "dequant_q4_0":
             q8.dequant_q4_0_f16(w4, n, k)
+        elif kq and a.kernel.startswith("gemv"):
+            q8.gemv_kq(kq, wk, xq, xd, n)
+        elif kq:
+            q8.dequant_kq_f16(kq, wk, n, k)
         else:
             q8.dequant_q8_0_f16(w, n, k)
 
