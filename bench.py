@@ -593,6 +593,41 @@ def time_b2b(fns, reps, stream, torch):
     return a.elapsed_time(b) / reps
 
 
+def graph_fields(ms, nbytes, peaks):
+    if ms is None:
+        return {"us_graph": None, "gbs_graph": None, "frac_graph": None}
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"us_graph": round(ms * 1e3, 2), "gbs_graph": round(gbs, 1), "frac_graph": round(gbs / peaks["hbm_gbs"], 4)}
+
+
+def time_graph(fns, reps, torch):
+    """Mean ms per call when the `reps` calls (cycling through `fns`, each closure issuing its
+    call on torch's current stream) are captured once into a CUDA graph and replayed: the
+    device's own time per call in a sequence, without the host's per-call launch cost.  None
+    when the capture is refused."""
+    try:
+        for f in fns[:3]:
+            f()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                fns[i % len(fns)]()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        del g
+        return ms
+    except Exception:   # capture unsupported in this environment: no graph figure
+        torch.cuda.synchronize()
+        return None
+
+
 def n_copies(nbytes, cap=32):
     """Weight copies whose total exceeds twice L2 (at most `cap`)."""
     return max(1, min(cap, -(-2 * L2_BYTES // max(1, nbytes))))
@@ -654,9 +689,10 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
         by = gemv_bytes(m, n, k)
         copies = [w] + [w.clone() for _ in range(n_copies(n * row_bytes(k)) - 1)]
 
-        def mk(wc):
-            return lambda: q8.check(q8.q8act_gemv_q8_0(wc, xq, xd, y, m, n, k, stream))
+        def mk(wc, st=stream):
+            return lambda: q8.check(q8.q8act_gemv_q8_0(wc, xq, xd, y, m, n, k, st))
         b2b = time_b2b([mk(wc) for wc in copies], max(reps, 4 * len(copies)), stream, torch)
+        gr = time_graph([mk(wc, None) for wc in copies], max(reps, 4 * len(copies)), torch)
         del copies
         o_s, extrap, smp = (None, None, None) if args.no_cpu_baseline else orc(n, k, x, 512)
         rows_out.append({"config": name, "op": "gemv", "m": m, "n": n, "k": k, "act": kind,
@@ -665,6 +701,7 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
                          "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                          "us_b2b": round(b2b * 1e3, 2), "gbs_b2b": round(by / (b2b * 1e-3) / 1e9, 1),
                          "frac_b2b": round(by / (b2b * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         **graph_fields(gr, by, peaks),
                          "b2b_weight_copies": n_copies(n * row_bytes(k)),
                          "l2": "resident weights larger than L2" if big else "flushed before each call",
                          "oracle_s": None if o_s is None else round(o_s, 4), "oracle_extrapolated": extrap,
@@ -698,24 +735,30 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
             if variant == "raw":
                 cps = [w] + [w.clone() for _ in range(ncp - 1)]
 
-                def mk(wc):
-                    return lambda: q8.check(q8.q8act_gemm_q8_0(wc, x_d, y, m, n, k, ws, ws.numel(), stream))
+                def mk(wc, st=stream):
+                    return lambda: q8.check(q8.q8act_gemm_q8_0(wc, x_d, y, m, n, k, ws, ws.numel(), st))
                 fns = [mk(wc) for wc in cps]
+                gfns = [mk(wc, None) for wc in cps]
             else:
                 cps = [(wq16, wdt)] + [(wq16.clone(), wdt.clone()) for _ in range(ncp - 1)]
 
-                def mk(pr):
+                def mk(pr, st=stream):
                     return lambda: q8.check(q8.q8act_gemm_q8_0_repacked(pr[0], pr[1], x_d, y, m, n, k, ws, ws.numel(),
-                                                                        stream))
+                                                                        st))
                 fns = [mk(pr) for pr in cps]
+                gfns = [mk(pr, None) for pr in cps]
             b2b = time_b2b(fns, max(nrep, 2 * len(fns)), stream, torch)
-            del fns, cps
+            gr = time_graph(gfns, max(nrep, 2 * len(fns)), torch)
+            del fns, gfns, cps
             tfb = fl / (b2b * 1e-3) / 1e12
             rows_out.append({"config": name, "op": f"gemm_{variant}", "m": m, "n": n, "k": k, "act": kind,
                              "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
                              "tflops": round(tf, 1), "bound": "tensor", "frac": round(tf / peaks["bf16_tflops"], 4),
                              "us_b2b": round(b2b * 1e3, 2), "tflops_b2b": round(tfb, 1),
                              "frac_b2b": round(tfb / peaks["bf16_tflops"], 4), "b2b_weight_copies": ncp,
+                             "us_graph": None if gr is None else round(gr * 1e3, 2),
+                             "tflops_graph": None if gr is None else round(fl / (gr * 1e-3) / 1e12, 1),
+                             "frac_graph": None if gr is None else round(fl / (gr * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                              "l2": "flushed before each call",
                              "oracle_s": None if o_s is None else round(o_s, 3), "oracle_extrapolated": extrap,
                              "oracle_rows": smp})
@@ -732,9 +775,10 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
         by = dequant_bytes(n, k)
         cps = [w] + [w.clone() for _ in range(n_copies(n * row_bytes(k)) - 1)]
 
-        def mk(wc):
-            return lambda: q8.check(q8.q8act_dequant_q8_0_f16(wc, w16, n, k, stream))
+        def mk(wc, st=stream):
+            return lambda: q8.check(q8.q8act_dequant_q8_0_f16(wc, w16, n, k, st))
         b2b = time_b2b([mk(wc) for wc in cps], max(reps, 4 * len(cps)), stream, torch)
+        gr = time_graph([mk(wc, None) for wc in cps], max(reps, 4 * len(cps)), torch)
         del cps
         rows_out.append({"config": f"dequant_{k}x{n}", "op": "dequant_q8_0_f16", "m": 0, "n": n, "k": k,
                          "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
@@ -742,6 +786,7 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
                          "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                          "us_b2b": round(b2b * 1e3, 2), "gbs_b2b": round(by / (b2b * 1e-3) / 1e9, 1),
                          "frac_b2b": round(by / (b2b * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         **graph_fields(gr, by, peaks),
                          "l2": "flushed before each call", "oracle_s": None, "oracle_extrapolated": None,
                          "oracle_rows": None})
     # K-quant superblocks (Q6_K, Q4_K, Q5_K): the fp16 mirror of a 4096 x 4096 weight and the
@@ -772,17 +817,19 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
             ncp = n_copies(wbytes)
             cps = [wk] + [wk.clone() for _ in range(ncp - 1)]
             if what == "dequant":
-                fns = [(lambda wc: (lambda: q8.check(fn_dq(wc, w16, n, k, stream))))(wc) for wc in cps]
+                mkf = (lambda wc, st: (lambda: q8.check(fn_dq(wc, w16, n, k, st))))
             else:
-                fns = [(lambda wc: (lambda: q8.check(fn_gv(wc, xq1, xd1, yk, 1, n, k, stream))))(wc) for wc in cps]
-            b2b = time_b2b(fns, max(reps, 4 * ncp), stream, torch)
-            del fns, cps
+                mkf = (lambda wc, st: (lambda: q8.check(fn_gv(wc, xq1, xd1, yk, 1, n, k, st))))
+            b2b = time_b2b([mkf(wc, stream) for wc in cps], max(reps, 4 * ncp), stream, torch)
+            gr = time_graph([mkf(wc, None) for wc in cps], max(reps, 4 * ncp), torch)
+            del cps
             rows_out.append({"config": f"{what}_{fmt}_{k}x{n}", "op": f"{what}_{fmt}", "m": 1 if what == "gemv" else 0,
                              "n": n, "k": k, "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
                              "gbs": round(by / (med * 1e-3) / 1e9, 1), "bound": "hbm",
                              "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                              "us_b2b": round(b2b * 1e3, 2), "gbs_b2b": round(by / (b2b * 1e-3) / 1e9, 1),
                              "frac_b2b": round(by / (b2b * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                             **graph_fields(gr, by, peaks),
                              "b2b_weight_copies": ncp,
                              "l2": "weights larger than L2" if big else "flushed before each call",
                              "oracle_s": None, "oracle_extrapolated": None, "oracle_rows": None})
@@ -797,7 +844,9 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
                     "events after an L2 flush (includes the launch and the event pair, a few us); us_b2b: the "
                     "mean of calls issued back to back in one event pair, cycling through b2b_weight_copies "
                     "weight copies (more than twice L2 in total where the cap allows, so each call still reads "
-                    "its weights from HBM), the census's way of timing (it repeats one warm buffer).  "
+                    "its weights from HBM), the census's way of timing (it repeats one warm buffer); us_graph: "
+                    "the same calls captured once into a CUDA graph and replayed, the device's time per call "
+                    "without the host's per-call launch cost.  "
                     "oracle_s: the single-threaded C oracle on the same inputs (q8_1 quantize + fold), timed on "
                     "oracle_rows weight rows and scaled to n (oracle_extrapolated)"}
 
