@@ -157,22 +157,34 @@ constexpr int DQ_TARGET_CHUNK = 17408;
 
 // Round-to-odd difference of two f32 values: the truncated difference with its last bit set
 // when the difference is inexact.  Rounding that to binary16 (11 bits, far fewer than f32's
-// 24) gives the correctly rounded binary16 of the exact difference.
+// 24) gives the correctly rounded binary16 of the exact difference.  Inexactness is read from
+// the directed roundings without a compare: for a positive difference the rounding down is
+// the truncation and the rounding up is the next float (encoding + 1) when inexact; for a
+// negative one the roles swap.  Either way bit 0 of (up | down) is set exactly when the
+// truncation is odd or the difference inexact, which is the round-to-odd bit.
 __device__ __forceinline__ float sub_round_odd(float a, float b)
 {
-    const float z = __fsub_rz(a, b);
-    const bool inexact = __fsub_ru(a, b) != __fsub_rd(a, b);
-    return inexact ? __uint_as_float(__float_as_uint(z) | 1u) : z;
+    const uint32_t z = __float_as_uint(__fsub_rz(a, b));
+    const uint32_t t = __float_as_uint(__fsub_ru(a, b)) | __float_as_uint(__fsub_rd(a, b));
+    return __uint_as_float((z & ~1u) | (t & 1u));
+}
+
+// Byte b (0..3) of w as the f32 value 2^23 + byte: the byte placed under the exponent of 2^23.
+__device__ __forceinline__ float byte_magic(uint32_t w, int b)
+{
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u + (uint32_t)b));
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
-    const __half2 h = __halves2half2(__float2half_rn(lo), __float2half_rn(hi));
+    const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // The bytes lane j needs for weights e0 = 8j .. 8j + 7 of a superblock, read from shared
-// memory (load), and those weights' binary16-bound values (values).
+// memory (load), and those weights' values rounded once to binary16, packed in element order
+// (packed).  The codes are unpacked four to a word; each code becomes an exact f32 through
+// byte_magic and one exact subtraction, and every product below is exact in f32.
 template <class F, bool Q6 = F::BYTES == KQ6::BYTES>
 struct KqPiece;
 
@@ -191,18 +203,25 @@ struct KqPiece<F, true> {
         qh1 = b[2] | ((uint32_t)b[3] << 16);
         head = *reinterpret_cast<const uint16_t *>(sb + 208) | ((uint32_t)sb[192 + (e0 >> 4)] << 16);
     }
-    __device__ void values(int e0, float (&v)[8]) const
+    // value = d * scale * (code - 32): 11 + 7 + 5 significant bits, exact in f32.
+    __device__ uint4 packed(int e0) const
     {
         const int g = (e0 & 127) >> 5;
+        const uint32_t s1 = 4 * (g >> 1), s2 = 2 * g;
         const float d = half_bits_to_float(head & 0xffffu);
-        const float ds = __fmul_rn(d, (float)(int8_t)(head >> 16));   // exact
+        const float ds = __fmul_rn(d, (float)(int8_t)(head >> 16));
+        uint32_t o[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint32_t qlb = ((c < 4 ? ql0 : ql1) >> (8 * (c & 3))) & 0xFFu;
-            const uint32_t qhb = ((c < 4 ? qh0 : qh1) >> (8 * (c & 3))) & 0xFFu;
-            const int code = (int)((qlb >> (4 * (g >> 1))) & 15u) | (int)(((qhb >> (2 * g)) & 3u) << 4);
-            v[c] = __fmul_rn(ds, (float)(code - 32));                     // exact
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t ql = h ? ql1 : ql0, qh = h ? qh1 : qh0;
+            const uint32_t code = ((ql >> s1) & 0x0F0F0F0Fu) | (((qh >> s2) & 0x03030303u) << 4);
+            float v[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v[b] = __fmul_rn(ds, __fsub_rn(byte_magic(code, b), 8388640.0f));   // 2^23 + 32
+            o[2 * h] = pack_h2(v[0], v[1]);
+            o[2 * h + 1] = pack_h2(v[2], v[3]);
         }
+        return make_uint4(o[0], o[1], o[2], o[3]);
     }
 };
 
@@ -220,21 +239,28 @@ struct KqPiece<F, false> {
         hv = make_uint2(0, 0);
         if constexpr (F::BYTES == KQ5::BYTES) hv = *reinterpret_cast<const uint2 *>(sb + 16 + l0);
     }
-    __device__ void values(int e0, float (&v)[8]) const
+    // value = d * sc * code - dmin * mn: both products exact in f32 (11 + 6 + 5 and 11 + 6
+    // significant bits), their difference rounded once (to odd, then to binary16).
+    __device__ uint4 packed(int e0) const
     {
         const int u2 = (e0 >> 5) & 1, j = e0 >> 5;
         int sc, mn;
         k4_scale_min(head, j, sc, mn);
         const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
-        const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);   // exact
+        const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);
+        uint32_t o[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint32_t qb = ((c < 4 ? qv.x : qv.y) >> (8 * (c & 3))) & 0xFFu;
-            int code = (int)((qb >> (4 * u2)) & 15u);
-            if constexpr (F::BYTES == KQ5::BYTES)
-                code += 16 * (int)((((c < 4 ? hv.x : hv.y) >> (8 * (c & 3))) >> j) & 1u);
-            v[c] = sub_round_odd(__fmul_rn(dsc, (float)code), dmm);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t code = ((h ? qv.y : qv.x) >> (4 * u2)) & 0x0F0F0F0Fu;
+            if constexpr (F::BYTES == KQ5::BYTES) code |= (((h ? hv.y : hv.x) >> j) & 0x01010101u) << 4;
+            float v[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                v[b] = sub_round_odd(__fmul_rn(dsc, __fsub_rn(byte_magic(code, b), 8388608.0f)), dmm);
+            o[2 * h] = pack_h2(v[0], v[1]);
+            o[2 * h + 1] = pack_h2(v[2], v[3]);
         }
+        return make_uint4(o[0], o[1], o[2], o[3]);
     }
 };
 
@@ -299,10 +325,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 2)
             for (int e = 0; e < UNR; ++e) {
                 const int u = u0 + e * DQ_WARPS;
                 if (u >= units) break;
-                float v[8];
-                pc[e].values(e0, v);
+                const uint4 o = pc[e].packed(e0);
                 const int row = u / p.G, gsb = u - row * p.G;
-                const uint4 o = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
                 __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)gsb * QK_K) / 8 + lane, o);
             }
         }
