@@ -789,6 +789,41 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
                          **graph_fields(gr, by, peaks),
                          "l2": "flushed before each call", "oracle_s": None, "oracle_extrapolated": None,
                          "oracle_rows": None})
+    # The q8_1 quantizers on their own: the MMQ layout that the GEMM's fused quantization writes
+    # (m = 512, 2048: binary16 quants + transposed scales) and the row layout of the decode GEMV
+    # (m = 1).  Bytes: the f32 activation read once, the quants and scales written once.
+    for m, k, layout in ((512, 4096, "mmq"), (2048, 4096, "mmq"), (1, 4096, "row")):
+        x_d = torch.from_numpy(inputs.activations_f32(m, k)).to(dev)
+        if layout == "mmq":
+            ldm = q8.q8act_mmq_ldm(m)
+            oq = torch.empty((m, k), dtype=torch.uint16, device=dev)
+            od = torch.empty((k // 32, ldm), dtype=torch.float32, device=dev)
+            fnq = q8.q8act_quantize_q8_1_mmq
+            by = 4 * m * k + 2 * m * k + 4 * (k // 32) * ldm
+        else:
+            oq = torch.empty((m, k), dtype=torch.int8, device=dev)
+            od = torch.empty((m, k // 32), dtype=torch.float32, device=dev)
+            fnq = q8.q8act_quantize_q8_1
+            by = quantize_bytes(m, k)
+
+        def mkq(xc, st):
+            return lambda: q8.check(fnq(xc, oq, od, m, k, st))
+        t = time_events(mkq(x_d, stream), reps, 3, stream, torch, flush_l2)
+        med, mean = float(np.median(t)), float(np.mean(t))
+        ncp = n_copies(4 * m * k)
+        cps = [x_d] + [x_d.clone() for _ in range(ncp - 1)]
+        b2b = time_b2b([mkq(xc, stream) for xc in cps], max(reps, 4 * ncp), stream, torch)
+        gr = time_graph([mkq(xc, None) for xc in cps], max(reps, 4 * ncp), torch)
+        del cps, x_d, oq, od
+        rows_out.append({"config": f"quantize_q8_1_{layout}_m{m}", "op": f"quantize_q8_1_{layout}", "m": m, "n": 0,
+                         "k": k, "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
+                         "gbs": round(by / (med * 1e-3) / 1e9, 1), "bound": "hbm",
+                         "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "us_b2b": round(b2b * 1e3, 2), "gbs_b2b": round(by / (b2b * 1e-3) / 1e9, 1),
+                         "frac_b2b": round(by / (b2b * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         **graph_fields(gr, by, peaks),
+                         "b2b_input_copies": ncp, "l2": "flushed before each call",
+                         "oracle_s": None, "oracle_extrapolated": None, "oracle_rows": None})
     # K-quant superblocks (Q6_K, Q4_K, Q5_K): the fp16 mirror of a 4096 x 4096 weight and the
     # m = 1 GEMV at 4096 -> 64448, on seeded random superblocks
     xq1, xd1 = q8.quantize_q8_1(torch.from_numpy(inputs.activations_f32(1, 4096)).to(dev))

@@ -705,6 +705,9 @@ bool gemv_kq_supported(const DeviceInfo &dev, int fmt, int64_t m, int64_t k)
 cudaError_t launch_gemv_kq(const DeviceInfo &dev, int fmt, const uint8_t *w, const int8_t *xq, const float *xd,
                            float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream)
 {
+    // from m = 2 on, the tensor-core kernel (same bits) where the row layout allows it
+    if (m >= 2 && gemv_kq_mma_supported(dev, fmt, m, k))
+        return launch_gemv_kq_mma(dev, fmt, w, xq, xd, y, dots, m, n, k, stream);
     switch (fmt) {
     case 6: return launch_kq_gemv<KQ6>(dev, w, xq, xd, y, dots, m, n, k, stream);
     case 4: return launch_kq_gemv<KQ4>(dev, w, xq, xd, y, dots, m, n, k, stream);

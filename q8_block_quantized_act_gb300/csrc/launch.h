@@ -45,6 +45,11 @@ cudaError_t launch_gemv_q4_0_mma(const DeviceInfo &dev, const uint8_t *w, const 
 cudaError_t launch_dequant_kq_f16(const DeviceInfo &dev, int fmt, const uint8_t *w, uint16_t *w16, int64_t n,
                                   int64_t k, cudaStream_t stream);
 bool gemv_kq_supported(const DeviceInfo &dev, int fmt, int64_t m, int64_t k);
+// The tensor-core K-quant GEMV (2 <= m <= 8, rows a multiple of 16 bytes); the same bits as
+// the dp4a kernel, which launch_gemv_kq routes to otherwise.
+bool gemv_kq_mma_supported(const DeviceInfo &dev, int fmt, int64_t m, int64_t k);
+cudaError_t launch_gemv_kq_mma(const DeviceInfo &dev, int fmt, const uint8_t *w, const int8_t *xq, const float *xd,
+                               float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 cudaError_t launch_gemv_kq(const DeviceInfo &dev, int fmt, const uint8_t *w, const int8_t *xq, const float *xd,
                            float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 
