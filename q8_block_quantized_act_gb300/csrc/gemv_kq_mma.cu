@@ -23,6 +23,8 @@
 // combining a chunk's per-superblock sums while the MMA warps go on; every hand-off is an
 // mbarrier with a bounded wait.  Rows must be a multiple of 16 bytes (Q4_K, Q5_K always; Q6_K
 // when k is a multiple of 2048); other shapes stay on the dp4a kernel.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -147,6 +149,7 @@ struct MK45 {
     static constexpr bool Q6 = false;
     static constexpr bool Q5 = B == 176;
     static constexpr int QS = Q5 ? 48 : 16;
+    template <bool ALIGNED>
     __device__ static void codes(const uint8_t *sb, int j, int c, uint32_t &lo, uint32_t &hi)
     {
         const int g = j >> 1, u = j & 1;
@@ -167,12 +170,13 @@ struct MK45 {
 struct MK6 {
     static constexpr int BYTES = 210;
     static constexpr bool Q6 = true;
-    // the 4 bytes at p (2-byte aligned): two aligned words, funnel-shifted by 0 or 16 bits
+    // the 4 bytes at p: one word when the superblock is 4-byte aligned, else (2 mod 4) the
+    // two aligned words around them, funnel-shifted by 16 bits
+    template <bool ALIGNED>
     __device__ static uint32_t word(const uint8_t *p)
     {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-        const uint8_t *al = reinterpret_cast<const uint8_t *>(a & ~(uintptr_t)3);
-        return __funnelshift_r(lds32(al), lds32(al + 4), (uint32_t)(a & 3) * 8);
+        if constexpr (ALIGNED) return lds32(p);
+        return __funnelshift_r(lds32(p - 2), lds32(p + 2), 16u);
     }
     __device__ static uint32_t signed_code(uint32_t ql, uint32_t qh, int s1, int s2)
     {
@@ -183,13 +187,14 @@ struct MK6 {
         const uint32_t s = t & 0x20202020u;
         return t | (s << 1) | (s << 2);
     }
+    template <bool ALIGNED>
     __device__ static void codes(const uint8_t *sb, int j, int c, uint32_t &lo, uint32_t &hi)
     {
         const int n = j >> 2, g = j & 3;
         const uint8_t *ql = sb + 64 * n + 32 * (g & 1) + 4 * c;
         const uint8_t *qh = sb + 128 + 32 * n + 4 * c;
-        lo = signed_code(word(ql), word(qh), 4 * (g >> 1), 2 * g);
-        hi = signed_code(word(ql + 16), word(qh + 16), 4 * (g >> 1), 2 * g);
+        lo = signed_code(word<ALIGNED>(ql), word<ALIGNED>(qh), 4 * (g >> 1), 2 * g);
+        hi = signed_code(word<ALIGNED>(ql + 16), word<ALIGNED>(qh + 16), 4 * (g >> 1), 2 * g);
     }
 };
 
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *xs8 = smem + p.off_x;                                          // int8 [8][xs]
     float *xds = reinterpret_cast<float *>(smem + p.off_xd);                // f32 [k/32][8]
-    int *xsum = reinterpret_cast<int *>(smem + p.off_xsum);                 // int [k/32][8]
+    float *xsum = reinterpret_cast<float *>(smem + p.off_xsum);             // f32 [k/32][8], exact integers
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + MAX_STAGES;
     uint64_t *pfull = empty + MAX_STAGES;
@@ -312,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int sum = 0;
 #pragma unroll
             for (int c = 0; c < 8; ++c) sum = dp4a(0x01010101u, lds32(xp + 4 * c), sum);
-            xsum[idx] = sum;
+            xsum[idx] = __int2float_rn(sum);   // |sum| <= 32 * 127: exact
         }
         named_bar_sync(1, NW * 32);
     }
@@ -356,66 +361,83 @@ __global__ void __launch_bounds__(THREADS, 1)
                 d1 = half_bits_to_float(h1[0] & 0xffffu);
                 dmin1 = half_bits_to_float(h1[0] >> 16);
             }
+            auto fold_superblock = [&](auto aligned) {
+                constexpr bool AL = decltype(aligned)::value;
 #pragma unroll
-            for (int j = 0; j < SUB_BLOCKS; ++j) {
-                uint32_t w0lo, w0hi, w1lo, w1hi;
-                F::codes(sb0, j, c, w0lo, w0hi);
-                F::codes(sb1, j, c, w1lo, w1hi);
-                const int b = g * SUB_BLOCKS + j;
-                const uint8_t *xp = xs8 + (size_t)gl * p.xs + 32 * b + 4 * c;
-                const float2 da = *reinterpret_cast<const float2 *>(xds + b * 8 + 2 * c);
-                int E[4];
-                if constexpr (F::Q6) {
-                    // two 16-wide halves, each with its own int8 scale
-                    int Da[4], Db[4];
-                    mma_s8_16816(Da, w0lo, w1lo, lds32(xp));
-                    mma_s8_16816(Db, w0hi, w1hi, lds32(xp + 16));
-                    const uint32_t s0 = lds16(sb0 + 192 + 2 * j), s1 = lds16(sb1 + 192 + 2 * j);
-                    const int s0a = (int)(int8_t)(s0 & 0xFFu), s0b = (int)(int8_t)(s0 >> 8);
-                    const int s1a = (int)(int8_t)(s1 & 0xFFu), s1b = (int)(int8_t)(s1 >> 8);
-                    E[0] = s0a * Da[0] + s0b * Db[0];
-                    E[1] = s0a * Da[1] + s0b * Db[1];
-                    E[2] = s1a * Da[2] + s1b * Db[2];
-                    E[3] = s1a * Da[3] + s1b * Db[3];
-                } else {
-                    const uint32_t a[4] = {w0lo, w1lo, w0hi, w1hi};
-                    mma_s8_16832(E, a, lds32(xp), lds32(xp + 16));
-                }
-                // E[0]: (row gl, token 2c), E[1]: (gl, 2c+1), E[2]: (gl+8, 2c), E[3]: (gl+8, 2c+1)
-                if (DOTS) {
+                for (int j = 0; j < SUB_BLOCKS; ++j) {
+                    uint32_t w0lo, w0hi, w1lo, w1hi;
+                    F::template codes<AL>(sb0, j, c, w0lo, w0hi);
+                    F::template codes<AL>(sb1, j, c, w1lo, w1hi);
+                    const int b = g * SUB_BLOCKS + j;
+                    const uint8_t *xp = xs8 + (size_t)gl * p.xs + 32 * b + 4 * c;
+                    const float2 da = *reinterpret_cast<const float2 *>(xds + b * 8 + 2 * c);
+                    // the exact integers of the block dots as f32 (E, or D for Q4_K / Q5_K)
+                    float Ef[4];
+                    int E[4];
+                    if constexpr (F::Q6) {
+                        // two 16-wide halves, each with its own int8 scale
+                        int Da[4], Db[4];
+                        mma_s8_16816(Da, w0lo, w1lo, lds32(xp));
+                        mma_s8_16816(Db, w0hi, w1hi, lds32(xp + 16));
+                        const uint32_t s0 = lds16(sb0 + 192 + 2 * j), s1 = lds16(sb1 + 192 + 2 * j);
+                        const int s0a = (int)(int8_t)(s0 & 0xFFu), s0b = (int)(int8_t)(s0 >> 8);
+                        const int s1a = (int)(int8_t)(s1 & 0xFFu), s1b = (int)(int8_t)(s1 >> 8);
+                        E[0] = s0a * Da[0] + s0b * Db[0];
+                        E[1] = s0a * Da[1] + s0b * Db[1];
+                        E[2] = s1a * Da[2] + s1b * Db[2];
+                        E[3] = s1a * Da[3] + s1b * Db[3];
+                        // |E| < 2^24: exact in f32, but beyond the magic conversion's 2^22
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 16 * rt + gl + 8 * (e >> 1);
-                        const int t = 2 * c + (e & 1);
-                        if (r < rows && t < m) dots[((int64_t)t * n + row0 + r) * nb + b] = E[e];
+                        for (int e = 0; e < 4; ++e) Ef[e] = __int2float_rn(E[e]);
+                    } else {
+                        const uint32_t a[4] = {w0lo, w1lo, w0hi, w1hi};
+                        mma_s8_16832(E, a, lds32(xp), lds32(xp + 16));
+                        // |D| < 2^22: the f32 with the bits of D + bits(1.5 * 2^23) is exactly
+                        // 1.5 * 2^23 + D, and subtracting 1.5 * 2^23 leaves D
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) Ef[e] = __fsub_rn(__int_as_float(E[e] + 0x4B400000), 12582912.0f);
                     }
-                    continue;
+                    // E[0]: (row gl, token 2c), E[1]: (gl, 2c+1), E[2]: (gl+8, 2c), E[3]: (gl+8, 2c+1)
+                    if (DOTS) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = 16 * rt + gl + 8 * (e >> 1);
+                            const int t = 2 * c + (e & 1);
+                            if (r < rows && t < m) dots[((int64_t)t * n + row0 + r) * nb + b] = E[e];
+                        }
+                        continue;
+                    }
+                    if constexpr (F::Q6) {
+                        const float s00 = __fmul_rn(d0, da.x), s01 = __fmul_rn(d0, da.y);
+                        const float s10 = __fmul_rn(d1, da.x), s11 = __fmul_rn(d1, da.y);
+                        acc[q][0] = __fmaf_rn(s00, Ef[0], acc[q][0]);
+                        acc[q][1] = __fmaf_rn(s01, Ef[1], acc[q][1]);
+                        acc[q][2] = __fmaf_rn(s10, Ef[2], acc[q][2]);
+                        acc[q][3] = __fmaf_rn(s11, Ef[3], acc[q][3]);
+                    } else {
+                        int sc0, mn0, sc1, mn1;
+                        k4_scale_min(h0[1], h0[2], h0[3], j, sc0, mn0);
+                        k4_scale_min(h1[1], h1[2], h1[3], j, sc1, mn1);
+                        const float dsc0 = __fmul_rn(d0, (float)sc0), dmm0 = __fmul_rn(dmin0, (float)mn0);   // exact
+                        const float dsc1 = __fmul_rn(d1, (float)sc1), dmm1 = __fmul_rn(dmin1, (float)mn1);
+                        const float2 X = *reinterpret_cast<const float2 *>(xsum + b * 8 + 2 * c);
+                        const float v0 = __fsub_rn(__fmul_rn(dsc0, Ef[0]), __fmul_rn(dmm0, X.x));
+                        const float v1 = __fsub_rn(__fmul_rn(dsc0, Ef[1]), __fmul_rn(dmm0, X.y));
+                        const float v2 = __fsub_rn(__fmul_rn(dsc1, Ef[2]), __fmul_rn(dmm1, X.x));
+                        const float v3 = __fsub_rn(__fmul_rn(dsc1, Ef[3]), __fmul_rn(dmm1, X.y));
+                        acc[q][0] = __fmaf_rn(da.x, v0, acc[q][0]);
+                        acc[q][1] = __fmaf_rn(da.y, v1, acc[q][1]);
+                        acc[q][2] = __fmaf_rn(da.x, v2, acc[q][2]);
+                        acc[q][3] = __fmaf_rn(da.y, v3, acc[q][3]);
+                    }
                 }
-                if constexpr (F::Q6) {
-                    const float s00 = __fmul_rn(d0, da.x), s01 = __fmul_rn(d0, da.y);
-                    const float s10 = __fmul_rn(d1, da.x), s11 = __fmul_rn(d1, da.y);
-                    acc[q][0] = __fmaf_rn(s00, __int2float_rn(E[0]), acc[q][0]);
-                    acc[q][1] = __fmaf_rn(s01, __int2float_rn(E[1]), acc[q][1]);
-                    acc[q][2] = __fmaf_rn(s10, __int2float_rn(E[2]), acc[q][2]);
-                    acc[q][3] = __fmaf_rn(s11, __int2float_rn(E[3]), acc[q][3]);
-                } else {
-                    int sc0, mn0, sc1, mn1;
-                    k4_scale_min(h0[1], h0[2], h0[3], j, sc0, mn0);
-                    k4_scale_min(h1[1], h1[2], h1[3], j, sc1, mn1);
-                    const float dsc0 = __fmul_rn(d0, (float)sc0), dmm0 = __fmul_rn(dmin0, (float)mn0);   // exact
-                    const float dsc1 = __fmul_rn(d1, (float)sc1), dmm1 = __fmul_rn(dmin1, (float)mn1);
-                    const int2 X = *reinterpret_cast<const int2 *>(xsum + b * 8 + 2 * c);
-                    const float Xf0 = __int2float_rn(X.x), Xf1 = __int2float_rn(X.y);
-                    const float v0 = __fsub_rn(__fmul_rn(dsc0, __int2float_rn(E[0])), __fmul_rn(dmm0, Xf0));
-                    const float v1 = __fsub_rn(__fmul_rn(dsc0, __int2float_rn(E[1])), __fmul_rn(dmm0, Xf1));
-                    const float v2 = __fsub_rn(__fmul_rn(dsc1, __int2float_rn(E[2])), __fmul_rn(dmm1, Xf0));
-                    const float v3 = __fsub_rn(__fmul_rn(dsc1, __int2float_rn(E[3])), __fmul_rn(dmm1, Xf1));
-                    acc[q][0] = __fmaf_rn(da.x, v0, acc[q][0]);
-                    acc[q][1] = __fmaf_rn(da.y, v1, acc[q][1]);
-                    acc[q][2] = __fmaf_rn(da.x, v2, acc[q][2]);
-                    acc[q][3] = __fmaf_rn(da.y, v3, acc[q][3]);
-                }
-            }
+            };
+            // Q6_K superblocks sit 2 (mod 4) bytes into the row slot for odd g (the same for
+            // every row of the tile: row slots are 16-byte multiples apart)
+            if (!F::Q6 || (g & 1) == 0)
+                fold_superblock(std::integral_constant<bool, true>{});
+            else
+                fold_superblock(std::integral_constant<bool, false>{});
         }
         // this warp's reads of the stage are done
         __syncwarp();
