@@ -180,6 +180,9 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
         const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
         const int units = rows * p.G;
+        // unit u (row u / G, group u % G of the chunk) starts at element row0 * k + 256 u of
+        // the output, since k = 256 G
+        uint4 *outc = out + row0 * (int64_t)(k / 8) + lane;
         // Four units per warp step: their shared-memory reads are issued together.
         constexpr int UNR = 4;
         for (int u0 = warp; u0 < units; u0 += UNR * CONV_WARPS) {
@@ -204,11 +207,12 @@ __global__ void __launch_bounds__(THREADS, 2)
                     const __half2 prod = REPACK ? h[j] : __hmul2_rn(h[j], d2);
                     ow[j] = *reinterpret_cast<const uint32_t *>(&prod);
                 }
-                const int row = u / p.G, g = u - row * p.G;
-                if (REPACK && sub == 0)
+                if (REPACK && sub == 0) {
+                    const int row = u / p.G, g = u - row * p.G;
                     wdt[(int64_t)(g * GROUP_BLOCKS + jb) * ldn + row0 + row] = half_bits_to_float(dbits[e]);
+                }
                 // 256 outputs of the unit = 32 pieces of 16 bytes: piece `lane`.
-                __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)g * 256) / 8 + lane, o);
+                __stcs(outc + 32 * u, o);
             }
         }
         __syncwarp();

@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 2)
         const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
         const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;
         const int units = rows * p.G;
+        // unit u (row u / G, superblock u % G of the chunk) starts at element row0 * k + 256 u
+        // of the output, since k = 256 G
+        uint4 *outc = out + row0 * (int64_t)(k / 8) + lane;
         // Two superblocks per warp step: both are read from shared memory before either is
         // converted (more loads in flight per warp).
         constexpr int UNR = 2;
@@ -325,9 +328,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 2)
             for (int e = 0; e < UNR; ++e) {
                 const int u = u0 + e * DQ_WARPS;
                 if (u >= units) break;
-                const uint4 o = pc[e].packed(e0);
-                const int row = u / p.G, gsb = u - row * p.G;
-                __stcs(out + ((row0 + row) * (int64_t)k + (int64_t)gsb * QK_K) / 8 + lane, o);
+                __stcs(outc + 32 * u, pc[e].packed(e0));
             }
         }
         __syncwarp();

@@ -53,6 +53,62 @@ __device__ __forceinline__ Block4 quantize4(float4 v)
     return r;
 }
 
+// The q8_1 activation quantizer's form of the same arithmetic, with the quants returned as
+// integer-valued floats (+0 for zero).  For a value whose approximate quotient qa = v * (1/d)
+// lies farther than 1e-3 from every half-integer, rint(qa) is round-half-away(fl(v / d)): qa
+// differs from v / d by under 4e-5 (|v / d| <= 127; the reciprocal's relative error is at most
+// 2^-23, the product's 2^-24) and fl(v / d) from v / d by under 8e-6, so all three round to the
+// same integer, and no tie is involved.  The test |qa - rint(qa)| < 0.499 selects exactly those
+// values; the rest (near a half-integer, or qa not finite) take the IEEE division and the
+// rounding of the scalar formula, as in quantize4.  A block whose amax is 0 gives q = 0.
+struct Block4f {
+    float t[4];
+    float d;
+};
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ Block4f quantize4f(float4 v)
+{
+    float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
+    Block4f r;
+    r.d = __fdiv_rn(a, 127.0f);
+    const float rc = rcp_approx(r.d);
+    const float vals[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float qa = __fmul_rn(vals[i], rc);
+        float t = rintf(qa);
+        if (r.d == 0.0f) {
+            t = 0.0f;
+        } else if (fabsf(__fsub_rn(qa, t)) < 0.499f) {
+            t = fminf(fmaxf(t, -127.0f), 127.0f);
+        } else {
+            t = roundf(__fdiv_rn(vals[i], r.d));
+            if (t > 127.0f) t = 127.0f;
+            if (t < -127.0f) t = -127.0f;
+            if (!(t == t)) t = 0.0f;       // NaN quantizes to 0
+        }
+        r.t[i] = __fadd_rn(t, 0.0f);       // -0 -> +0
+    }
+    return r;
+}
+
+// An integer-valued float t, |t| <= 127, as its int8 byte: the bits of t + 1.5 * 2^23 are
+// those of 1.5 * 2^23 plus t (unit spacing there), so the low byte is t's two's complement.
+__device__ __forceinline__ uint32_t byte_of(float t)
+{
+    return (uint32_t)__float_as_int(__fadd_rn(t, 12582912.0f)) & 0xFFu;
+}
+
 __device__ __forceinline__ float4 load_stream(const float4 *p)
 {
     return __ldcs(p);
@@ -78,9 +134,8 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__rest
         for (int h = 0; h < 2; ++h) {
             if (h == 1 && !two) break;
             const int64_t c = i + h * stride;
-            Block4 b = quantize4(h ? v1 : v0);
-            xq[c] = (uint32_t)(b.q[0] & 0xff) | ((uint32_t)(b.q[1] & 0xff) << 8) |
-                    ((uint32_t)(b.q[2] & 0xff) << 16) | ((uint32_t)(b.q[3] & 0xff) << 24);
+            const Block4f b = quantize4f(h ? v1 : v0);
+            xq[c] = byte_of(b.t[0]) | (byte_of(b.t[1]) << 8) | (byte_of(b.t[2]) << 16) | (byte_of(b.t[3]) << 24);
             if ((c & 7) == 0) xd[c >> 3] = b.d;
         }
     }
@@ -117,11 +172,11 @@ __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__
             const int64_t t = t0 + j * ys;
             if (t >= m) break;
             const int64_t g = t * chunks_per_row + c;
-            Block4 b = quantize4(v[j]);
-            uint32_t h[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = __half_as_ushort(__int2half_rn(b.q[e]));
-            xqh[g] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+            const Block4f b = quantize4f(v[j]);
+            // the quants are small integers: exact in binary16
+            const __half2 h01 = __floats2half2_rn(b.t[0], b.t[1]);
+            const __half2 h23 = __floats2half2_rn(b.t[2], b.t[3]);
+            xqh[g] = make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
             if ((c & 7) == 0) xdt[(int64_t)(c >> 3) * ldm + t] = b.d;
         }
     }
