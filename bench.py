@@ -824,42 +824,44 @@ def run_configs(args, q8, torch, dev, stream, peaks, flush_l2, resident):
                          **graph_fields(gr, by, peaks),
                          "b2b_input_copies": ncp, "l2": "flushed before each call",
                          "oracle_s": None, "oracle_extrapolated": None, "oracle_rows": None})
-    # K-quant superblocks (Q6_K, Q4_K, Q5_K): the fp16 mirror of a 4096 x 4096 weight and the
-    # m = 1 GEMV at 4096 -> 64448, on seeded random superblocks
-    xq1, xd1 = q8.quantize_q8_1(torch.from_numpy(inputs.activations_f32(1, 4096)).to(dev))
+    # K-quant superblocks (Q6_K, Q4_K, Q5_K) on seeded random superblocks: the fp16 mirror of a
+    # 4096 x 4096 and a 20480 x 4096 weight, and the GEMV at 4096 -> 64448 for one token (the
+    # dp4a kernel) and for eight (the tensor-core kernel)
+    xs_kq = {}
+    for mm in (1, 8):
+        xs_kq[mm] = q8.quantize_q8_1(torch.from_numpy(inputs.activations_f32(mm, 4096)).to(dev))
     for fmt, sbytes in (("q6_k", 210), ("q4_k", 144), ("q5_k", 176)):
-        for n, k, what in ((4096, 4096, "dequant"), (64448, 4096, "gemv")):
+        for n, k, what, mm in ((4096, 4096, "dequant", 0), (20480, 4096, "dequant", 0), (64448, 4096, "gemv", 1),
+                               (64448, 4096, "gemv", 8)):
             wk = torch.from_numpy(inputs.kquant_superblocks(fmt, n, k)).to(dev)
             wbytes = n * (k // 256) * sbytes
             if what == "dequant":
                 w16 = torch.empty((n, k), dtype=torch.float16, device=dev)
                 fn_dq = getattr(q8, f"q8act_dequant_{fmt}_f16")
 
-                def kq():
-                    q8.check(fn_dq(wk, w16, n, k, stream))
+                def mkf(wc, st, fn_dq=fn_dq, w16=w16, n=n, k=k):
+                    return lambda: q8.check(fn_dq(wc, w16, n, k, st))
                 by = wbytes + 2 * n * k
                 big = False
             else:
-                yk = torch.empty((1, n), dtype=torch.float32, device=dev)
+                xqk, xdk = xs_kq[mm]
+                yk = torch.empty((mm, n), dtype=torch.float32, device=dev)
                 fn_gv = getattr(q8, f"q8act_gemv_{fmt}")
 
-                def kq():
-                    q8.check(fn_gv(wk, xq1, xd1, yk, 1, n, k, stream))
-                by = wbytes + k + (k // 32) * 4 + n * 4
+                def mkf(wc, st, fn_gv=fn_gv, xqk=xqk, xdk=xdk, yk=yk, mm=mm, n=n, k=k):
+                    return lambda: q8.check(fn_gv(wc, xqk, xdk, yk, mm, n, k, st))
+                by = wbytes + mm * k + mm * (k // 32) * 4 + mm * n * 4
                 big = True
-            t = time_events(kq, reps, 3, stream, torch, None if big else flush_l2)
+            t = time_events(mkf(wk, stream), reps, 3, stream, torch, None if big else flush_l2)
             med, mean = float(np.median(t)), float(np.mean(t))
             ncp = n_copies(wbytes)
             cps = [wk] + [wk.clone() for _ in range(ncp - 1)]
-            if what == "dequant":
-                mkf = (lambda wc, st: (lambda: q8.check(fn_dq(wc, w16, n, k, st))))
-            else:
-                mkf = (lambda wc, st: (lambda: q8.check(fn_gv(wc, xq1, xd1, yk, 1, n, k, st))))
             b2b = time_b2b([mkf(wc, stream) for wc in cps], max(reps, 4 * ncp), stream, torch)
             gr = time_graph([mkf(wc, None) for wc in cps], max(reps, 4 * ncp), torch)
             del cps
-            rows_out.append({"config": f"{what}_{fmt}_{k}x{n}", "op": f"{what}_{fmt}", "m": 1 if what == "gemv" else 0,
-                             "n": n, "k": k, "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
+            cfg = f"{what}_{fmt}_{k}x{n}" + (f"_m{mm}" if what == "gemv" and mm > 1 else "")
+            rows_out.append({"config": cfg, "op": f"{what}_{fmt}", "m": mm, "n": n, "k": k,
+                             "us_median": round(med * 1e3, 2), "us_mean": round(mean * 1e3, 2),
                              "gbs": round(by / (med * 1e-3) / 1e9, 1), "bound": "hbm",
                              "frac": round(by / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                              "us_b2b": round(b2b * 1e3, 2), "gbs_b2b": round(by / (b2b * 1e-3) / 1e9, 1),
