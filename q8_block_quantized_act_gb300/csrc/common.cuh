@@ -83,20 +83,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // try_wait with a suspend-time hint: the waiting thread is parked by the hardware until the
 // phase completes or about `hint_ns` nanoseconds pass, instead of spinning on the issue slots
 // that the working warps of the same SM sub-partition need.
-// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
-// may start while the previous kernel of the stream still runs; it must pass
-// griddep_wait() before touching what that kernel writes (the wait returns once that grid
-// has completed and its writes are visible; without a prerequisite grid it returns at once).
-// griddep_launch_dependents() lets such a dependent grid start early.
+// Programmatic dependent launch.  The GEMVs, dequants and K-quant kernels are launched with
+// programmatic stream serialization, so they may become resident while the previous kernel
+// of the stream still runs; each passes griddep_wait() before touching global memory (the
+// wait returns once that grid has completed and its writes are visible; without a
+// prerequisite grid it returns at once), and only then calls griddep_launch_dependents(),
+// which lets the next kernel become resident in turn.  So a dependent that starts early knows
+// that everything before its predecessor has completed.  The quantizers are ordinary launches
+// (grids of many small CTAs, beside which waiting dependents would take issue slots) that
+// trigger their dependents at entry; the second kernel of a fused call (the GEMV or GEMM
+// after the call's own quantizer) streams weights before its wait, which the quantizer does
+// not write.  Resident dependents cannot starve their predecessor: they launch only once every
+// CTA of it has started.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// The entry of a kernel with nothing to do before its predecessor completes.
+__device__ __forceinline__ void griddep_enter()
+{
+    griddep_wait();
+    griddep_launch_dependents();
+}
 
 // Host: launch `kern` as a programmatic dependent of the stream's previous kernel.
 template <typename Kern, typename... Args>
-cudaError_t launch_dependent(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t stream, Args... args)
+cudaError_t launch_dependent(Kern kern, dim3 grid, unsigned block, size_t smem, cudaStream_t stream, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

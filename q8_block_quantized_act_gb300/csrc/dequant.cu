@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent of the stream's previous kernel
+    griddep_enter();
 
     const int64_t my_chunks =
         blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -237,9 +239,8 @@ cudaError_t launch_stream(const DeviceInfo &dev, const uint8_t *w, uint16_t *w16
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    kern<<<(int)grid, THREADS, p.smem, stream>>>(w, reinterpret_cast<uint4 *>(w16), wdt, ldn, (int)n,
-                                                 (int)k, p, dev.status);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)grid, THREADS, p.smem, stream, w, reinterpret_cast<uint4 *>(w16), wdt,
+                            ldn, (int)n, (int)k, p, dev.status);
 }
 
 }  // namespace

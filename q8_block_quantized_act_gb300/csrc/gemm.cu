@@ -330,8 +330,12 @@ __global__ void __launch_bounds__(Cfg<BN_T, !REPACKED>::THREADS, Cfg<BN_T, !REPA
                 if (!wait_or_abort(&bars.stage_empty[st], ((kc / STAGES) & 1) ^ 1, status, abort_flag)) break;
                 // The activation may come from the kernel just before this one in the stream
                 // (launched as its programmatic dependent): everything above -- barriers, TMEM,
-                // the first raw weight group -- overlaps that kernel's tail.
-                if (kc == 0) griddep_wait();
+                // the first raw weight group -- overlaps that kernel's tail.  After the wait the
+                // next kernel of the stream may become resident in turn.
+                if (kc == 0) {
+                    griddep_wait();
+                    griddep_launch_dependents();
+                }
                 mbar_arrive_expect_tx(&bars.stage_full[st], ACT_TILE_BYTES + (REPACKED ? A_TILE_BYTES : 0));
                 tma_load_2d(smem + OFF_ACT + st * ACT_TILE_BYTES, &tm_x, kch * KC, tok0, &bars.stage_full[st]);
                 if (REPACKED)

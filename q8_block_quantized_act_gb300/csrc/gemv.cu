@@ -98,6 +98,7 @@ struct Plan {
     int stages;
     int ctas_per_sm;    // resident CTAs per SM the shared-memory plan allows
     int warp_reduce;    // 1: a row's units are consecutive lanes of one warp (G divides 32)
+    int wait_weights;   // 1: the producer waits for the stream's previous kernel before streaming
     uint32_t row_bytes;
     uint32_t chunk_bytes;
     int64_t nchunks;
@@ -204,9 +205,11 @@ __global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
     // activation cache -- quants [token][group][68 words], scales [token][group][12 words] --
     // and meet at a named barrier before their first chunk.
     if (tid < CONSUMERS) {
-        // The activation may come from the kernel just before this one in the stream (launched
-        // as its programmatic dependent); the weight stream above does not depend on it.
+        // The activation may come from the kernel just before this one in the stream (this
+        // kernel is launched as its programmatic dependent); in a fused call that is the
+        // call's own quantizer, and the weight stream does not wait for it.
         griddep_wait();
+        griddep_launch_dependents();
         for (int idx = tid; idx < M * G * 16; idx += CONSUMERS) {
             const int t = idx / (G * 16), rem = idx - t * G * 16, g = rem >> 4, c = rem & 15;
             const uint4 v = *reinterpret_cast<const uint4 *>(xq + (int64_t)t * k + g * 256 + c * 16);
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
         // ---------------- producer warp: one lane issues the bulk copies ----------------
         if (tid == CONSUMERS) {
             const uint64_t policy = l2_policy_evict_first();   // the weights are read once
+            if (p.wait_weights) griddep_wait();
             int64_t issued = 0;
             for (int64_t i = 0; i < my_chunks; ++i) {
                 const int s = (int)(i % p.stages);
@@ -364,10 +368,8 @@ cudaError_t launch_m(const DeviceInfo &dev, Group grp, const int8_t *xq, const f
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * p.ctas_per_sm;
     int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    if (!pdl) {
-        kern<<<(int)grid, F::CONSUMERS + 32, p.smem, stream>>>(grp, xq, xd, dots, (int)k, p, dev.status);
-        return cudaGetLastError();
-    }
+    // fused: the previous kernel is this call's quantizer, which does not write the weights
+    p.wait_weights = pdl ? 0 : 1;
     return launch_dependent(kern, (unsigned)grid, F::CONSUMERS + 32, p.smem, stream, grp, xq, xd, dots, (int)k, p,
                             dev.status);
 }

@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- producer: one bulk copy per weight row into its padded slot ----------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();   // the weights are read once
+            griddep_wait();   // after the stream's previous kernel (a programmatic dependent)
             int64_t issued = 0;
             for (int64_t i = 0; i < my_chunks; ++i) {
                 const int s = (int)(i % p.stages);
@@ -298,6 +299,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------- MMA warps: the activation cache (tokens >= m read as zero) -------------
+    griddep_wait();
+    griddep_launch_dependents();
     for (int idx = tid; idx < 8 * (k / 16); idx += NW * 32) {
         const int t = idx / (k / 16), c16 = idx - t * (k / 16);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -491,9 +494,8 @@ cudaError_t launch_f(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, 
     cudaError_t e = set_kernel_smem<kq_mma_kernel<F, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
-    kq_mma_kernel<F, DOTS><<<(int)grid, THREADS, p.smem, stream>>>(w, y, xq, xd, dots, (int)m, (int)n, (int)k, p,
-                                                                   dev.status);
-    return cudaGetLastError();
+    return launch_dependent(kq_mma_kernel<F, DOTS>, (unsigned)grid, THREADS, p.smem, stream, w, y, xq, xd, dots,
+                            (int)m, (int)n, (int)k, p, dev.status);
 }
 
 template <class F>

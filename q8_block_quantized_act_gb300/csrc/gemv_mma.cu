@@ -52,6 +52,7 @@ struct MPlan {
     uint32_t stage_bytes;
     uint32_t part_bytes; // one partial slot: [G][8 mt][R] f32
     int nparts;          // partial slots (1 or 2)
+    int wait_weights;    // 1: the producer waits for the stream's previous kernel before streaming
     int64_t nchunks;    // chunks of the whole group (set at launch)
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- producer: one bulk copy per weight row into its padded slot ----------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();   // the weights are read once
+            if (p.wait_weights) griddep_wait();
             int64_t issued = 0;
             for (int64_t i = 0; i < my_chunks; ++i) {
                 const int s = (int)(i % p.stages);
@@ -302,9 +304,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------- MMA warps: the activation cache (tokens >= m read as zero) -------------
-    // (after the kernel that produced the activation, when launched as its programmatic
-    // dependent; the weight stream does not depend on it)
+    // (after the stream's previous kernel: this kernel is launched as its programmatic
+    // dependent; in a fused call that is the call's own quantizer, and the weight stream does
+    // not wait for it)
     griddep_wait();
+    griddep_launch_dependents();
     for (int idx = tid; idx < TOK * (k / 16); idx += NW * 32) {
         const int t = idx / (k / 16), c16 = idx - t * (k / 16);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -472,10 +476,8 @@ cudaError_t launch_mt(const DeviceInfo &dev, Group grp, const int8_t *xq, const 
     cudaError_t e = set_kernel_smem<gemv_mma_kernel<F, MT, DOTS>>(dev.device, p.smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.nchunks < dev.num_sms ? p.nchunks : dev.num_sms;
-    if (!pdl) {
-        kern<<<(int)grid, THREADS, p.smem, stream>>>(grp, xq, xd, dots, (int)m, (int)k, p, dev.status);
-        return cudaGetLastError();
-    }
+    // pdl: the previous kernel is this call's quantizer, which does not write the weights
+    p.wait_weights = pdl ? 0 : 1;
     return launch_dependent(kern, (unsigned)grid, THREADS, p.smem, stream, grp, xq, xd, dots, (int)m, (int)k, p,
                             dev.status);
 }

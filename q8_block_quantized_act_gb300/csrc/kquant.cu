@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 2)
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent of the stream's previous kernel
+    griddep_enter();
     const int64_t my_chunks = blockIdx.x < p.nchunks ? (p.nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     if (warp == DQ_WARPS) {
@@ -371,9 +373,8 @@ cudaError_t launch_kq_dequant(const DeviceInfo &dev, const uint8_t *w, uint16_t 
     if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    kq_dequant_kernel<F><<<(int)grid, DQ_THREADS, p.smem, stream>>>(w, reinterpret_cast<uint4 *>(w16), (int)n, (int)k,
-                                                                   p, dev.status);
-    return cudaGetLastError();
+    return launch_dependent(kq_dequant_kernel<F>, (unsigned)grid, DQ_THREADS, p.smem, stream, w,
+                            reinterpret_cast<uint4 *>(w16), (int)n, (int)k, p, dev.status);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -458,6 +459,8 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent of the stream's previous kernel
+    griddep_enter();
     if (tid < GV_CONSUMERS) {
         // The activation cache: quants [t][group][68 words], scales [t][group][12], and the
         // sum of each 32-wide block's quants (the Q4_K / Q5_K min term).
@@ -655,9 +658,8 @@ cudaError_t launch_kq_gemv_m(const DeviceInfo &dev, const uint8_t *w, const int8
         per_sm = resident;
     const int64_t slots = (int64_t)dev.num_sms * per_sm;
     const int64_t grid = p.nchunks < slots ? p.nchunks : slots;
-    kq_gemv_kernel<F, MM><<<(int)grid, GV_CONSUMERS + 32, p.smem, stream>>>(w, xq, xd, y, dots, (int)m, (int)n,
-                                                                           (int)k, p, dev.status);
-    return cudaGetLastError();
+    return launch_dependent(kq_gemv_kernel<F, MM>, (unsigned)grid, GV_CONSUMERS + 32, p.smem, stream, w, xq, xd, y,
+                            dots, (int)m, (int)n, (int)k, p, dev.status);
 }
 
 template <class F>

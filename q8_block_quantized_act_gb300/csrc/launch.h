@@ -60,8 +60,9 @@ cudaError_t launch_gemv_q8_0_group(const DeviceInfo &dev, const uint8_t *const *
                                    int64_t m, int64_t k, cudaStream_t stream);
 // The tensor-core GEMV for 2 <= m <= 16 (bitwise the same results as launch_gemv_q8_0).
 bool gemv_mma_supported(const DeviceInfo &dev, int64_t m, int64_t k);
-// pdl: launch as a programmatic dependent of the stream's previous kernel, which must be the
-// q8_1 quantizer producing xq / xd (the GEMV streams weights while it finishes).
+// Every GEMV launch is a programmatic dependent of the stream's previous kernel.  pdl: that
+// kernel is the call's own q8_1 quantizer producing xq / xd, and the GEMV streams weights
+// while it finishes; otherwise the GEMV waits for it before touching memory.
 cudaError_t launch_gemv_q8_0_mma(const DeviceInfo &dev, const uint8_t *w, const int8_t *xq, const float *xd,
                                  float *y, int32_t *dots, int64_t m, int64_t n, int64_t k, cudaStream_t stream,
                                  bool pdl = false);

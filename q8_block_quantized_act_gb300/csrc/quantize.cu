@@ -120,8 +120,9 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4 *__rest
                                                             float *__restrict__ xd,
                                                             int64_t nchunks)
 {
-    // The GEMV that consumes this activation may be launched as a programmatic dependent: let
-    // it start streaming its weights (it waits for this grid before reading the activation).
+    // An ordinary launch (it starts once everything before it in the stream has completed);
+    // the GEMV that consumes this activation is launched as its programmatic dependent and may
+    // start streaming its weights now (it waits for this grid before reading the activation).
     griddep_launch_dependents();
     // Two independent chunks per step (more loads in flight).  nchunks is a multiple of 64
     // and the stride of 32, so both halves are warp-uniform, as the shuffles need.
@@ -154,8 +155,9 @@ __global__ void __launch_bounds__(256) quantize_q8_1_mmq_kernel(const float4 *__
                                                                 int64_t m, int chunks_per_row,
                                                                 int64_t ldm)
 {
-    // The GEMM that consumes this layout may be launched as a programmatic dependent: let it
-    // start its prologue (it waits for this grid before reading the activation).
+    // An ordinary launch (it starts once everything before it in the stream has completed);
+    // the GEMM that consumes this layout is launched as its programmatic dependent and may
+    // start its prologue now (it waits for this grid before reading the activation).
     griddep_launch_dependents();
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= chunks_per_row) return;
