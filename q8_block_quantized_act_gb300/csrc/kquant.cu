@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
     extern __shared__ __align__(1024) uint8_t smem[];
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem + p.off_x);
     float *xds = reinterpret_cast<float *>(smem + p.off_xd);
-    int *xsum = reinterpret_cast<int *>(smem + p.off_xs);
+    float *xsum = reinterpret_cast<float *>(smem + p.off_xs);   // exact integers
     float *part = reinterpret_cast<float *>(smem + p.off_part);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + KMAX_STAGES;
@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
             int sum = 0;
 #pragma unroll
             for (int c = 0; c < 8; ++c) sum = dp4a(0x01010101u, xv[c], sum);
-            xsum[idx] = sum;
+            xsum[idx] = __int2float_rn(sum);   // |sum| <= 32 * 127: exact
         }
         named_bar_sync(2, GV_CONSUMERS);
     }
@@ -526,11 +526,18 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
                 uint32_t wv[F::WORDS];
                 load_superblock<F>(sbase + (size_t)row * p.row_bytes + (size_t)g * F::BYTES, wv);
                 float d, dmin = 0.0f;
+                // Q4_K / Q5_K: the 6-bit scales and mins of all 8 sub-blocks, four to a word
+                // (byte j & 3 of the word for sub-block j), unpacked from the 12 scale bytes
+                uint32_t sc_lo = 0, mn_lo = 0, sc_hi = 0, mn_hi = 0;
                 if constexpr (F::BYTES == KQ6::BYTES) {
                     d = half_bits_to_float(wv[52] & 0xffffu);
                 } else {
                     d = half_bits_to_float(wv[0] & 0xffffu);
                     dmin = half_bits_to_float(wv[0] >> 16);
+                    sc_lo = wv[1] & 0x3F3F3F3Fu;
+                    mn_lo = wv[2] & 0x3F3F3F3Fu;
+                    sc_hi = (wv[3] & 0x0F0F0F0Fu) | ((wv[1] >> 2) & 0x30303030u);
+                    mn_hi = ((wv[3] >> 4) & 0x0F0F0F0Fu) | ((wv[2] >> 2) & 0x30303030u);
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -543,10 +550,10 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
                         sc0 = (int)(int8_t)(sw & 0xFFu);
                         sc1 = (int)(int8_t)((sw >> 8) & 0xFFu);
                     } else {
-                        int sc, mn;
-                        k4_scale_min(wv, j, sc, mn);
-                        dsc = __fmul_rn(d, (float)sc);       // exact
-                        dmm = __fmul_rn(dmin, (float)mn);    // exact
+                        const float scf = __fsub_rn(byte_magic(j < 4 ? sc_lo : sc_hi, j & 3), 8388608.0f);
+                        const float mnf = __fsub_rn(byte_magic(j < 4 ? mn_lo : mn_hi, j & 3), 8388608.0f);
+                        dsc = __fmul_rn(d, scf);       // exact
+                        dmm = __fmul_rn(dmin, mnf);    // exact
                     }
 #pragma unroll
                     for (int t = 0; t < MM; ++t) {
@@ -562,8 +569,11 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
                         D0 = dp4a(q[3], a.w, D0);
                         D1 = dp4a(q[7], b.w, D1);
                         const float da = xds[(t * G + g) * XDG_WORDS + j];
+                        // exact int -> f32 for |D| < 2^22: the bits of D + bits(1.5 * 2^23) are those
+                        // of 1.5 * 2^23 + D, and subtracting 1.5 * 2^23 leaves D
+                        auto exact_f = [](int D) { return __fsub_rn(__int_as_float(D + 0x4B400000), 12582912.0f); };
                         if constexpr (F::BYTES == KQ6::BYTES) {
-                            const int E = sc0 * D0 + sc1 * D1;                       // exact
+                            const int E = sc0 * D0 + sc1 * D1;   // exact, |E| < 2^24
                             if (dots)
                                 dots[((int64_t)t * n + row0 + row) * nb + g * 8 + j] = E;
                             else
@@ -573,9 +583,8 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
                             if (dots) {
                                 dots[((int64_t)t * n + row0 + row) * nb + g * 8 + j] = D;
                             } else {
-                                const int X = xsum[(t * G + g) * 8 + j];
-                                const float v = __fsub_rn(__fmul_rn(dsc, __int2float_rn(D)),
-                                                          __fmul_rn(dmm, __int2float_rn(X)));
+                                const float X = xsum[(t * G + g) * 8 + j];
+                                const float v = __fsub_rn(__fmul_rn(dsc, exact_f(D)), __fmul_rn(dmm, X));
                                 acc[t] = __fmaf_rn(da, v, acc[t]);
                             }
                         }
