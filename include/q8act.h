@@ -32,6 +32,13 @@
  *   - dimensions: k must be a positive multiple of 256 (every row then starts 16-byte
  *     aligned, which the bulk/TMA copies need); n >= 1; m as stated per call;
  *   - alignment: every pointer must be 16-byte aligned.
+ *   - stream order: the calls keep the stream's order.  Most of their kernels are launched
+ *     as programmatic dependents of the stream's previous kernel (they become resident early
+ *     and wait for it to complete before touching memory), and every kernel lets the next
+ *     one start early; a kernel that the caller launches after a call with programmatic
+ *     stream serialization must therefore wait on its grid dependency (griddepcontrol.wait /
+ *     cudaGridDependencySynchronize) before reading the call's outputs, as any such kernel
+ *     must.  Ordinary launches, copies and events need nothing.
  *
  * Kernels time out instead of hanging: a pipeline wait that exceeds about two seconds makes
  * the kernel record an error in a device-side status word and return early.
