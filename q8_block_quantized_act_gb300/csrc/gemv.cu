@@ -161,20 +161,6 @@ Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
     return p;
 }
 
-__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 template <class F, int M, bool DOTS>
 __global__ void __launch_bounds__(F::CONSUMERS + 32, 2)
     gemv_kernel(const __grid_constant__ Group grp, const int8_t *__restrict__ xq,

@@ -7,7 +7,7 @@
 // 32-wide sub-block with mma.sync: Q4_K / Q5_K take one m16n8k32 per sub-block (the unsigned
 // 4- or 5-bit codes against the signed activation quants: D exact in int32), Q6_K takes two
 // m16n8k16, one per 16-wide half, because each half has its own int8 scale (E = s0 * D_a +
-// s1 * D_b, exact).  The superblock layouts are the GGUF formats' (see kquant.cu).
+// s1 * D_b, exact).  The superblock layouts are the GGUF formats' (kquant.cuh).
 //
 // Per (row, token) the fold is the dp4a K-quant kernel's, operation for operation: per
 // superblock acc = 0, then over its 8 sub-blocks in order
@@ -26,6 +26,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "kquant.cuh"
 #include "launch.h"
 
 namespace q8 {
@@ -100,43 +101,6 @@ KMPlan make_plan(int64_t k, size_t smem_cap, int sb_bytes, int rt_cap)
 
 bool plan_ok(const KMPlan &p) { return p.stages >= 2 && (p.items + NW - 1) / NW <= MAX_ITEMS; }
 
-__device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
-__device__ __forceinline__ uint32_t lds16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
-
-__device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%10,%10,%10};"
-        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
-}
-
-__device__ __forceinline__ void mma_s8_16816(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%7,%7,%7};"
-        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-        : "r"(a0), "r"(a1), "r"(b0), "r"(0));
-}
-
-// The 6-bit scale and min of sub-block j (compile-time here) from the 12 scale bytes, words
-// w1..w3 of the superblock.
-__device__ __forceinline__ void k4_scale_min(uint32_t w1, uint32_t w2, uint32_t w3, int j, int &sc, int &mn)
-{
-    auto b = [&](int i) {
-        const uint32_t x = i < 4 ? w1 : (i < 8 ? w2 : w3);
-        return (int)((x >> (8 * (i & 3))) & 0xFFu);
-    };
-    if (j < 4) {
-        sc = b(j) & 63;
-        mn = b(j + 4) & 63;
-    } else {
-        sc = (b(j + 4) & 15) | ((b(j - 4) >> 6) << 4);
-        mn = (b(j + 4) >> 4) | ((b(j) >> 6) << 4);
-    }
-}
-
 // Weight formats.  codes(sb, j, c, lo, hi): the two words of sub-block j of the superblock at
 // sb that lane column c feeds to the MMA, elements 4c..4c+3 (lo) and 16+4c..16+4c+3 (hi) of
 // the sub-block as bytes.
@@ -180,12 +144,7 @@ struct MK6 {
     }
     __device__ static uint32_t signed_code(uint32_t ql, uint32_t qh, int s1, int s2)
     {
-        const uint32_t code = ((ql >> s1) & 0x0F0F0F0Fu) | (((qh >> s2) & 0x03030303u) << 4);
-        // code - 32 as a signed byte: flip bit 5; where it is now set (code < 32) the byte is
-        // code + 32 and must become code + 32 - 64, i.e. gain bits 6 and 7
-        const uint32_t t = code ^ 0x20202020u;
-        const uint32_t s = t & 0x20202020u;
-        return t | (s << 1) | (s << 2);
+        return q6_signed_bytes(((ql >> s1) & 0x0F0F0F0Fu) | (((qh >> s2) & 0x03030303u) << 4));
     }
     template <bool ALIGNED>
     __device__ static void codes(const uint8_t *sb, int j, int c, uint32_t &lo, uint32_t &hi)

@@ -1,44 +1,21 @@
-// kquant.cu -- the GGUF K-quant superblocks (256 weights each) that memra-engine 0.81.0
-// f16_ffi.rs names beside Q8_0 and Q4_0: Q6_K (210 bytes), Q4_K (144 bytes), Q5_K (176 bytes).
-// Two passes over them:
-//   * the fp16 mirror (memra_q6_K / q4_K / q5_K_dequant_f16): every weight's exact value,
-//     rounded once to binary16;
+// kquant.cu -- two passes over the GGUF K-quant superblocks (layouts in kquant.cuh):
+//   * the fp16 mirror (memra-engine 0.81.0 f16_ffi.rs memra_q6_K / q4_K / q5_K_dequant_f16):
+//     every weight's exact value, rounded once to binary16;
 //   * the decode GEMV with the q8_1 activation (1 <= m <= 8), exact integer dots per 32-wide
-//     activation block and an f32 fold.
-// Superblock layouts (the GGUF formats'), weight e = 0..255:
-//   Q6_K: ql[128] | qh[64] | int8 scales[16] | fp16 d.  e = 128h + 32g + l: code = low 4 bits
-//         from ql[64h + 32(g&1) + l] (low nibble for g < 2, high for g >= 2) + 16 * 2 bits
-//         (qh[32h + l] >> 2g); value = d * scales[e/16] * (code - 32).
-//   Q4_K: fp16 d | fp16 dmin | 12 scale bytes | qs[128].  Sub-block j = e/32 has a 6-bit scale
-//         and min (j < 4: s[j] & 63, s[j+4] & 63; j >= 4: (s[j+4] & 15) | (s[j-4] >> 6) << 4,
-//         (s[j+4] >> 4) | (s[j] >> 6) << 4); e = 64g + 32u + l: code = nibble u of qs[32g + l];
-//         value = d * sc_j * code - dmin * m_j.
-//   Q5_K: as Q4_K with qh[32] before qs; the code gains bit j of qh[l] as its fifth bit.
+//     activation block and an f32 fold (from m = 2 the tensor-core kernel of gemv_kq_mma.cu
+//     takes over where the row layout allows it, with the same bits).
 // Both passes stream chunks of whole rows into a shared-memory ring with cp.async.bulk, as
 // the Q8_0 kernels do.  Q6_K rows are a 16-byte multiple only when k is a multiple of 2048,
 // so a chunk holds a multiple of 8 rows (8 rows always are) and the last chunk's final
 // 0..14 bytes are copied by the producer thread itself.
 #include "common.cuh"
+#include "kquant.cuh"
 #include "launch.h"
 
 namespace q8 {
 namespace {
 
-constexpr int QK_K = 256;
 constexpr int KMAX_STAGES = 6;
-
-struct KQ6 {
-    static constexpr int BYTES = 210;
-    static constexpr int WORDS = 53;   // 212 bytes cover the superblock from any 2-byte offset
-};
-struct KQ4 {
-    static constexpr int BYTES = 144;
-    static constexpr int WORDS = 36;
-};
-struct KQ5 {
-    static constexpr int BYTES = 176;
-    static constexpr int WORDS = 44;
-};
 
 __host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 
@@ -72,24 +49,6 @@ __device__ __forceinline__ void load_superblock(const uint8_t *p, uint32_t (&w)[
     }
 }
 
-// The 6-bit scale and min of sub-block j from the 12 scale bytes held in words w[1..3] (selects
-// rather than an indexed register array, so that a lane-dependent j stays in registers).
-__device__ __forceinline__ void k4_scale_min(const uint32_t *w, int j, int &sc, int &mn)
-{
-    const uint32_t w1 = w[1], w2 = w[2], w3 = w[3];
-    auto b = [&](int i) {
-        const uint32_t x = i < 4 ? w1 : (i < 8 ? w2 : w3);
-        return (int)((x >> (8 * (i & 3))) & 0xFFu);
-    };
-    if (j < 4) {
-        sc = b(j) & 63;
-        mn = b(j + 4) & 63;
-    } else {
-        sc = (b(j + 4) & 15) | ((b(j - 4) >> 6) << 4);
-        mn = (b(j + 4) >> 4) | ((b(j) >> 6) << 4);
-    }
-}
-
 // The codes of 32-wide block j of a superblock, as 8 words of 4 bytes each (element order),
 // ready for dp4a: Q6_K gives the signed bytes code - 32; Q4_K / Q5_K the unsigned codes.
 template <class F>
@@ -101,12 +60,7 @@ __device__ __forceinline__ void block_codes(const uint32_t (&w)[F::WORDS], int j
         const int s1 = 4 * (g >> 1), s2 = 2 * g;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint32_t code = ((w[qlw + c] >> s1) & 0x0F0F0F0Fu) | (((w[qhw + c] >> s2) & 0x03030303u) << 4);
-            // code - 32 as a signed byte: flip bit 5; where it is now set (code < 32) the byte
-            // is code + 32 and must become code + 32 - 64, i.e. gain bits 6 and 7.
-            const uint32_t t = code ^ 0x20202020u;
-            const uint32_t s = t & 0x20202020u;
-            q[c] = t | (s << 1) | (s << 2);
+            q[c] = q6_signed_bytes(((w[qlw + c] >> s1) & 0x0F0F0F0Fu) | (((w[qhw + c] >> s2) & 0x03030303u) << 4));
         }
     } else {
         const int g = j >> 1, u = j & 1;
@@ -245,7 +199,7 @@ struct KqPiece<F, false> {
     {
         const int u2 = (e0 >> 5) & 1, j = e0 >> 5;
         int sc, mn;
-        k4_scale_min(head, j, sc, mn);
+        k4_scale_min(head[1], head[2], head[3], j, sc, mn);
         const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
         const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);
         uint32_t o[4];
@@ -419,20 +373,6 @@ KPlan gemv_plan(int64_t m, int64_t n, int64_t k, int sb_bytes, size_t smem_cap, 
     return p;
 }
 
-__device__ __forceinline__ bool kbar_red_or(int id, int nthreads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 // MM: the largest token count of the instance; the call's m (<= MM) tokens are folded, each
 // with the same operations in the same order for every MM (decode == verify).
 template <class F, int MM>
@@ -510,7 +450,7 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
     for (int64_t i = 0; i < my_chunks; ++i) {
         const int s = (int)(i % p.stages);
         const bool ok = mbar_wait(&full[s], (uint32_t)((i / p.stages) & 1), status);
-        if (p.warp_reduce ? __any_sync(0xffffffffu, !ok) : kbar_red_or(1, GV_CONSUMERS, !ok)) break;
+        if (p.warp_reduce ? __any_sync(0xffffffffu, !ok) : bar_red_or(1, GV_CONSUMERS, !ok)) break;
         const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
         const int rows = (int)((n - row0) < p.R ? (n - row0) : p.R);
         const uint8_t *sbase = smem + (size_t)s * p.chunk_bytes;

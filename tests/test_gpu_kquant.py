@@ -64,6 +64,25 @@ def test_kq_gemv_block_integers_exact(fmt, m, n, k):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("m", [1, 8])
+def test_kq_gemv_block_integers_full_shape_sampled(fmt, m):
+    """4096 -> 20493 (a serving width with a ragged last 16-row tile): the production block
+    integers of the dp4a kernel (m = 1) and of the tensor-core kernel (m = 8), exact on a
+    seeded row sample plus the last 40 rows."""
+    ensure_built()
+    n, k = 20493, 4096
+    wb, xq, _ = kq_problem(fmt, m, n, k, "outliers")
+    D = torch.full((m, n, k // 32), -7, dtype=torch.int32, device="cuda")
+    fn = {"q6_k": q8.q8act_debug_gemv_q6_k_block_dots, "q4_k": q8.q8act_debug_gemv_q4_k_block_dots,
+          "q5_k": q8.q8act_debug_gemv_q5_k_block_dots}[fmt]
+    q8.check(fn(cuda(wb), cuda(xq), D, m, n, k))
+    device_ok()
+    rows = np.union1d(sample_rows(n, 256), np.arange(n - 40, n)).astype(np.int64)
+    got = host(D[:, torch.from_numpy(rows).cuda(), :])
+    assert np.array_equal(got, oracle.block_dots_kq(fmt, wb, xq, k, rows=rows))
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("m,n,k,kind", [(1, 512, 256, "normal"), (1, 4096, 4096, "outliers"),
                                          (3, 1000, 1280, "normal"), (4, 777, 4096, "token_scales"),
                                          (8, 300, 4096, "outliers"), (2, 1, 256, "normal")])
