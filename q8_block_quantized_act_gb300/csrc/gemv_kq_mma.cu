@@ -432,14 +432,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 int sb_bytes_of(int fmt) { return fmt == 6 ? 210 : fmt == 4 ? 144 : fmt == 5 ? 176 : 0; }
 
-// At most this many 16-row tiles per chunk: fewer where the matrix would otherwise be cut into
-// fewer chunks than there are SMs.
+// 16-row tiles per chunk: the count that minimises waves of chunks over the SMs times rounds
+// of items per MMA warp, ties to fewer (more SMs streaming).
 int rt_cap_for(const DeviceInfo &dev, int64_t n, int64_t k)
 {
     const int64_t tiles = (n + 15) / 16;
-    const int g = (int)(k / 256), rt0 = (NW + g - 1) / g;
-    int cap = rt0 > 1 ? rt0 : 1;
-    while (cap > 1 && tiles / cap < dev.num_sms) --cap;
+    const int g = (int)(k / 256), rt0 = (NW + g - 1) / g > 1 ? (NW + g - 1) / g : 1;
+    int cap = 1;
+    int64_t best = -1;
+    for (int rt = 1; rt <= rt0; ++rt) {
+        const int64_t waves = ((tiles + rt - 1) / rt + dev.num_sms - 1) / dev.num_sms;
+        const int64_t cost = waves * ((rt * g + NW - 1) / NW);
+        if (best < 0 || cost < best) {
+            best = cost;
+            cap = rt;
+        }
+    }
     return cap;
 }
 

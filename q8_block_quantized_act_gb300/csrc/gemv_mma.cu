@@ -57,10 +57,11 @@ struct MPlan {
     size_t off_x, off_xd, off_part, off_bar, smem;
 };
 
-// rt_cap: at most this many 16-row tiles per chunk.  A chunk takes enough tiles to give each
-// MMA warp an item (16 / G of them), unless the matrix is then cut into fewer chunks than
-// there are SMs: short rows (k = 1280: five groups per row) on a 4096-row matrix would give
-// 64 chunks of 64 rows, leaving most SMs idle, so fewer tiles per chunk are taken there.
+// rt_cap: at most this many 16-row tiles per chunk.  A chunk takes up to enough tiles to give
+// each MMA warp an item (16 / G of them); the launch picks the count that minimises waves of
+// chunks over the SMs times rounds of items per warp (k = 1280, five groups per row: two tiles
+// per chunk at 4096 rows -- one wave of 128 chunks, 10 items each -- and three at 20480 rows,
+// where four would give 20 items to 16 warps).
 MPlan make_mplan(int mt, int64_t k, size_t smem_cap, int block_bytes, int rt_cap = 1 << 20)
 {
     MPlan p{};
@@ -434,14 +435,22 @@ template <class F, int MT, bool DOTS>
 cudaError_t launch_mt(const DeviceInfo &dev, Group grp, const int8_t *xq, const float *xd, int32_t *dots, int64_t m,
                       int64_t k, cudaStream_t stream, bool pdl)
 {
-    // 16-row tiles of the whole group, and the most tiles per chunk that still give every SM
-    // a chunk (when the matrix has that many tiles at all)
+    // 16-row tiles of the whole group
     int64_t tiles = 0;
     for (int i = 0; i < grp.count; ++i) tiles += (grp.n[i] + 15) / 16;
-    int rt_cap = 1 << 20;
+    // 16-row tiles per chunk: the fewest (waves of chunks over the SMs) x (rounds of items per
+    // MMA warp), ties to fewer tiles per chunk (more SMs streaming)
+    int rt_cap = 1;
     {
-        const int g = (int)(k / 256), rt0 = (NW + g - 1) / g;
-        for (rt_cap = rt0 > 1 ? rt0 : 1; rt_cap > 1 && tiles / rt_cap < dev.num_sms; --rt_cap) {
+        const int g = (int)(k / 256), rt0 = (NW + g - 1) / g > 1 ? (NW + g - 1) / g : 1;
+        int64_t best = -1;
+        for (int rt = 1; rt <= rt0; ++rt) {
+            const int64_t waves = ((tiles + rt - 1) / rt + dev.num_sms - 1) / dev.num_sms;
+            const int64_t cost = waves * ((rt * g + NW - 1) / NW);
+            if (best < 0 || cost < best) {
+                best = cost;
+                rt_cap = rt;
+            }
         }
     }
     MPlan p = make_mplan(MT, k, dev.max_smem_optin, F::BLOCK_BYTES, rt_cap);
