@@ -73,6 +73,19 @@ __device__ __forceinline__ float rcp_approx(float x)
     return r;
 }
 
+// amax / 127 correctly rounded, for amax >= 0: Markstein's correction for a division by a
+// known divisor (a quotient q0 = amax * RN(1/127), its exact residual amax - 127 q0 by one FMA,
+// and q0 + residual * RN(1/127) by another).  Checked against IEEE division on the host for
+// every non-negative binary32 value: all agree except amax = +inf (the residual is then NaN),
+// which is selected separately.
+__device__ __forceinline__ float div127(float a)
+{
+    const float c = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(a, c);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, 127.0f, a), c, q0);
+    return a == __int_as_float(0x7f800000) ? a : q1;
+}
+
 __device__ __forceinline__ Block4f quantize4f(float4 v)
 {
     float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -80,7 +93,7 @@ __device__ __forceinline__ Block4f quantize4f(float4 v)
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
     Block4f r;
-    r.d = __fdiv_rn(a, 127.0f);
+    r.d = div127(a);
     const float rc = rcp_approx(r.d);
     const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
