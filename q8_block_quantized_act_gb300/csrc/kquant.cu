@@ -376,7 +376,7 @@ KPlan gemv_plan(int64_t m, int64_t n, int64_t k, int sb_bytes, size_t smem_cap, 
 // MM: the largest token count of the instance; the call's m (<= MM) tokens are folded, each
 // with the same operations in the same order for every MM (decode == verify).
 template <class F, int MM>
-__global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
+__global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6::BYTES) ? 4 : (MM <= 2 ? 3 : 2))
     kq_gemv_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ xq, const float *__restrict__ xd,
                    float *__restrict__ y, int32_t *__restrict__ dots, int m, int n, int k, KPlan p, int *status)
 {
@@ -563,14 +563,23 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, MM <= 2 ? 3 : 2)
     }
 }
 
-// Three CTAs per SM when three stages (two for Q6_K, whose 27 KB chunks leave room for only
-// two) fit in a third of shared memory -- the consumers of these formats work harder per
-// streamed byte than Q8_0's, so more of them pay -- else two when three stages fit in half,
-// else one CTA with as many stages as fit.
+// Q4_K / Q5_K at m = 1: four CTAs per SM, two 18-22 KB stages each in a quarter of shared
+// memory (4096 -> 64448: Q4_K 29.8 -> 27.7 us, Q5_K 32.4 -> 30.9 us against three CTAs; Q6_K,
+// whose 27 KB chunks leave room for one stage there, stays at three).  Otherwise three CTAs per
+// SM when three stages (two for Q6_K) fit in a third of shared memory -- the consumers of these
+// formats work harder per streamed byte than Q8_0's, so more of them pay -- else two when three
+// stages fit in half, else one CTA with as many stages as fit.
 template <class F>
 KPlan choose_gemv_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin, int *per_sm)
 {
-    const size_t third_sm = 74 * 1024, half_sm = 113 * 1024;
+    const size_t third_sm = 74 * 1024, half_sm = 113 * 1024, quarter_sm = 56 * 1024;
+    if (m <= 1 && F::BYTES != KQ6::BYTES) {
+        KPlan p4 = gemv_plan(m, n, k, F::BYTES, quarter_sm < smem_optin ? quarter_sm : smem_optin, GV_CONSUMERS);
+        if (p4.stages >= 2) {
+            *per_sm = 4;
+            return p4;
+        }
+    }
     if (m <= 2) {
         KPlan p3 = gemv_plan(m, n, k, F::BYTES, third_sm < smem_optin ? third_sm : smem_optin, GV_CONSUMERS);
         if (p3.stages >= (F::BYTES == KQ6::BYTES ? 2 : 3)) {
