@@ -134,16 +134,25 @@ Plan make_plan(int64_t m, int64_t n, int64_t k, size_t smem_cap, int r_cap, int 
     return p;
 }
 
-// Three CTAs per SM when rings of at least 3 stages fit in a third of the shared memory (Q4_0
-// at small m: its consumers, with twice the work per streamed byte, need the extra warps --
-// 4096 -> 64448 at m = 1: 33.1 -> 27.7 us), else two when 3-stage rings fit in half, else one
-// CTA with up to 6 stages.
+// Q4_0 at m = 1: four CTAs per SM with two 18.4 KB stages each in a quarter of the shared
+// memory (its consumers do twice the work per streamed byte of Q8_0's and need the warps:
+// 4096 -> 64448 26.0 -> 24.5 us against three CTAs, 33.1 us with two).  Otherwise three CTAs per
+// SM when rings of at least 3 stages fit in a third of the shared memory, else two when 3-stage
+// rings fit in half, else one CTA with up to 6 stages.
 // When a large activation leaves room for fewer than 2 full-size stages, the chunk shrinks
 // (fewer rows per chunk) until two fit.
 template <class F>
 Plan choose_plan(int64_t m, int64_t n, int64_t k, size_t smem_optin)
 {
-    const size_t third = 74 * 1024;
+    const size_t third = 74 * 1024, quarter = 56 * 1024;
+    if (m == 1 && F::BLOCK_BYTES == Q4_0_BYTES) {
+        Plan p4 = make_plan(m, n, k, quarter < smem_optin ? quarter : smem_optin, F::CHUNK_UNITS, F::BLOCK_BYTES,
+                            F::CHUNK_UNITS);
+        if (p4.stages >= 2) {
+            p4.ctas_per_sm = 4;
+            return p4;
+        }
+    }
     Plan p = make_plan(m, n, k, third < smem_optin ? third : smem_optin, F::CHUNK_UNITS, F::BLOCK_BYTES, F::CHUNK_UNITS);
     if (p.stages >= 3) {
         p.ctas_per_sm = 3;
