@@ -194,7 +194,14 @@ struct KqPiece<F, false> {
         if constexpr (F::BYTES == KQ5::BYTES) hv = *reinterpret_cast<const uint2 *>(sb + 16 + l0);
     }
     // value = d * sc * code - dmin * mn: both products exact in f32 (11 + 6 + 5 and 11 + 6
-    // significant bits), their difference rounded once (to odd, then to binary16).
+    // significant bits), their difference rounded once to binary16.  Write a finite binary16
+    // h as M * 2^(E - 25), M < 2048 and E its exponent field (1 for subnormals).  The
+    // difference is then an integer N times 2^(min(Ed, Em) - 25) with
+    // |N| <= 2047 * 63 * 31 * 2^(Ed - min) + 2047 * 63 * 2^(Em - min), below 2^24 whenever
+    // -6 <= Ed - Em <= 2: there it is an f32, one FMA yields it exactly, and its binary16
+    // rounding is the correctly rounded one.  Other superblocks (wider exponent gaps, an
+    // infinite or NaN scale) take the difference rounded to odd first, which gives the same
+    // binary16 whenever both apply.  The choice is per superblock, so uniform over a warp.
     __device__ uint4 packed(int e0) const
     {
         const int u2 = (e0 >> 5) & 1, j = e0 >> 5;
@@ -202,17 +209,36 @@ struct KqPiece<F, false> {
         k4_scale_min(head[1], head[2], head[3], j, sc, mn);
         const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
         const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);
-        uint32_t o[4];
+        uint32_t code[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint32_t code = ((h ? qv.y : qv.x) >> (4 * u2)) & 0x0F0F0F0Fu;
-            if constexpr (F::BYTES == KQ5::BYTES) code |= (((h ? hv.y : hv.x) >> j) & 0x01010101u) << 4;
-            float v[4];
+            code[h] = ((h ? qv.y : qv.x) >> (4 * u2)) & 0x0F0F0F0Fu;
+            if constexpr (F::BYTES == KQ5::BYTES) code[h] |= (((h ? hv.y : hv.x) >> j) & 0x01010101u) << 4;
+        }
+        const int ed = (int)((head[0] >> 10) & 31u), em = (int)((head[0] >> 26) & 31u);
+        const int gap = (ed > 1 ? ed : 1) - (em > 1 ? em : 1);
+        uint32_t o[4];
+        if (ed != 31 && em != 31 && gap <= 2 && gap >= -6) {
+            const float ndmm = -dmm;
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                v[b] = sub_round_odd(__fmul_rn(dsc, __fsub_rn(byte_magic(code, b), 8388608.0f)), dmm);
-            o[2 * h] = pack_h2(v[0], v[1]);
-            o[2 * h + 1] = pack_h2(v[2], v[3]);
+            for (int h = 0; h < 2; ++h) {
+                float v[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    v[b] = __fmaf_rn(dsc, __fsub_rn(byte_magic(code[h], b), 8388608.0f), ndmm);
+                o[2 * h] = pack_h2(v[0], v[1]);
+                o[2 * h + 1] = pack_h2(v[2], v[3]);
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    v[b] = sub_round_odd(__fmul_rn(dsc, __fsub_rn(byte_magic(code[h], b), 8388608.0f)), dmm);
+                o[2 * h] = pack_h2(v[0], v[1]);
+                o[2 * h + 1] = pack_h2(v[2], v[3]);
+            }
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }

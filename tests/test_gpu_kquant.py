@@ -37,6 +37,28 @@ def test_kq_dequant_bit_exact(fmt, n, k):
     assert np.array_equal(w16.view(np.uint16), oracle.dequant_kq_f16(fmt, wb, k))
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_kq_dequant_bit_exact_any_finite_scales(fmt):
+    """Scale fields (d, dmin) drawn from every finite binary16 pattern: both signs, zeros,
+    subnormals, exponent gaps of any width between d and dmin (the mirror takes one exact FMA
+    for close exponents and a rounding to odd otherwise), products beyond the binary16 range."""
+    ensure_built()
+    n, k = 600, 4096
+    nbytes, offsets = inputs.KQUANT_LAYOUT[fmt]
+    wb = inputs.kquant_superblocks(fmt, n, k, seed=9)
+    sb = wb.reshape(-1, nbytes)
+    rng = np.random.default_rng(1234)
+    for off in offsets:
+        bits = rng.integers(0, 65536, size=sb.shape[0]).astype(np.uint32)
+        bits = (bits & 0x83FF) | (rng.integers(0, 31, size=sb.shape[0]).astype(np.uint32) << 10)
+        sb[:, off] = (bits & 0xFF).astype(np.uint8)
+        sb[:, off + 1] = (bits >> 8).astype(np.uint8)
+    wb = sb.reshape(n, -1)
+    w16 = host(q8.dequant_kq_f16(fmt, cuda(wb), n, k))
+    device_ok()
+    assert np.array_equal(w16.view(np.uint16), oracle.dequant_kq_f16(fmt, wb, k))
+
+
 def test_kq_dequant_golden_superblocks():
     """The hand-built superblocks: the GPU mirror carries the hand-worked binary16 values."""
     ensure_built()
