@@ -49,9 +49,18 @@ __device__ __forceinline__ void load_superblock(const uint8_t *p, uint32_t (&w)[
     }
 }
 
+// Unsigned bytes of a times signed bytes of b, summed into c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // The codes of 32-wide block j of a superblock, as 8 words of 4 bytes each (element order),
-// ready for dp4a: Q6_K gives the signed bytes code - 32; Q4_K / Q5_K the unsigned codes.
-template <class F>
+// ready for dp4a: Q6_K gives the signed bytes code - 32 (or, with Q6_UNSIGNED, the codes
+// 0..63 themselves); Q4_K / Q5_K the unsigned codes.
+template <class F, bool Q6_UNSIGNED = false>
 __device__ __forceinline__ void block_codes(const uint32_t (&w)[F::WORDS], int j, uint32_t (&q)[8])
 {
     if constexpr (F::BYTES == KQ6::BYTES) {
@@ -60,7 +69,8 @@ __device__ __forceinline__ void block_codes(const uint32_t (&w)[F::WORDS], int j
         const int s1 = 4 * (g >> 1), s2 = 2 * g;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            q[c] = q6_signed_bytes(((w[qlw + c] >> s1) & 0x0F0F0F0Fu) | (((w[qhw + c] >> s2) & 0x03030303u) << 4));
+            const uint32_t code = ((w[qlw + c] >> s1) & 0x0F0F0F0Fu) | (((w[qhw + c] >> s2) & 0x03030303u) << 4);
+            q[c] = Q6_UNSIGNED ? code : q6_signed_bytes(code);
         }
     } else {
         const int g = j >> 1, u = j & 1;
@@ -381,7 +391,9 @@ KPlan gemv_plan(int64_t m, int64_t n, int64_t k, int sb_bytes, size_t smem_cap, 
     p.nchunks = (n + p.R - 1) / p.R;
     const size_t x_bytes = (size_t)m * p.G * XG_WORDS * 4;
     const size_t xd_bytes = (size_t)m * p.G * XDG_WORDS * 4;
-    const size_t xs_bytes = (size_t)m * p.G * 8 * 4;
+    // per (token, 32-wide block): the quant sum as an f32 (Q4_K / Q5_K), or for Q6_K at m = 1
+    // the two 16-wide halves' sums times -32 as int32
+    const size_t xs_bytes = (size_t)m * p.G * 8 * (sb_bytes == KQ6::BYTES && m == 1 ? 8 : 4);
     const size_t part_bytes = 2 * (size_t)p.U * m * 4;
     const size_t fixed = 16 + x_bytes + xd_bytes + xs_bytes + part_bytes + 2 * KMAX_STAGES * 8 + 64;
     const size_t room = smem_cap > fixed ? smem_cap - fixed : 0;
@@ -416,6 +428,11 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6
     const int tid = threadIdx.x;
     const int G = p.G;
     const int nb = k / QK;
+    // Q6_K at m = 1: the dots take the codes 0..63 as unsigned bytes and start from -32 times
+    // the activation's sum over each 16-wide half, which gives the same integers as the signed
+    // codes - 32 without making them signed word by word (4096 -> 64448: 45.4 -> 42.4 us); with
+    // more tokens the extra per-token load costs more than it saves.
+    constexpr bool Q6U = F::BYTES == KQ6::BYTES && MM == 1;
 
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -444,10 +461,20 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6
         for (int idx = tid; idx < m * G * 8; idx += GV_CONSUMERS) {
             const int tg = idx >> 3, j = idx & 7;
             const uint32_t *xv = xs + tg * XG_WORDS + 8 * j;
-            int sum = 0;
+            if constexpr (Q6U) {
+                int s0 = 0, s1 = 0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) sum = dp4a(0x01010101u, xv[c], sum);
-            xsum[idx] = __int2float_rn(sum);   // |sum| <= 32 * 127: exact
+                for (int c = 0; c < 4; ++c) {
+                    s0 = dp4a(0x01010101u, xv[c], s0);
+                    s1 = dp4a(0x01010101u, xv[4 + c], s1);
+                }
+                reinterpret_cast<int2 *>(xsum)[idx] = make_int2(-32 * s0, -32 * s1);
+            } else {
+                int sum = 0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) sum = dp4a(0x01010101u, xv[c], sum);
+                xsum[idx] = __int2float_rn(sum);   // |sum| <= 32 * 127: exact
+            }
         }
         named_bar_sync(2, GV_CONSUMERS);
     }
@@ -508,7 +535,7 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint32_t q[8];
-                    block_codes<F>(wv, j, q);
+                    block_codes<F, Q6U>(wv, j, q);
                     int sc0 = 0, sc1 = 0;
                     float dsc = 0.0f, dmm = 0.0f;
                     if constexpr (F::BYTES == KQ6::BYTES) {
@@ -526,14 +553,28 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6
                         if (t >= m) break;
                         const uint4 *xv = reinterpret_cast<const uint4 *>(xs + (t * G + g) * XG_WORDS + j * 8);
                         const uint4 a = xv[0], b = xv[1];
-                        int D0 = dp4a(q[0], a.x, 0);
-                        int D1 = dp4a(q[4], b.x, 0);
-                        D0 = dp4a(q[1], a.y, D0);
-                        D1 = dp4a(q[5], b.y, D1);
-                        D0 = dp4a(q[2], a.z, D0);
-                        D1 = dp4a(q[6], b.z, D1);
-                        D0 = dp4a(q[3], a.w, D0);
-                        D1 = dp4a(q[7], b.w, D1);
+                        int D0, D1;
+                        if constexpr (Q6U) {
+                            // sum (code - 32) * x = sum code * x - 32 * sum x, per 16-wide half
+                            const int2 nx = reinterpret_cast<const int2 *>(xsum)[(t * G + g) * 8 + j];
+                            D0 = dp4a_us(q[0], a.x, nx.x);
+                            D1 = dp4a_us(q[4], b.x, nx.y);
+                            D0 = dp4a_us(q[1], a.y, D0);
+                            D1 = dp4a_us(q[5], b.y, D1);
+                            D0 = dp4a_us(q[2], a.z, D0);
+                            D1 = dp4a_us(q[6], b.z, D1);
+                            D0 = dp4a_us(q[3], a.w, D0);
+                            D1 = dp4a_us(q[7], b.w, D1);
+                        } else {
+                            D0 = dp4a(q[0], a.x, 0);
+                            D1 = dp4a(q[4], b.x, 0);
+                            D0 = dp4a(q[1], a.y, D0);
+                            D1 = dp4a(q[5], b.y, D1);
+                            D0 = dp4a(q[2], a.z, D0);
+                            D1 = dp4a(q[6], b.z, D1);
+                            D0 = dp4a(q[3], a.w, D0);
+                            D1 = dp4a(q[7], b.w, D1);
+                        }
                         const float da = xds[(t * G + g) * XDG_WORDS + j];
                         // exact int -> f32 for |D| < 2^22: the bits of D + bits(1.5 * 2^23) are those
                         // of 1.5 * 2^23 + D, and subtracting 1.5 * 2^23 leaves D
