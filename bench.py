@@ -480,7 +480,9 @@ def run_e2e(args, q8, torch, dev, stream):
     every step copies the token's f32 activation in from pinned host memory, the fused decode
     call quantizes it and runs the GEMV, and y is copied back to pinned host memory.
     `weights_each_step`: the same, with all 280.5 MB of weights also copied in from pinned host
-    memory every step (bound by the host link)."""
+    memory every step (bound by the host link).
+    `prefill_gemm`: the fused prefill call (m = 512, 4096 -> 4096) the same way as `e2e`:
+    resident weights, the f32 activation in and y out through pinned host memory every step."""
     from q8_block_quantized_act_gb300 import inputs
     m, n, k = GEMV["m"], GEMV["n"], GEMV["k"]
     w_host = torch.empty((n, row_bytes(k)), dtype=torch.uint8).pin_memory()
@@ -521,7 +523,31 @@ def run_e2e(args, q8, torch, dev, stream):
     w_dev.copy_(w_host)            # load time: the weights stay resident from here on
     torch.cuda.synchronize()
     ms_res = timed(resident, max(10, min(args.steps, 200)))
+
+    # The prefill call the same way: resident Q8_0 weights, every step copies the f32 activation
+    # in from pinned host memory, makes the fused GEMM call (q8_1 quantize + GEMM) and copies y out.
+    gm, gn, gk = GEMM["m"], GEMM["n"], GEMM["k"]
+    wg_dev = q8.quantize_q8_0(torch.from_numpy(inputs.weights_f32(gn, gk)).to(dev))
+    xg_host = torch.from_numpy(inputs.activations_f32(gm, gk)).pin_memory()
+    yg_host = torch.empty((gm, gn), dtype=torch.float32).pin_memory()
+    xg_dev = torch.empty_like(xg_host, device=dev)
+    yg_dev = torch.empty((gm, gn), dtype=torch.float32, device=dev)
+    wsg = q8.gemm_workspace(gm, gk, dev)
+
+    def prefill():
+        xg_dev.copy_(xg_host, non_blocking=True)
+        q8.check(q8.q8act_gemm_q8_0(wg_dev, xg_dev, yg_dev, gm, gn, gk, wsg, wsg.numel(), stream))
+        yg_host.copy_(yg_dev, non_blocking=True)
+
+    ms_pf = timed(prefill, max(10, min(args.steps, 100)))
+    prefill_gemm = {"value": round(2.0 * gm * gn * gk / (ms_pf * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(xg_host.numel() * 4), "d2h_bytes_per_step": int(yg_host.numel() * 4),
+                    "ms_per_step": round(ms_pf, 4),
+                    "what": f"fused prefill call (q8_1 quantize + GEMM, m={gm}, {gk}->{gn}) through the C ABI; "
+                            "weights resident; every step copies x in from pinned host memory and y out to pinned "
+                            "host memory"}
     return {"value": round(gemv_bytes(m, n, k) / (ms_res * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "prefill_gemm": prefill_gemm,
             "h2d_bytes_per_step": int(x_host.numel() * 4),
             "d2h_bytes_per_step": int(y_host.numel() * 4), "ms_per_step": round(ms_res, 4),
             "what": "fused decode call (q8_1 quantize + GEMV, m=1, 4096->64448) through the C ABI; weights "
