@@ -12,7 +12,7 @@
 // Per (row, token) the fold is the dp4a K-quant kernel's, operation for operation: per
 // superblock acc = 0, then over its 8 sub-blocks in order
 //   Q6_K:         acc = fma(d * d_a, E, acc)
-//   Q4_K / Q5_K:  acc = fma(d_a, d*sc*D - dmin*mn*X, acc)   (X: the activation block's quant sum)
+//   Q4_K / Q5_K:  acc = fma(d_a, fma(d*sc, D, -(dmin*mn*X)), acc)   (X: the activation block's quant sum)
 // and the superblock sums of a row combined by the same fixed tree (pairwise when the
 // superblock count divides 32, else left to right).  Token t's result is therefore bitwise
 // the same for every m, and the same as the m = 1 kernel's (the pages' decode == verify law).
@@ -383,10 +383,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float dsc0 = __fmul_rn(d0, (float)sc0), dmm0 = __fmul_rn(dmin0, (float)mn0);   // exact
                         const float dsc1 = __fmul_rn(d1, (float)sc1), dmm1 = __fmul_rn(dmin1, (float)mn1);
                         const float2 X = *reinterpret_cast<const float2 *>(xsum + b * 8 + 2 * c);
-                        const float v0 = __fsub_rn(__fmul_rn(dsc0, Ef[0]), __fmul_rn(dmm0, X.x));
-                        const float v1 = __fsub_rn(__fmul_rn(dsc0, Ef[1]), __fmul_rn(dmm0, X.y));
-                        const float v2 = __fsub_rn(__fmul_rn(dsc1, Ef[2]), __fmul_rn(dmm1, X.x));
-                        const float v3 = __fsub_rn(__fmul_rn(dsc1, Ef[3]), __fmul_rn(dmm1, X.y));
+                        const float v0 = __fmaf_rn(dsc0, Ef[0], -__fmul_rn(dmm0, X.x));
+                        const float v1 = __fmaf_rn(dsc0, Ef[1], -__fmul_rn(dmm0, X.y));
+                        const float v2 = __fmaf_rn(dsc1, Ef[2], -__fmul_rn(dmm1, X.x));
+                        const float v3 = __fmaf_rn(dsc1, Ef[3], -__fmul_rn(dmm1, X.y));
                         acc[q][0] = __fmaf_rn(da.x, v0, acc[q][0]);
                         acc[q][1] = __fmaf_rn(da.y, v1, acc[q][1]);
                         acc[q][2] = __fmaf_rn(da.x, v2, acc[q][2]);

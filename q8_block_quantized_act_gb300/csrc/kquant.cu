@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6
                                 dots[((int64_t)t * n + row0 + row) * nb + g * 8 + j] = D;
                             } else {
                                 const float X = xsum[(t * G + g) * 8 + j];
-                                const float v = __fsub_rn(__fmul_rn(dsc, exact_f(D)), __fmul_rn(dmm, X));
+                                const float v = __fmaf_rn(dsc, exact_f(D), -__fmul_rn(dmm, X));
                                 acc[t] = __fmaf_rn(da, v, acc[t]);
                             }
                         }
