@@ -309,19 +309,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint8_t *sb0 = stage + (size_t)(16 * rt + gl) * p.rs + (size_t)g * F::BYTES;
             const uint8_t *sb1 = sb0 + (size_t)8 * p.rs;
             float d0, d1, dmin0 = 0.0f, dmin1 = 0.0f;
-            uint32_t h0[4] = {0u, 0u, 0u, 0u}, h1[4] = {0u, 0u, 0u, 0u};
+            // Q4_K / Q5_K: each row's 8 scales and mins, four to a word (scales of sub-blocks
+            // 0..3, mins 0..3, scales 4..7, mins 4..7)
+            uint32_t s0[4] = {0u, 0u, 0u, 0u}, s1[4] = {0u, 0u, 0u, 0u};
             if constexpr (F::Q6) {
                 d0 = half_bits_to_float(lds16(sb0 + 208));
                 d1 = half_bits_to_float(lds16(sb1 + 208));
             } else {
                 const uint4 a = *reinterpret_cast<const uint4 *>(sb0);
                 const uint4 b = *reinterpret_cast<const uint4 *>(sb1);
-                h0[0] = a.x; h0[1] = a.y; h0[2] = a.z; h0[3] = a.w;
-                h1[0] = b.x; h1[1] = b.y; h1[2] = b.z; h1[3] = b.w;
-                d0 = half_bits_to_float(h0[0] & 0xffffu);
-                dmin0 = half_bits_to_float(h0[0] >> 16);
-                d1 = half_bits_to_float(h1[0] & 0xffffu);
-                dmin1 = half_bits_to_float(h1[0] >> 16);
+                d0 = half_bits_to_float(a.x & 0xffffu);
+                dmin0 = half_bits_to_float(a.x >> 16);
+                d1 = half_bits_to_float(b.x & 0xffffu);
+                dmin1 = half_bits_to_float(b.x >> 16);
+                k4_scales_mins(a.y, a.z, a.w, s0[0], s0[1], s0[2], s0[3]);
+                k4_scales_mins(b.y, b.z, b.w, s1[0], s1[1], s1[2], s1[3]);
             }
             auto fold_superblock = [&](auto aligned) {
                 constexpr bool AL = decltype(aligned)::value;
@@ -377,11 +379,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         acc[q][2] = __fmaf_rn(s10, Ef[2], acc[q][2]);
                         acc[q][3] = __fmaf_rn(s11, Ef[3], acc[q][3]);
                     } else {
-                        int sc0, mn0, sc1, mn1;
-                        k4_scale_min(h0[1], h0[2], h0[3], j, sc0, mn0);
-                        k4_scale_min(h1[1], h1[2], h1[3], j, sc1, mn1);
-                        const float dsc0 = __fmul_rn(d0, (float)sc0), dmm0 = __fmul_rn(dmin0, (float)mn0);   // exact
-                        const float dsc1 = __fmul_rn(d1, (float)sc1), dmm1 = __fmul_rn(dmin1, (float)mn1);
+                        // the 6-bit scale and min as exact f32 (byte under 2^23, one exact subtraction)
+                        const int hi = j < 4 ? 0 : 2;
+                        const float sc0 = __fsub_rn(byte_magic(s0[hi], j & 3), 8388608.0f);
+                        const float mn0 = __fsub_rn(byte_magic(s0[hi + 1], j & 3), 8388608.0f);
+                        const float sc1 = __fsub_rn(byte_magic(s1[hi], j & 3), 8388608.0f);
+                        const float mn1 = __fsub_rn(byte_magic(s1[hi + 1], j & 3), 8388608.0f);
+                        const float dsc0 = __fmul_rn(d0, sc0), dmm0 = __fmul_rn(dmin0, mn0);   // exact
+                        const float dsc1 = __fmul_rn(d1, sc1), dmm1 = __fmul_rn(dmin1, mn1);
                         const float2 X = *reinterpret_cast<const float2 *>(xsum + b * 8 + 2 * c);
                         const float v0 = __fmaf_rn(dsc0, Ef[0], -__fmul_rn(dmm0, X.x));
                         const float v1 = __fmaf_rn(dsc0, Ef[1], -__fmul_rn(dmm0, X.y));

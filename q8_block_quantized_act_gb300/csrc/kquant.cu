@@ -133,12 +133,6 @@ __device__ __forceinline__ float sub_round_odd(float a, float b)
     return __uint_as_float((z & ~1u) | (t & 1u));
 }
 
-// Byte b (0..3) of w as the f32 value 2^23 + byte: the byte placed under the exponent of 2^23.
-__device__ __forceinline__ float byte_magic(uint32_t w, int b)
-{
-    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u + (uint32_t)b));
-}
-
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -527,10 +521,7 @@ __global__ void __launch_bounds__(GV_CONSUMERS + 32, (MM <= 1 && F::BYTES != KQ6
                 } else {
                     d = half_bits_to_float(wv[0] & 0xffffu);
                     dmin = half_bits_to_float(wv[0] >> 16);
-                    sc_lo = wv[1] & 0x3F3F3F3Fu;
-                    mn_lo = wv[2] & 0x3F3F3F3Fu;
-                    sc_hi = (wv[3] & 0x0F0F0F0Fu) | ((wv[1] >> 2) & 0x30303030u);
-                    mn_hi = ((wv[3] >> 4) & 0x0F0F0F0Fu) | ((wv[2] >> 2) & 0x30303030u);
+                    k4_scales_mins(wv[1], wv[2], wv[3], sc_lo, mn_lo, sc_hi, mn_hi);
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {

@@ -49,6 +49,24 @@ __device__ __forceinline__ void k4_scale_min(uint32_t w1, uint32_t w2, uint32_t 
     }
 }
 
+// The 6-bit scales and mins of all 8 sub-blocks of a Q4_K / Q5_K superblock, four to a word
+// (byte j & 3 of the word for sub-block j; scales of sub-blocks 0..3 in sc_lo, 4..7 in sc_hi),
+// unpacked from the 12 scale bytes (words w1..w3) with word-wide masks.
+__device__ __forceinline__ void k4_scales_mins(uint32_t w1, uint32_t w2, uint32_t w3, uint32_t &sc_lo, uint32_t &mn_lo,
+                                               uint32_t &sc_hi, uint32_t &mn_hi)
+{
+    sc_lo = w1 & 0x3F3F3F3Fu;
+    mn_lo = w2 & 0x3F3F3F3Fu;
+    sc_hi = (w3 & 0x0F0F0F0Fu) | ((w1 >> 2) & 0x30303030u);
+    mn_hi = ((w3 >> 4) & 0x0F0F0F0Fu) | ((w2 >> 2) & 0x30303030u);
+}
+
+// Byte b (0..3) of w as the f32 value 2^23 + byte: the byte placed under the exponent of 2^23.
+__device__ __forceinline__ float byte_magic(uint32_t w, int b)
+{
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u + (uint32_t)b));
+}
+
 // Four 6-bit Q6_K codes (one per byte) as the signed bytes code - 32: flip bit 5; where it is
 // now set (code < 32) the byte is code + 32 and must become code + 32 - 64, i.e. gain bits 6
 // and 7.
