@@ -199,8 +199,9 @@ struct KqPiece<F, false> {
     }
     // value = d * sc * code - dmin * mn: both products exact in f32 (11 + 6 + 5 and 11 + 6
     // significant bits), their difference rounded once to binary16.  Write a finite binary16
-    // h as M * 2^(E - 25), M < 2048 and E its exponent field (1 for subnormals).  The
-    // difference is then an integer N times 2^(min(Ed, Em) - 25) with
+    // h as M * 2^(E - 25) with M < 2048 and E its exponent field as stored (a subnormal,
+    // M' * 2^-24 with M' < 1024, is 2M' * 2^(0 - 25)).  The difference is then an integer N
+    // times 2^(min(Ed, Em) - 25) with
     // |N| <= 2047 * 63 * 31 * 2^(Ed - min) + 2047 * 63 * 2^(Em - min), below 2^24 whenever
     // -6 <= Ed - Em <= 2: there it is an f32, one FMA yields it exactly, and its binary16
     // rounding is the correctly rounded one.  Other superblocks (wider exponent gaps, an
@@ -209,10 +210,12 @@ struct KqPiece<F, false> {
     __device__ uint4 packed(int e0) const
     {
         const int u2 = (e0 >> 5) & 1, j = e0 >> 5;
-        int sc, mn;
-        k4_scale_min(head[1], head[2], head[3], j, sc, mn);
+        uint32_t sc_lo, mn_lo, sc_hi, mn_hi;
+        k4_scales_mins(head[1], head[2], head[3], sc_lo, mn_lo, sc_hi, mn_hi);
+        const float scf = __fsub_rn(byte_magic(j < 4 ? sc_lo : sc_hi, j & 3), 8388608.0f);
+        const float mnf = __fsub_rn(byte_magic(j < 4 ? mn_lo : mn_hi, j & 3), 8388608.0f);
         const float d = half_bits_to_float(head[0] & 0xffffu), dmin = half_bits_to_float(head[0] >> 16);
-        const float dsc = __fmul_rn(d, (float)sc), dmm = __fmul_rn(dmin, (float)mn);
+        const float dsc = __fmul_rn(d, scf), dmm = __fmul_rn(dmin, mnf);
         uint32_t code[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -220,9 +223,8 @@ struct KqPiece<F, false> {
             if constexpr (F::BYTES == KQ5::BYTES) code[h] |= (((h ? hv.y : hv.x) >> j) & 0x01010101u) << 4;
         }
         const int ed = (int)((head[0] >> 10) & 31u), em = (int)((head[0] >> 26) & 31u);
-        const int gap = (ed > 1 ? ed : 1) - (em > 1 ? em : 1);
         uint32_t o[4];
-        if (ed != 31 && em != 31 && gap <= 2 && gap >= -6) {
+        if (ed != 31 && em != 31 && (uint32_t)(ed - em + 6) <= 8u) {
             const float ndmm = -dmm;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {

@@ -31,24 +31,6 @@ struct KQ5 {
     static constexpr int WORDS = 44;
 };
 
-// The 6-bit scale and min of sub-block j of a Q4_K / Q5_K superblock from its 12 scale bytes,
-// words w1..w3 (bytes 4..15 of the superblock).  Selects rather than an indexed register array,
-// so that a run-time j stays in registers.
-__device__ __forceinline__ void k4_scale_min(uint32_t w1, uint32_t w2, uint32_t w3, int j, int &sc, int &mn)
-{
-    auto b = [&](int i) {
-        const uint32_t x = i < 4 ? w1 : (i < 8 ? w2 : w3);
-        return (int)((x >> (8 * (i & 3))) & 0xFFu);
-    };
-    if (j < 4) {
-        sc = b(j) & 63;
-        mn = b(j + 4) & 63;
-    } else {
-        sc = (b(j + 4) & 15) | ((b(j - 4) >> 6) << 4);
-        mn = (b(j + 4) >> 4) | ((b(j) >> 6) << 4);
-    }
-}
-
 // The 6-bit scales and mins of all 8 sub-blocks of a Q4_K / Q5_K superblock, four to a word
 // (byte j & 3 of the word for sub-block j; scales of sub-blocks 0..3 in sc_lo, 4..7 in sc_hi),
 // unpacked from the 12 scale bytes (words w1..w3) with word-wide masks.
